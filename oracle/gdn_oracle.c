@@ -1,0 +1,281 @@
+/*
+ * Gated DeltaNet recurrence: CPU oracle in fp64.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously correct
+ * statement of what the GPU library computes.  Only the test-suite, the
+ * smoke check and the CPU-baseline leg of the benchmark load it; the product
+ * path never does.  It shares no code, header or constant with the CUDA
+ * library.
+ *
+ * Source of the method: "Optimizing on-device inference for Apple Silicon"
+ * (Perplexity blog), section "Qwen creates three workload shapes": each Gated
+ * DeltaNet layer squeezes history into a fixed-size recurrent state; a learned
+ * gate decides how much of the old state is kept and a delta update writes
+ * the current token in, token after token.  The same section says prefill may
+ * evaluate this either by scanning tokens or by regrouping the updates into
+ * blocks.  Section "Keep recurrent state on chip" fixes the state (and its
+ * gate) as fp32 on the device; this oracle carries it in fp64.
+ *
+ * Per sequence n and value head h, with S (dv x dk) starting at init_state
+ * (or zero), for each token t:
+ *     alpha_t = exp(log_alpha_t)
+ *     S <- alpha_t * S * (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t  = S q_t                                   (post-update state)
+ * and final_state = S after the last token.  The sequential scan below uses
+ * the algebraically identical expanded form
+ *     S <- alpha_t S + beta_t (v_t - alpha_t S k_t) k_t^T .
+ * Value head h reads query/key head h / (hv / hk).
+ *
+ * Layouts (row-major): q,k [T, hk, dk]; v [T, hv, dv]; log_alpha, beta
+ * [T, hv]; state [n_seqs, hv, dv, dk] (row = value index); out [T, hv, dv].
+ * cu_seqlens [n_seqs + 1] holds token offsets of the packed sequences.
+ *
+ * Return value: 0 on success, a negative number for invalid arguments.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static int check_common(int n_seqs, const int32_t *cu, int hk, int hv, int dk, int dv)
+{
+    if (n_seqs < 0 || hk <= 0 || hv <= 0 || dk <= 0 || dv <= 0) return -1;
+    if (hv % hk != 0) return -2;
+    if (n_seqs > 0 && cu == NULL) return -3;
+    for (int n = 0; n < n_seqs; ++n)
+        if (cu[n + 1] < cu[n]) return -4;
+    return 0;
+}
+
+/* One token of the recurrence on one (sequence, head) state, fp64. */
+static void token_update(double *S, int dk, int dv, const float *q, const float *k,
+                         const float *v, double log_alpha, double beta, double *o,
+                         double *sk)
+{
+    const double alpha = exp(log_alpha);   /* log_alpha = -inf gives alpha = 0 */
+    for (int i = 0; i < dv; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * (double)k[j];
+        sk[i] = acc;
+    }
+    for (int i = 0; i < dv; ++i) {
+        const double u = beta * ((double)v[i] - alpha * sk[i]);
+        for (int j = 0; j < dk; ++j)
+            S[(size_t)i * dk + j] = alpha * S[(size_t)i * dk + j] + u * (double)k[j];
+    }
+    for (int i = 0; i < dv; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * (double)q[j];
+        o[i] = acc;
+    }
+}
+
+int gdn_oracle_prefill(int n_seqs, const int32_t *cu_seqlens, int hk, int hv, int dk, int dv,
+                       const float *q, const float *k, const float *v,
+                       const float *log_alpha, const float *beta,
+                       const double *init_state, double *out, double *final_state,
+                       int n_threads)
+{
+    int rc = check_common(n_seqs, cu_seqlens, hk, hv, dk, dv);
+    if (rc) return rc;
+    const int group = hv / hk;
+    const long n_units = (long)n_seqs * hv;
+    if (n_threads <= 0) n_threads = 1;
+    int failed = 0;
+
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
+    for (long unit = 0; unit < n_units; ++unit) {
+        const int n = (int)(unit / hv), h = (int)(unit % hv), hq = h / group;
+        double *S = (double *)malloc(sizeof(double) * ((size_t)dv * dk + 2 * (size_t)dv));
+        if (!S) { failed = 1; continue; }
+        double *sk = S + (size_t)dv * dk, *o = sk + dv;
+        const size_t soff = ((size_t)n * hv + h) * dv * dk;
+        if (init_state) memcpy(S, init_state + soff, sizeof(double) * dv * dk);
+        else memset(S, 0, sizeof(double) * dv * dk);
+        for (int t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
+            token_update(S, dk, dv, q + ((size_t)t * hk + hq) * dk, k + ((size_t)t * hk + hq) * dk,
+                         v + ((size_t)t * hv + h) * dv, log_alpha[(size_t)t * hv + h],
+                         beta[(size_t)t * hv + h], o, sk);
+            if (out) memcpy(out + ((size_t)t * hv + h) * dv, o, sizeof(double) * dv);
+        }
+        if (final_state) memcpy(final_state + soff, S, sizeof(double) * dv * dk);
+        free(S);
+    }
+    return failed ? -10 : 0;
+}
+
+/*
+ * One decode step: the same token update applied to n independent states
+ * (a batch of one token each), in place.  q,k [n, hk, dk]; v [n, hv, dv];
+ * log_alpha, beta [n, hv]; state [n, hv, dv, dk]; out [n, hv, dv].
+ */
+int gdn_oracle_decode_step(int n, int hk, int hv, int dk, int dv, double *state,
+                           const float *q, const float *k, const float *v,
+                           const float *log_alpha, const float *beta, double *out,
+                           int n_threads)
+{
+    if (n < 0 || hk <= 0 || hv <= 0 || dk <= 0 || dv <= 0 || hv % hk) return -1;
+    const int group = hv / hk;
+    const long n_units = (long)n * hv;
+    if (n_threads <= 0) n_threads = 1;
+    int failed = 0;
+#pragma omp parallel for schedule(static) num_threads(n_threads)
+    for (long unit = 0; unit < n_units; ++unit) {
+        const int b = (int)(unit / hv), h = (int)(unit % hv), hq = h / group;
+        double *tmp = (double *)malloc(sizeof(double) * 2 * (size_t)dv);
+        if (!tmp) { failed = 1; continue; }
+        double *S = state + ((size_t)b * hv + h) * dv * dk;
+        token_update(S, dk, dv, q + ((size_t)b * hk + hq) * dk, k + ((size_t)b * hk + hq) * dk,
+                     v + ((size_t)b * hv + h) * dv, log_alpha[(size_t)b * hv + h],
+                     beta[(size_t)b * hv + h], tmp + dv, tmp);
+        if (out) memcpy(out + ((size_t)b * hv + h) * dv, tmp + dv, sizeof(double) * dv);
+        free(tmp);
+    }
+    return failed ? -10 : 0;
+}
+
+/*
+ * The blocked ("chunked") evaluation of the same recurrence, in fp64, used
+ * only to pin the two readings of the method against each other.
+ *
+ * The pages say the updates may be regrouped into blocks that expose matrix
+ * work ("Qwen creates three workload shapes") but print no algorithm; this is
+ * our derivation.  Inside a chunk of L tokens with local index i and the
+ * running log-decay g_i = sum_{j<=i} log_alpha_j, unrolling the recurrence
+ * gives S_i = e^{g_i} S0 + sum_{j<=i} e^{g_i-g_j} u_j k_j^T, where u_j are the
+ * per-token delta vectors.  Substituting into u_i = beta_i (v_i - alpha_i
+ * S_{i-1} k_i) yields the unit lower-triangular system
+ *     (I + A) U = diag(beta) V - diag(beta e^g) K S0^T,
+ *     A_ij = beta_i e^{g_i - g_j} k_i.k_j   (j < i),
+ * solved here as U = Ut - W S0^T with T = (I + A)^-1 (forward substitution),
+ * W = T diag(beta e^g) K and Ut = T diag(beta) V.  Then
+ *     O   = diag(e^g) Q S0^T + (M o Q K^T) U,  M_ij = e^{g_i - g_j} (j <= i)
+ *     S_L = e^{g_L} S0 + U^T diag(e^{g_L - g_j}) K .
+ * Decay factors are always exponentials of differences g_i - g_j <= 0.
+ * The chunk never straddles a sequence boundary; a sequence's last chunk may
+ * be shorter than `chunk`.  Gates must be finite here.
+ */
+int gdn_oracle_prefill_chunked(int n_seqs, const int32_t *cu_seqlens, int hk, int hv, int dk,
+                               int dv, const float *q, const float *k, const float *v,
+                               const float *log_alpha, const float *beta,
+                               const double *init_state, double *out, double *final_state,
+                               int chunk, int n_threads)
+{
+    int rc = check_common(n_seqs, cu_seqlens, hk, hv, dk, dv);
+    if (rc) return rc;
+    if (chunk <= 0) return -5;
+    const int group = hv / hk;
+    const long n_units = (long)n_seqs * hv;
+    const int C = chunk;
+    if (n_threads <= 0) n_threads = 1;
+    int failed = 0;
+
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
+    for (long unit = 0; unit < n_units; ++unit) {
+        const int n = (int)(unit / hv), h = (int)(unit % hv), hq = h / group;
+        const size_t nS = (size_t)dv * dk;
+        /* S, Snew, g, A, T, W, Ut, U, Kc, Qc, Vc, tmp */
+        size_t need = 2 * nS + C + 2 * (size_t)C * C + (size_t)C * dk * 3 + (size_t)C * dv * 3;
+        double *mem = (double *)malloc(sizeof(double) * need);
+        if (!mem) { failed = 1; continue; }
+        double *S = mem, *Sn = S + nS, *g = Sn + nS, *A = g + C, *Tm = A + (size_t)C * C;
+        double *W = Tm + (size_t)C * C, *Kc = W + (size_t)C * dk, *Qc = Kc + (size_t)C * dk;
+        double *Ut = Qc + (size_t)C * dk, *U = Ut + (size_t)C * dv, *Vc = U + (size_t)C * dv;
+        const size_t soff = ((size_t)n * hv + h) * nS;
+        if (init_state) memcpy(S, init_state + soff, sizeof(double) * nS);
+        else memset(S, 0, sizeof(double) * nS);
+
+        for (int t0 = cu_seqlens[n]; t0 < cu_seqlens[n + 1]; t0 += C) {
+            const int L = (cu_seqlens[n + 1] - t0 < C) ? cu_seqlens[n + 1] - t0 : C;
+            double bet[L > 0 ? L : 1];
+            for (int i = 0; i < L; ++i) {
+                const size_t t = (size_t)t0 + i;
+                for (int j = 0; j < dk; ++j) {
+                    Kc[(size_t)i * dk + j] = k[(t * hk + hq) * dk + j];
+                    Qc[(size_t)i * dk + j] = q[(t * hk + hq) * dk + j];
+                }
+                for (int j = 0; j < dv; ++j) Vc[(size_t)i * dv + j] = v[(t * hv + h) * dv + j];
+                g[i] = (i ? g[i - 1] : 0.0) + (double)log_alpha[t * hv + h];
+                bet[i] = beta[t * hv + h];
+            }
+            /* A (strictly lower) */
+            for (int i = 0; i < L; ++i)
+                for (int j = 0; j < L; ++j) {
+                    double a = 0.0;
+                    if (j < i) {
+                        double kk = 0.0;
+                        for (int d = 0; d < dk; ++d) kk += Kc[(size_t)i * dk + d] * Kc[(size_t)j * dk + d];
+                        a = bet[i] * exp(g[i] - g[j]) * kk;
+                    }
+                    A[(size_t)i * L + j] = a;
+                }
+            /* T = (I + A)^-1 by forward substitution, one column at a time */
+            for (int c = 0; c < L; ++c)
+                for (int i = 0; i < L; ++i) {
+                    double x = (i == c) ? 1.0 : 0.0;
+                    for (int j = 0; j < i; ++j) x -= A[(size_t)i * L + j] * Tm[(size_t)j * L + c];
+                    Tm[(size_t)i * L + c] = x;
+                }
+            /* W = T diag(beta e^g) K ; Ut = T diag(beta) V */
+            for (int i = 0; i < L; ++i) {
+                for (int d = 0; d < dk; ++d) {
+                    double acc = 0.0;
+                    for (int j = 0; j < L; ++j)
+                        acc += Tm[(size_t)i * L + j] * bet[j] * exp(g[j]) * Kc[(size_t)j * dk + d];
+                    W[(size_t)i * dk + d] = acc;
+                }
+                for (int d = 0; d < dv; ++d) {
+                    double acc = 0.0;
+                    for (int j = 0; j < L; ++j) acc += Tm[(size_t)i * L + j] * bet[j] * Vc[(size_t)j * dv + d];
+                    Ut[(size_t)i * dv + d] = acc;
+                }
+            }
+            /* U = Ut - W S0^T */
+            for (int i = 0; i < L; ++i)
+                for (int e = 0; e < dv; ++e) {
+                    double acc = 0.0;
+                    for (int d = 0; d < dk; ++d) acc += W[(size_t)i * dk + d] * S[(size_t)e * dk + d];
+                    U[(size_t)i * dv + e] = Ut[(size_t)i * dv + e] - acc;
+                }
+            /* O = diag(e^g) Q S0^T + (M o Q K^T) U */
+            if (out)
+                for (int i = 0; i < L; ++i)
+                    for (int e = 0; e < dv; ++e) {
+                        double acc = 0.0;
+                        for (int d = 0; d < dk; ++d) acc += Qc[(size_t)i * dk + d] * S[(size_t)e * dk + d];
+                        acc *= exp(g[i]);
+                        for (int j = 0; j <= i; ++j) {
+                            double qk = 0.0;
+                            for (int d = 0; d < dk; ++d) qk += Qc[(size_t)i * dk + d] * Kc[(size_t)j * dk + d];
+                            acc += exp(g[i] - g[j]) * qk * U[(size_t)j * dv + e];
+                        }
+                        out[(((size_t)t0 + i) * hv + h) * dv + e] = acc;
+                    }
+            /* S_L = e^{g_L} S0 + U^T diag(e^{g_L - g}) K */
+            const double gl = g[L - 1];
+            for (int e = 0; e < dv; ++e)
+                for (int d = 0; d < dk; ++d) {
+                    double acc = exp(gl) * S[(size_t)e * dk + d];
+                    for (int j = 0; j < L; ++j)
+                        acc += U[(size_t)j * dv + e] * exp(gl - g[j]) * Kc[(size_t)j * dk + d];
+                    Sn[(size_t)e * dk + d] = acc;
+                }
+            memcpy(S, Sn, sizeof(double) * nS);
+        }
+        if (final_state) memcpy(final_state + soff, S, sizeof(double) * nS);
+        free(mem);
+    }
+    return failed ? -10 : 0;
+}
+
+int gdn_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
