@@ -1,0 +1,464 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 Gated DeltaNet hot path.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+One step is one single-layer prefill of the 4096-token workload (16 q/k heads,
+32 value heads, d = 128, chunk 64) through the chunked tcgen05 path: the
+per-chunk preparation kernel followed by the state-passing kernel.  `value`
+is prefill tokens/s over all ranks, device-timed with CUDA events over exactly
+K back-to-back steps whose inputs are already in HBM.  Input replicas are
+rotated so that the data each step reads (about 4 x 97 MiB in total) does not
+sit in the 126 MiB L2 from the previous step.
+
+Also measured and reported on the same line:
+  * per-kernel CUDA-event durations inside the timed region and the roofline
+    of the dominant kernel (algorithmic FLOPs / duration against the measured
+    bf16 tensor peak);
+  * the 30-layer batch-1 decode step (us per step and HBM GB/s of the state
+    read+write, rotating 5 replicas of the 60 MiB state);
+  * the direct-scan prefill on the same 4K workload (the scan vs. blocks
+    comparison);
+  * e2e: the same prefill metric through the public call with host buffers
+    (pinned host -> device copies of the inputs and device -> host copies of
+    the outputs and final state inside the timed region);
+  * cpu_baseline: the fp64 CPU oracle timed on this host's cores;
+  * SM clocks sampled with nvidia-smi while the GPU is under load.
+
+--impl reference times the CPU oracle (the only reference this method has) on
+the same workload, metric and unit.  Multi-GPU runs (torchrun) run independent
+replicas of the workload on every rank (no collective on the data path) and
+report the aggregate over ranks with max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tok/s @4K; decode step µs (30 layers); % tensor/HBM roofline"
+UNIT = "tok/s"
+T_TOKENS = 4096
+HK, HV, D, C = 16, 32, 128, 64
+WORKLOAD = ("single-layer Gated DeltaNet prefill, 1 sequence x 4096 tokens, 16 q/k heads, 32 v heads, "
+            "dk=dv=128, chunk 64, bf16 q/k/v, fp32 gates and state, bf16 out")
+
+# Algorithmic work per token per value head (dense-equivalent, no split-precision passes):
+#   preparation: K K^T and Q K^T (4 C d) + triangular solve (C^2 / 3) + P = K^T Gamma T (2 d C) + R = Aqk T (2 C^2)
+#   state pass:  Q S^T and K S^T (4 d^2) + P X (2 d^2) + R X (2 C d)
+FLOPS_PREP = 4 * C * D + C * C / 3 + 2 * D * C + 2 * C * C
+FLOPS_PASS = 4 * D * D + 2 * D * D + 2 * C * D
+FLOPS_SCAN = 6 * D * D
+DECODE_LAYERS = 30
+DECODE_STATE_BYTES = DECODE_LAYERS * HV * D * D * 4 * 2   # fp32 state read + written per 30-layer step
+
+
+# --------------------------------------------------------------------------- distributed helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def aggregate(local_seconds: float, local_units: float, group=None):
+    """Max of the timed seconds and sum of the units over all ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return local_seconds, local_units
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- peaks and clocks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks, power and throttle reasons every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="gdn_clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            if self.path:
+                try:
+                    os.unlink(self.path)
+                except OSError:
+                    pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        loaded = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in loaded if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i in range(4) if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": reasons, "samples": len(rows),
+                "samples_under_load": len(loaded),
+                "power_w_max": max((num(r[3]) or 0) for r in loaded)}
+
+
+# --------------------------------------------------------------------------- workloads
+def make_prefill_replicas(n_rep: int, dev):
+    import torch
+    from gated_deltanet_linear_03_gb300 import gdn, synth
+    inp = synth.prefill_4k()
+    cu_host = inp.cu_seqlens.tolist()
+    host = {"q": inp.q, "k": inp.k, "v": inp.v, "la": inp.log_alpha, "b": inp.beta, "cu": inp.cu_seqlens}
+    base = {k: v.to(dev) for k, v in host.items()}
+    ws_bytes = gdn.workspace_size(1, T_TOKENS, HK, HV, D, D, cu_host, "chunked")
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)       # one workspace, reused every step
+    plans = []
+    for r in range(n_rep):
+        t = base if r == 0 else {k: v.clone() for k, v in base.items()}
+        plans.append(gdn.PrefillPlan(t["q"], t["k"], t["v"], t["la"], t["b"], t["cu"], workspace=ws,
+                                     cu_seqlens_host=cu_host))
+    return inp, host, plans, cu_host
+
+
+def time_prefill_steps(plans, steps, warmup, stream):
+    """Exactly `steps` prefill steps; per-step events split the two kernels."""
+    import torch
+    R = len(plans)
+    for i in range(warmup):
+        plans[i % R].run(stream=stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            p = plans[i % R]
+            ev[i][0].record(stream)
+            p.run_phase("prep", stream=stream)
+            ev[i][1].record(stream)
+            p.run_phase("pass", stream=stream)
+            ev[i][2].record(stream)
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    prep = [e[0].elapsed_time(e[1]) for e in ev]
+    pas = [e[1].elapsed_time(e[2]) for e in ev]
+    return total_ms, statistics.mean(prep), statistics.mean(pas)
+
+
+def soak(fn, seconds: float):
+    import torch
+    t0 = time.time()
+    while time.time() - t0 < seconds:
+        for _ in range(20):
+            fn()
+        torch.cuda.synchronize()
+
+
+def time_decode(dev, stream, steps=256, n_rep=5):
+    import torch
+    from gated_deltanet_linear_03_gb300 import gdn, synth
+    di = synth.decode_30(steps=steps)
+    states = [di.state.to(dev) for _ in range(n_rep)]
+    q, k, v = di.q.to(dev), di.k.to(dev), di.v.to(dev)
+    la, b = di.log_alpha.to(dev), di.beta.to(dev)
+    out = torch.empty(DECODE_LAYERS, HV, D, dtype=torch.bfloat16, device=dev)
+
+    def step(i):
+        gdn.decode_step(states[i % n_rep], q[i], k[i], v[i], la[i], b[i], out=out, stream=stream)
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            step(i)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for i in range(steps):
+            step(i)
+        e.record(stream)
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) * 1e3 / steps
+    return us
+
+
+def time_scan(plan_scan, stream, iters=5):
+    import torch
+    with torch.cuda.stream(stream):
+        plan_scan.run(stream=stream)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(iters):
+            plan_scan.run(stream=stream)
+        e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def time_e2e(host, cu_host, dev, stream, steps):
+    """Public call with host buffers: H2D inputs, gdn.prefill, D2H outputs + final state, every step."""
+    import torch
+    from gated_deltanet_linear_03_gb300 import gdn
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_h = torch.empty(T_TOKENS, HV, D, dtype=torch.bfloat16).pin_memory()
+    fin_h = torch.empty(1, HV, D, D, dtype=torch.float32).pin_memory()
+    ws = torch.empty(gdn.workspace_size(1, T_TOKENS, HK, HV, D, D, cu_host), dtype=torch.uint8, device=dev)
+    out_d = torch.empty(T_TOKENS, HV, D, dtype=torch.bfloat16, device=dev)
+    fin_d = torch.empty(1, HV, D, D, dtype=torch.float32, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+
+    def step():
+        for key in dbuf:
+            dbuf[key].copy_(pinned[key], non_blocking=True)
+        gdn.prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["la"], dbuf["b"], dbuf["cu"], out=out_d,
+                    final_state=fin_d, workspace=ws, cu_seqlens_host=cu_host, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+        fin_h.copy_(fin_d, non_blocking=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return T_TOKENS / (ms * 1e-3), h2d, d2h
+
+
+def cpu_baseline(budget_s: float = 20.0):
+    """The fp64 oracle (as it stands) on the 4K workload, all host cores."""
+    import oracle
+    from gated_deltanet_linear_03_gb300 import synth
+    inp = synth.prefill_4k()
+    args = (inp.q.float().numpy(), inp.k.float().numpy(), inp.v.float().numpy(), inp.log_alpha.numpy(),
+            inp.beta.numpy(), inp.cu_seqlens.numpy())
+    cores = os.cpu_count() or 1
+    times = []
+    t_start = time.time()
+    while True:
+        t0 = time.perf_counter()
+        oracle.prefill(*args, n_threads=cores)
+        times.append(time.perf_counter() - t0)
+        if len(times) >= 3 or time.time() - t_start > budget_s:
+            break
+    t = statistics.median(times)
+    return {"value": T_TOKENS / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"full 4096-token layer, all 32 value heads, fp64, median of {len(times)} runs "
+                      f"({t:.2f} s each)"}
+
+
+# --------------------------------------------------------------------------- arms
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from gated_deltanet_linear_03_gb300 import synth
+    inp = synth.prefill_4k()
+    a = (inp.q.float().numpy(), inp.k.float().numpy(), inp.v.float().numpy(), inp.log_alpha.numpy(),
+         inp.beta.numpy(), inp.cu_seqlens.numpy())
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.prefill(*a, n_threads=cores, want_out=False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.prefill(*a, n_threads=cores)
+    dt = time.perf_counter() - t0
+    value = T_TOKENS * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "each step: the full 4096-token layer, all 32 value heads, fp64"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_gb300(args):
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    from gated_deltanet_linear_03_gb300 import gdn
+    gdn.load_library()
+    stream = torch.cuda.Stream(dev)
+    peaks = load_peaks()
+
+    n_rep = 4
+    inp, host, plans, cu_host = make_prefill_replicas(n_rep, dev)
+    plan_scan = gdn.PrefillPlan(plans[0].tensors[0], plans[0].tensors[1], plans[0].tensors[2],
+                                plans[0].tensors[3], plans[0].tensors[4], plans[0].tensors[5], algo="scan",
+                                cu_seqlens_host=cu_host)
+
+    gpu_index = dev.index if dev.index is not None else 0
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[gpu_index])
+        except ValueError:
+            pass
+    with ClockSampler(gpu_index) as clk:
+        with torch.cuda.stream(stream):
+            soak(lambda: plans[0].run(stream=stream), 1.5)
+        total_ms, prep_ms, pass_ms = time_prefill_steps(plans, args.steps, args.warmup, stream)
+        decode_us = time_decode(dev, stream)
+        scan_ms = time_scan(plan_scan, stream)
+    clocks = clk.summary()
+    e2e_tps, h2d, d2h = time_e2e(host, cu_host, dev, stream, max(3, min(args.steps, 20)))
+    err = gdn.device_error(stream)
+
+    seconds, units = aggregate(total_ms * 1e-3, float(T_TOKENS * args.steps))
+    value = units / seconds
+    e2e_secs, e2e_units = aggregate(T_TOKENS / e2e_tps, float(T_TOKENS))
+
+    flops_prep = FLOPS_PREP * T_TOKENS * HV
+    flops_pass = FLOPS_PASS * T_TOKENS * HV
+    kernels = {
+        "chunk_prep_kernel": {"ms": prep_ms, "tflops": flops_prep / (prep_ms * 1e-3) / 1e12},
+        "state_pass_kernel": {"ms": pass_ms, "tflops": flops_pass / (pass_ms * 1e-3) / 1e12},
+    }
+    dom = max(kernels, key=lambda k: kernels[k]["ms"])
+    ach = kernels[dom]["tflops"]
+    traffic = load_traffic(dom)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
+                "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)",
+                "flops_per_launch": flops_prep if dom == "chunk_prep_kernel" else flops_pass}
+    dec_gbs = DECODE_STATE_BYTES / (decode_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "algo": "chunked (tcgen05)", "parallelism": f"replicas x{world}",
+                   "l2": f"{n_rep} rotating input replicas (~{n_rep * 97} MiB) > L2"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "decode": {"workload": "batch-1 decode step, 30 layers x 32 v heads x 128x128 fp32 state, bf16 q/k/v",
+                   "us_per_step": decode_us, "hbm_gbs": dec_gbs,
+                   "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": dec_gbs / peaks["hbm_gbs"], "traffic": load_traffic("decode_step_kernel")},
+                   "l2": "5 rotating state replicas (300 MiB)"},
+        "scan": {"tok_per_s": T_TOKENS / (scan_ms * 1e-3), "ms": scan_ms,
+                 "fp32_tflops": FLOPS_SCAN * T_TOKENS * HV / (scan_ms * 1e-3) / 1e12},
+        "e2e": {"value": e2e_units / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "device_error": err,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, when one exists for this kernel."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(kernel)
+    except Exception:
+        return None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,177 @@
+// Batch decode step: one token for each of n independent Gated DeltaNet states.
+//
+// "Optimizing on-device inference for Apple Silicon", section "Decode:
+// minimise the bytes moved per token" notes that batch-1 decode is bound by
+// the bytes moved per token; for this layer those bytes are the fp32 state,
+// read once and written once.  The kernel therefore streams every state row
+// exactly once: a row of dk fp32 values is spread over dk/4 lanes (one 16-byte
+// load each), the two dot products S k and S q of a row are finished with warp
+// shuffles, and the updated row is written back from the same registers.  For
+// a row s (one value index i) of one head:
+//     sk = s.k,  sq = s.q
+//     u  = beta (v_i - alpha sk)                 (delta)
+//     s' = alpha s + u k                         (new row)
+//     o_i = s'.q = alpha sq + u (k.q)            (output after the update)
+// The section "Reduce intermediate and state traffic" asks for exactly this
+// fusion: the temporaries never leave registers.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kRowsPerGroup = 8;   // rows each lane group carries at once
+constexpr int kThreads = 128;
+
+// Reduce 16 per-lane partial sums over groups of LPR lanes by recursive
+// halving: each round a lane keeps half of its values and receives the
+// partner's partials for that half.  Afterwards lane `g` of a group holds the
+// complete sums of indices [g*16/LPR, g*16/LPR + max(1, 16/LPR)).
+template <int LPR>
+__device__ __forceinline__ void reduce16(float (&v)[16], int lane) {
+    int n = 16;
+#pragma unroll
+    for (int off = LPR / 2; off >= 1; off >>= 1) {
+        if (n > 1) {
+            const int half = n / 2;
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i < half) {
+                    const float send = upper ? v[i] : v[i + half];
+                    const float keep = upper ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            n = half;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
+                   const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                   const __nv_bfloat16 *__restrict__ v, const float *__restrict__ log_alpha,
+                   const float *__restrict__ beta, void *__restrict__ out, int out_f32) {
+    constexpr int LPR = D / 4;                  // lanes per row
+    constexpr int GROUPS = 32 / LPR;            // lane groups per warp
+    constexpr int WARP_ROWS = GROUPS * kRowsPerGroup;
+    constexpr int PER = (16 / LPR) > 0 ? (16 / LPR) : 1;  // sums held per lane after reduce16
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int group = lane / LPR, gl = lane % LPR;
+    const long row0 = ((long)blockIdx.x * (kThreads / 32) + warp) * WARP_ROWS + group * kRowsPerGroup;
+    if (row0 >= total_rows) return;  // whole group out of range (8 | D keeps groups in one head)
+
+    const long head = row0 / D;                 // flat (n, h)
+    const int h = (int)(head % hv);
+    const long nb = head / hv;
+    const int hq = h / (hv / hk);
+    const int row_in_head = (int)(row0 % D);
+
+    // q, k slice of this lane: 4 bf16 = 8 bytes
+    const size_t qk_off = ((size_t)nb * hk + hq) * D + gl * 4;
+    const uint2 kraw = *reinterpret_cast<const uint2 *>(k + qk_off);
+    const uint2 qraw = *reinterpret_cast<const uint2 *>(q + qk_off);
+    const float kv[4] = {bf16_lo(kraw.x), bf16_hi(kraw.x), bf16_lo(kraw.y), bf16_hi(kraw.y)};
+    const float qv[4] = {bf16_lo(qraw.x), bf16_hi(qraw.x), bf16_lo(qraw.y), bf16_hi(qraw.y)};
+
+    float4 s[kRowsPerGroup];
+    float4 *srow = reinterpret_cast<float4 *>(state + (size_t)row0 * D) + gl;
+#pragma unroll
+    for (int i = 0; i < kRowsPerGroup; ++i) s[i] = __ldcs(srow + (size_t)i * (D / 4));
+
+    // k.q over the head (same for every row of the group)
+    float kq = kv[0] * qv[0] + kv[1] * qv[1] + kv[2] * qv[2] + kv[3] * qv[3];
+#pragma unroll
+    for (int off = LPR / 2; off >= 1; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+
+    const float la = clamp_log_alpha(log_alpha[head]);
+    const float alpha = __expf(la);
+    const float b = beta[head];
+
+    float part[16];
+#pragma unroll
+    for (int i = 0; i < kRowsPerGroup; ++i) {
+        part[i] = s[i].x * kv[0] + s[i].y * kv[1] + s[i].z * kv[2] + s[i].w * kv[3];
+        part[8 + i] = s[i].x * qv[0] + s[i].y * qv[1] + s[i].z * qv[2] + s[i].w * qv[3];
+    }
+    reduce16<LPR>(part, lane);
+
+    // v values of the group's rows, one per holder lane
+    const __nv_bfloat16 *vrow = v + (size_t)head * D + row_in_head;
+    const int my_base = gl * 16 / LPR;
+    const int group_lane0 = group * LPR;
+    float u[kRowsPerGroup];
+#pragma unroll
+    for (int i = 0; i < kRowsPerGroup; ++i) {
+        // holder of sum index i (sk_i) and 8 + i (sq_i) within the group
+        const int src_k = group_lane0 + (i * LPR) / 16;
+        float mine = 0.f;
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+            if (my_base + j == i) mine = part[j];
+        const float sk = __shfl_sync(0xffffffffu, mine, src_k);
+        u[i] = b * (__bfloat162float(vrow[i]) - alpha * sk);
+    }
+
+    // write the updated rows
+#pragma unroll
+    for (int i = 0; i < kRowsPerGroup; ++i) {
+        float4 o;
+        o.x = alpha * s[i].x + u[i] * kv[0];
+        o.y = alpha * s[i].y + u[i] * kv[1];
+        o.z = alpha * s[i].z + u[i] * kv[2];
+        o.w = alpha * s[i].w + u[i] * kv[3];
+        __stcs(srow + (size_t)i * (D / 4), o);
+    }
+
+    // outputs: the holder lane of sq_i writes o_i (with 32 lanes per row two
+    // lanes hold each sum; the even one writes)
+    if (LPR == 32 && (lane & 1)) return;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int idx = my_base + j;
+        if (idx >= 8 && idx < 16) {
+            const int i = idx - 8;
+            const float o = alpha * part[j] + u[i] * kq;
+            const size_t oi = (size_t)head * D + row_in_head + i;
+            if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
+            else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(o);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeProblem &p) {
+    const long total_rows = (long)p.n * p.hv * p.d;
+    if (total_rows == 0) return cudaSuccess;
+    int warp_rows = 0;
+    switch (p.d) {
+        case 32: warp_rows = 4 * kRowsPerGroup; break;
+        case 64: warp_rows = 2 * kRowsPerGroup; break;
+        case 128: warp_rows = kRowsPerGroup; break;
+        default: return cudaErrorInvalidValue;
+    }
+    const long rows_per_block = (long)warp_rows * (kThreads / 32);
+    const unsigned grid = (unsigned)((total_rows + rows_per_block - 1) / rows_per_block);
+    switch (p.d) {
+        case 32:
+            decode_step_kernel<32><<<grid, kThreads, 0, p.stream>>>((int)total_rows, p.hk, p.hv, p.state, p.q, p.k, p.v,
+                                                                   p.log_alpha, p.beta, p.out, p.out_f32);
+            break;
+        case 64:
+            decode_step_kernel<64><<<grid, kThreads, 0, p.stream>>>((int)total_rows, p.hk, p.hv, p.state, p.q, p.k, p.v,
+                                                                   p.log_alpha, p.beta, p.out, p.out_f32);
+            break;
+        default:
+            decode_step_kernel<128><<<grid, kThreads, 0, p.stream>>>((int)total_rows, p.hk, p.hv, p.state, p.q, p.k,
+                                                                    p.v, p.log_alpha, p.beta, p.out, p.out_f32);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,225 @@
+// extern "C" entry points of libgdn: argument validation on the host, then a
+// launch of the matching kernel on the caller's stream.  Validation never
+// touches the CUDA runtime, so argument errors are reported without side
+// effects (and work on machines without a GPU).
+#include <string.h>
+
+#include "gdn_internal.cuh"
+
+namespace {
+
+__device__ unsigned int g_device_error = 0;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+
+// [a, a + na) and [b, b + nb) byte ranges overlap?
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+gdn_status check_heads(int hk, int hv, int dk, int dv) {
+    if (hk <= 0 || hv <= 0 || dk <= 0 || dv <= 0) return GDN_ERR_INVALID_ARG;
+    if (hv % hk != 0) return GDN_ERR_INVALID_ARG;
+    if (dk != dv || !supported_dim(dk)) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+gdn_status check_cu(int n_seqs, int total_tokens, const int32_t *cu_host) {
+    if (n_seqs <= 0 || total_tokens < 0 || !cu_host) return GDN_ERR_INVALID_ARG;
+    if (cu_host[0] != 0 || cu_host[n_seqs] != total_tokens) return GDN_ERR_INVALID_ARG;
+    for (int i = 0; i < n_seqs; ++i)
+        if (cu_host[i + 1] < cu_host[i]) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+unsigned int *device_error_ptr() {
+    static unsigned int *ptr = nullptr;
+    static int dev_cached = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (ptr == nullptr || dev != dev_cached) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        ptr = static_cast<unsigned int *>(p);
+        dev_cached = dev;
+    }
+    return ptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_version(void) { return 100; }
+
+const char *gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: unsupported shape, dtype or algorithm";
+        case GDN_ERR_ALIGNMENT: return "GDN_ERR_ALIGNMENT: pointer not 16-byte aligned";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA call or kernel launch failed";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case GDN_ERR_INTERNAL: return "GDN_ERR_INTERNAL: device-side consistency check failed";
+        case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
+    }
+    return "unknown gdn_status";
+}
+
+size_t gdn_prefill_workspace_size(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                                  const int32_t *cu_seqlens_host, int algo, gdn_status *status) {
+    gdn_status st = check_heads(hk, hv, dk, dv);
+    if (st == GDN_OK) st = check_cu(n_seqs, total_tokens, cu_seqlens_host);
+    if (st == GDN_OK && algo != GDN_ALGO_CHUNKED && algo != GDN_ALGO_SCAN) st = GDN_ERR_UNSUPPORTED;
+    if (status) *status = st;
+    if (st != GDN_OK || algo == GDN_ALGO_SCAN) return 0;
+    return gdn::chunked_workspace_bytes(n_seqs, cu_seqlens_host, hv, dk);
+}
+
+}  // extern "C"
+
+static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                       const void *q, const void *k, const void *v,
+                       const float *log_alpha, const float *beta,
+                       const float *init_state,
+                       const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                       void *out, int out_dtype, float *final_state,
+                       int algo, void *workspace, size_t workspace_bytes, void *stream, int phases) {
+    gdn_status st = check_heads(hk, hv, dk, dv);
+    if (st != GDN_OK) return st;
+    if ((st = check_cu(n_seqs, total_tokens, cu_seqlens_host)) != GDN_OK) return st;
+    if (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
+    if (algo != GDN_ALGO_CHUNKED && algo != GDN_ALGO_SCAN) return GDN_ERR_UNSUPPORTED;
+    if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !out)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, log_alpha, beta, init_state, cu_seqlens, out, final_state, workspace};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+
+    const size_t T = (size_t)total_tokens;
+    const size_t state_bytes = (size_t)n_seqs * hv * dv * dk * sizeof(float);
+    const size_t out_bytes = T * hv * dv * (out_dtype == GDN_DTYPE_F32 ? 4 : 2);
+    const struct { const void *p; size_t n; } inputs[] = {
+        {q, T * hk * dk * 2}, {k, T * hk * dk * 2}, {v, T * hv * dv * 2},
+        {log_alpha, T * hv * 4}, {beta, T * hv * 4}, {cu_seqlens, (size_t)(n_seqs + 1) * 4},
+        {init_state, state_bytes}};
+    for (const auto &in : inputs) {
+        if (overlaps(out, out_bytes, in.p, in.n)) return GDN_ERR_INVALID_ARG;
+        if (in.p != init_state && overlaps(final_state, state_bytes, in.p, in.n)) return GDN_ERR_INVALID_ARG;
+    }
+    if (final_state && init_state && final_state != init_state &&
+        overlaps(final_state, state_bytes, init_state, state_bytes))
+        return GDN_ERR_INVALID_ARG;
+    if (overlaps(out, out_bytes, final_state, state_bytes)) return GDN_ERR_INVALID_ARG;
+
+    size_t need = 0;
+    if (algo == GDN_ALGO_CHUNKED) {
+        need = gdn::chunked_workspace_bytes(n_seqs, cu_seqlens_host, hv, dk);
+        if (need > 0 && (!workspace || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
+        if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return GDN_ERR_ALIGNMENT;
+        const struct { const void *p; size_t n; } all[] = {
+            {q, T * hk * dk * 2}, {k, T * hk * dk * 2}, {v, T * hv * dv * 2}, {log_alpha, T * hv * 4},
+            {beta, T * hv * 4}, {cu_seqlens, (size_t)(n_seqs + 1) * 4}, {init_state, state_bytes},
+            {out, out_bytes}, {final_state, state_bytes}};
+        for (const auto &a : all)
+            if (overlaps(workspace, need, a.p, a.n)) return GDN_ERR_INVALID_ARG;
+    }
+    if (total_tokens == 0 && !final_state) return GDN_OK;
+
+    gdn::PrefillProblem p{};
+    p.n_seqs = n_seqs; p.total_tokens = total_tokens; p.hk = hk; p.hv = hv; p.d = dk;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.log_alpha = log_alpha; p.beta = beta; p.init_state = init_state;
+    p.cu_seqlens = cu_seqlens; p.cu_seqlens_host = cu_seqlens_host;
+    p.out = out; p.out_f32 = out_dtype == GDN_DTYPE_F32; p.final_state = final_state;
+    p.workspace = workspace; p.workspace_bytes = workspace_bytes;
+    p.err = device_error_ptr();
+    p.stream = static_cast<cudaStream_t>(stream);
+    if (!p.err) return GDN_ERR_CUDA;
+    const cudaError_t e = (algo == GDN_ALGO_SCAN) ? gdn::launch_scan_prefill(p) : gdn::launch_chunked_prefill(p, phases);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" {
+
+gdn_status gdn_prefill(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                       const void *q, const void *k, const void *v,
+                       const float *log_alpha, const float *beta,
+                       const float *init_state,
+                       const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                       void *out, int out_dtype, float *final_state,
+                       int algo, void *workspace, size_t workspace_bytes, void *stream) {
+    return prefill_impl(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
+                        cu_seqlens_host, out, out_dtype, final_state, algo, workspace, workspace_bytes, stream, 3);
+}
+
+gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                                     const void *q, const void *k, const void *v,
+                                     const float *log_alpha, const float *beta,
+                                     const float *init_state,
+                                     const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                     void *out, int out_dtype, float *final_state,
+                                     void *workspace, size_t workspace_bytes, void *stream) {
+    if (phase != GDN_PHASE_PREP && phase != GDN_PHASE_PASS) return GDN_ERR_INVALID_ARG;
+    return prefill_impl(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
+                        cu_seqlens_host, out, out_dtype, final_state, GDN_ALGO_CHUNKED, workspace, workspace_bytes,
+                        stream, phase == GDN_PHASE_PREP ? 1 : 2);
+}
+
+gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
+                           const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *beta,
+                           void *out, int out_dtype, void *stream) {
+    gdn_status st = check_heads(hk, hv, dk, dv);
+    if (st != GDN_OK) return st;
+    if (n < 0) return GDN_ERR_INVALID_ARG;
+    if (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
+    if (n == 0) return GDN_OK;
+    if (!state || !q || !k || !v || !log_alpha || !beta || !out) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {state, q, k, v, log_alpha, beta, out};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_ALIGNMENT;
+    const size_t state_bytes = (size_t)n * hv * dv * dk * 4;
+    const size_t out_bytes = (size_t)n * hv * dv * (out_dtype == GDN_DTYPE_F32 ? 4 : 2);
+    const struct { const void *p; size_t n; } inputs[] = {
+        {q, (size_t)n * hk * dk * 2}, {k, (size_t)n * hk * dk * 2}, {v, (size_t)n * hv * dv * 2},
+        {log_alpha, (size_t)n * hv * 4}, {beta, (size_t)n * hv * 4}, {out, out_bytes}};
+    for (const auto &in : inputs)
+        if (overlaps(state, state_bytes, in.p, in.n)) return GDN_ERR_INVALID_ARG;
+    if (overlaps(out, out_bytes, q, (size_t)n * hk * dk * 2) || overlaps(out, out_bytes, k, (size_t)n * hk * dk * 2) ||
+        overlaps(out, out_bytes, v, (size_t)n * hv * dv * 2))
+        return GDN_ERR_INVALID_ARG;
+
+    gdn::DecodeProblem p{};
+    p.n = n; p.hk = hk; p.hv = hv; p.d = dk; p.state = state;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.log_alpha = log_alpha; p.beta = beta; p.out = out; p.out_f32 = out_dtype == GDN_DTYPE_F32;
+    p.err = nullptr;
+    p.stream = static_cast<cudaStream_t>(stream);
+    return gdn::launch_decode(p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_device_error(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+    unsigned int *ptr = device_error_ptr();
+    if (!ptr) return GDN_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, ptr, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+    if (word) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(ptr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    if (word & gdn::kErrTimeout) return GDN_ERR_TIMEOUT;
+    if (word & gdn::kErrInternal) return GDN_ERR_INTERNAL;
+    return GDN_OK;
+}
+
+}  // extern "C"

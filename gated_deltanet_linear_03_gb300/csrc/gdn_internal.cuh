@@ -1,0 +1,63 @@
+// Internal declarations shared by the translation units of libgdn.
+// Nothing here is part of the public ABI (include/gdn.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+// Lowest log-decay the GPU paths use; see the gdn.h note on log_alpha.
+constexpr float kLogAlphaFloor = -20.0f;
+// Chunk length of the blocked evaluation.
+constexpr int kChunk = 64;
+
+__device__ __forceinline__ float clamp_log_alpha(float la) { return fmaxf(la, kLogAlphaFloor); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xffff0000u); }
+
+// Error word bits set by kernels (read back by gdn_device_error).
+enum : unsigned int { kErrTimeout = 1u, kErrInternal = 2u };
+
+__device__ __forceinline__ void raise_error(unsigned int *err, unsigned int bit) {
+    if (err) atomicOr(err, bit);
+}
+
+// Per-call plan passed to the launchers (validated on the host already).
+struct PrefillProblem {
+    int n_seqs, total_tokens, hk, hv, d;
+    const __nv_bfloat16 *q, *k, *v;
+    const float *log_alpha, *beta, *init_state;
+    const int32_t *cu_seqlens;        // device
+    const int32_t *cu_seqlens_host;   // host
+    void *out;
+    int out_f32;
+    float *final_state;
+    void *workspace;
+    size_t workspace_bytes;
+    unsigned int *err;
+    cudaStream_t stream;
+};
+
+struct DecodeProblem {
+    int n, hk, hv, d;
+    float *state;
+    const __nv_bfloat16 *q, *k, *v;
+    const float *log_alpha, *beta;
+    void *out;
+    int out_f32;
+    unsigned int *err;
+    cudaStream_t stream;
+};
+
+cudaError_t launch_decode(const DecodeProblem &p);
+cudaError_t launch_scan_prefill(const PrefillProblem &p);
+// phases: bit 0 = per-chunk preparation, bit 1 = state passing + outputs
+cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases);
+size_t chunked_workspace_bytes(int n_seqs, const int32_t *cu_host, int hv, int d);
+
+}  // namespace gdn

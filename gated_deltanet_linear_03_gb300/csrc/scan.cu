@@ -1,0 +1,216 @@
+// Direct-scan prefill: the recurrence evaluated token by token with the state
+// held in registers for the whole sequence.
+//
+// "Optimizing on-device inference for Apple Silicon", section "Keep recurrent
+// state on chip": the state matrix is loaded into registers once, carried
+// through the whole scan with partial sums exchanged by SIMD (warp) shuffles
+// rather than through shared memory, and written back only at the end.  The
+// same page (section "Qwen creates three workload shapes") says that whether
+// this direct scan or the blocked form is faster depends on the model
+// dimensions, the workload and the hardware, so the library ships both.
+//
+// Mapping on sm_103a: one CTA of 128 threads owns 32 consecutive value rows of
+// one (sequence, value head) state; thread (r, c) holds row r, columns
+// [c*D/4, (c+1)*D/4) in registers.  Inputs for the next 64 tokens are staged
+// into shared memory with cp.async while the current 64 are scanned; outputs
+// are staged and written back as coalesced rows.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kRows = 32;   // value rows per CTA
+constexpr int kTB = 64;     // tokens per staged block
+
+template <int D>
+struct ScanSmem {
+    __nv_bfloat16 k[2][kTB][D];
+    __nv_bfloat16 q[2][kTB][D];
+    __nv_bfloat16 v[2][kTB][kRows];
+    float la[2][kTB];
+    float b[2][kTB];
+    float o[kTB][kRows];
+};
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+template <int D>
+__device__ __forceinline__ void stage_block(ScanSmem<D> &sm, int buf, long t0, int nt, int hk, int hv,
+                                            int hq, int h, int row0, const __nv_bfloat16 *__restrict__ q,
+                                            const __nv_bfloat16 *__restrict__ k,
+                                            const __nv_bfloat16 *__restrict__ v,
+                                            const float *__restrict__ log_alpha,
+                                            const float *__restrict__ beta) {
+    constexpr int QK_CHUNKS = D / 8;      // 16-byte pieces per q/k row
+    constexpr int V_CHUNKS = kRows / 8;   // 16-byte pieces of the v slice
+    for (int i = threadIdx.x; i < nt * QK_CHUNKS; i += kThreads) {
+        const int t = i / QK_CHUNKS, c = i % QK_CHUNKS;
+        const size_t g = ((size_t)(t0 + t) * hk + hq) * D + c * 8;
+        cp_async16(&sm.k[buf][t][c * 8], k + g);
+        cp_async16(&sm.q[buf][t][c * 8], q + g);
+    }
+    for (int i = threadIdx.x; i < nt * V_CHUNKS; i += kThreads) {
+        const int t = i / V_CHUNKS, c = i % V_CHUNKS;
+        cp_async16(&sm.v[buf][t][c * 8], v + ((size_t)(t0 + t) * hv + h) * D + row0 + c * 8);
+    }
+    for (int t = threadIdx.x; t < nt; t += kThreads) {
+        cp_async4(&sm.la[buf][t], log_alpha + (size_t)(t0 + t) * hv + h);
+        cp_async4(&sm.b[buf][t], beta + (size_t)(t0 + t) * hv + h);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__restrict__ q,
+                    const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
+                    const float *__restrict__ log_alpha, const float *__restrict__ beta,
+                    const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
+                    void *__restrict__ out, int out_f32, float *__restrict__ final_state) {
+    constexpr int COLS = D / 4;           // state columns per thread
+    constexpr int SLICES = D / kRows;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ScanSmem<D> &sm = *reinterpret_cast<ScanSmem<D> *>(smem_raw);
+
+    const int slice = blockIdx.x % SLICES;
+    const int h = (blockIdx.x / SLICES) % hv;
+    const int n = blockIdx.x / (SLICES * hv);
+    const int hq = h / (hv / hk);
+    const int row0 = slice * kRows;
+    const int r = threadIdx.x >> 2, c = threadIdx.x & 3;
+
+    const long tbeg = min(max((long)cu_seqlens[n], 0L), (long)total_tokens);
+    const long tend = min(max((long)cu_seqlens[n + 1], tbeg), (long)total_tokens);
+
+    float S[COLS];
+    const size_t srow = (((size_t)n * hv + h) * D + row0 + r) * D + c * COLS;
+    if (init_state) {
+#pragma unroll
+        for (int j = 0; j < COLS; j += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(init_state + srow + j);
+            S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < COLS; ++j) S[j] = 0.f;
+    }
+
+    const long ntok = tend - tbeg;
+    const int nblk = (int)((ntok + kTB - 1) / kTB);
+    if (nblk > 0) {
+        stage_block<D>(sm, 0, tbeg, (int)min((long)kTB, ntok), hk, hv, hq, h, row0, q, k, v, log_alpha, beta);
+        cp_async_commit();
+    }
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int buf = blk & 1;
+        const long t0 = tbeg + (long)blk * kTB;
+        const int nt = (int)min((long)kTB, tend - t0);
+        if (blk + 1 < nblk) {
+            const long t1 = t0 + kTB;
+            stage_block<D>(sm, buf ^ 1, t1, (int)min((long)kTB, tend - t1), hk, hv, hq, h, row0, q, k, v,
+                           log_alpha, beta);
+        }
+        cp_async_commit();
+        cp_async_wait_prev();
+        __syncthreads();
+
+        for (int t = 0; t < nt; ++t) {
+            float kk[COLS], qq[COLS];
+            const uint4 *kp = reinterpret_cast<const uint4 *>(&sm.k[buf][t][c * COLS]);
+            const uint4 *qp = reinterpret_cast<const uint4 *>(&sm.q[buf][t][c * COLS]);
+#pragma unroll
+            for (int j = 0; j < COLS / 8; ++j) {
+                const uint4 a = kp[j], b = qp[j];
+                kk[8 * j + 0] = bf16_lo(a.x); kk[8 * j + 1] = bf16_hi(a.x);
+                kk[8 * j + 2] = bf16_lo(a.y); kk[8 * j + 3] = bf16_hi(a.y);
+                kk[8 * j + 4] = bf16_lo(a.z); kk[8 * j + 5] = bf16_hi(a.z);
+                kk[8 * j + 6] = bf16_lo(a.w); kk[8 * j + 7] = bf16_hi(a.w);
+                qq[8 * j + 0] = bf16_lo(b.x); qq[8 * j + 1] = bf16_hi(b.x);
+                qq[8 * j + 2] = bf16_lo(b.y); qq[8 * j + 3] = bf16_hi(b.y);
+                qq[8 * j + 4] = bf16_lo(b.z); qq[8 * j + 5] = bf16_hi(b.z);
+                qq[8 * j + 6] = bf16_lo(b.w); qq[8 * j + 7] = bf16_hi(b.w);
+            }
+            float sk[4] = {0.f, 0.f, 0.f, 0.f}, sq[4] = {0.f, 0.f, 0.f, 0.f}, kq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < COLS; ++j) {
+                sk[j & 3] = fmaf(S[j], kk[j], sk[j & 3]);
+                sq[j & 3] = fmaf(S[j], qq[j], sq[j & 3]);
+                kq[j & 3] = fmaf(kk[j], qq[j], kq[j & 3]);
+            }
+            float a0 = (sk[0] + sk[1]) + (sk[2] + sk[3]);
+            float a1 = (sq[0] + sq[1]) + (sq[2] + sq[3]);
+            float a2 = (kq[0] + kq[1]) + (kq[2] + kq[3]);
+            a0 += __shfl_xor_sync(0xffffffffu, a0, 1);
+            a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
+            a2 += __shfl_xor_sync(0xffffffffu, a2, 1);
+            a0 += __shfl_xor_sync(0xffffffffu, a0, 2);
+            a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
+            a2 += __shfl_xor_sync(0xffffffffu, a2, 2);
+            const float alpha = expf(clamp_log_alpha(sm.la[buf][t]));
+            const float bt = sm.b[buf][t];
+            const float u = bt * (__bfloat162float(sm.v[buf][t][r]) - alpha * a0);
+#pragma unroll
+            for (int j = 0; j < COLS; ++j) S[j] = fmaf(alpha, S[j], u * kk[j]);
+            if (c == 0) sm.o[t][r] = fmaf(alpha, a1, u * a2);
+        }
+        __syncthreads();
+        // write this block's outputs: row-contiguous 32-value pieces
+        for (int i = threadIdx.x; i < nt * kRows; i += kThreads) {
+            const int t = i / kRows, j = i % kRows;
+            const size_t oi = ((size_t)(t0 + t) * hv + h) * D + row0 + j;
+            if (out_f32) reinterpret_cast<float *>(out)[oi] = sm.o[t][j];
+            else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(sm.o[t][j]);
+        }
+        __syncthreads();
+    }
+    cp_async_wait_all();
+
+    if (final_state) {
+#pragma unroll
+        for (int j = 0; j < COLS; j += 4)
+            *reinterpret_cast<float4 *>(final_state + srow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+}
+
+template <int D>
+cudaError_t launch_scan_d(const PrefillProblem &p) {
+    const size_t smem = sizeof(ScanSmem<D>);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_set[128] = {};
+    if (dev < 128 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(scan_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const unsigned grid = (unsigned)(p.n_seqs * p.hv * (D / kRows));
+    scan_prefill_kernel<D><<<grid, kThreads, smem, p.stream>>>(
+        p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.out,
+        p.out_f32, p.final_state);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_scan_prefill(const PrefillProblem &p) {
+    if (p.n_seqs == 0) return cudaSuccess;
+    switch (p.d) {
+        case 32: return launch_scan_d<32>(p);
+        case 64: return launch_scan_d<64>(p);
+        case 128: return launch_scan_d<128>(p);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gdn

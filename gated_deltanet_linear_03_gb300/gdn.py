@@ -1,0 +1,229 @@
+"""Thin ctypes binding of libgdn (include/gdn.h).
+
+Argument marshalling only: every step of the recurrence runs in the CUDA
+kernels of ``libgdn.so``.  Torch provides device memory and streams.  There is
+no CPU fallback: if the library is missing or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_OK = 0
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIGNMENT",
+                4: "GDN_ERR_CUDA", 5: "GDN_ERR_TIMEOUT", 6: "GDN_ERR_INTERNAL", 7: "GDN_ERR_WORKSPACE"}
+ALGO = {"chunked": 0, "scan": 1}
+DTYPE = {torch.bfloat16: 0, torch.float32: 1}
+
+# every symbol include/gdn.h declares
+EXPORTS = ("gdn_prefill", "gdn_prefill_chunked_phase", "gdn_prefill_workspace_size", "gdn_decode_step",
+           "gdn_device_error", "gdn_status_string", "gdn_version")
+PHASE = {"prep": 1, "pass": 2}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({lib_status_string(status)})")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgdn.so (built by ``__graft_entry__.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libgdn.so not found at {path}; build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.gdn_prefill.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, P, Z, P]
+    lib.gdn_prefill.restype = I
+    lib.gdn_prefill_chunked_phase.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, P, Z, P]
+    lib.gdn_prefill_chunked_phase.restype = I
+    lib.gdn_prefill_workspace_size.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
+    lib.gdn_prefill_workspace_size.restype = Z
+    lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, P]
+    lib.gdn_decode_step.restype = I
+    lib.gdn_device_error.argtypes = [P]
+    lib.gdn_device_error.restype = I
+    lib.gdn_status_string.argtypes = [I]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_version.restype = I
+    _lib = lib
+    return lib
+
+
+def lib_status_string(status: int) -> str:
+    try:
+        return load_library().gdn_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def _host_cu(cu_seqlens: torch.Tensor, cu_host) -> Tuple[ctypes.Array, list]:
+    vals = [int(x) for x in (cu_host if cu_host is not None else cu_seqlens.cpu().tolist())]
+    arr = (ctypes.c_int32 * len(vals))(*vals)
+    return arr, vals
+
+
+def workspace_size(n_seqs: int, total_tokens: int, hk: int, hv: int, dk: int, dv: int,
+                   cu_seqlens_host: Sequence[int], algo: str = "chunked") -> int:
+    lib = load_library()
+    arr = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+    st = ctypes.c_int(0)
+    n = lib.gdn_prefill_workspace_size(n_seqs, total_tokens, hk, hv, dk, dv, arr, ALGO[algo], ctypes.byref(st))
+    if st.value != GDN_OK:
+        raise GdnError(st.value, "gdn_prefill_workspace_size")
+    return int(n)
+
+
+def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,
+            beta: torch.Tensor, cu_seqlens: torch.Tensor, *, init_state: Optional[torch.Tensor] = None,
+            out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+            final_state=True, algo: str = "chunked", workspace: Optional[torch.Tensor] = None,
+            cu_seqlens_host: Optional[Sequence[int]] = None, stream=None):
+    """Run ``gdn_prefill``.  Returns ``(out, final_state)``.
+
+    ``final_state`` may be ``True`` (allocate), ``False``/``None`` (do not emit)
+    or a tensor to write into (it may be ``init_state`` for an in-place update).
+    """
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(log_alpha, "log_alpha", torch.float32, 2)
+    _need(beta, "beta", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, hk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    n_seqs = cu_seqlens.numel() - 1
+    if init_state is not None:
+        _need(init_state, "init_state", torch.float32, 4)
+    if out is None:
+        out = torch.empty(T, hv, dv, device=q.device, dtype=out_dtype)
+    else:
+        _need(out, "out", out.dtype, 3)
+    if final_state is True:
+        final_state = torch.empty(n_seqs, hv, dv, dk, device=q.device, dtype=torch.float32)
+    elif final_state is False:
+        final_state = None
+    elif final_state is not None:
+        _need(final_state, "final_state", torch.float32, 4)
+    cu_arr, cu_vals = _host_cu(cu_seqlens, cu_seqlens_host)
+    need = workspace_size(n_seqs, T, hk, hv, dk, dv, cu_vals, algo) if n_seqs > 0 else 0
+    if need and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.gdn_prefill(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                         _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out), DTYPE[out.dtype],
+                         _ptr(final_state), ALGO[algo], _ptr(workspace), ws_bytes, _stream_ptr(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_prefill")
+    return out, final_state
+
+
+class PrefillPlan:
+    """Pre-marshalled arguments of one gdn_prefill problem, for repeated calls
+    with little host overhead (benchmarks, CUDA-graph capture).  All tensors
+    must stay alive and unmoved while the plan is used."""
+
+    def __init__(self, q, k, v, log_alpha, beta, cu_seqlens, *, init_state=None, out=None,
+                 out_dtype=torch.bfloat16, final_state=True, algo="chunked", workspace=None,
+                 cu_seqlens_host=None):
+        self.lib = load_library()
+        _need(q, "q", torch.bfloat16, 3)
+        _need(k, "k", torch.bfloat16, 3)
+        _need(v, "v", torch.bfloat16, 3)
+        _need(log_alpha, "log_alpha", torch.float32, 2)
+        _need(beta, "beta", torch.float32, 2)
+        _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+        T, hk, dk = q.shape
+        hv, dv = v.shape[1], v.shape[2]
+        n_seqs = cu_seqlens.numel() - 1
+        if out is None:
+            out = torch.empty(T, hv, dv, device=q.device, dtype=out_dtype)
+        if final_state is True:
+            final_state = torch.empty(n_seqs, hv, dv, dk, device=q.device, dtype=torch.float32)
+        elif final_state is False:
+            final_state = None
+        self.cu_arr, cu_vals = _host_cu(cu_seqlens, cu_seqlens_host)
+        need = workspace_size(n_seqs, T, hk, hv, dk, dv, cu_vals, algo)
+        if need and workspace is None:
+            workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+        self.out, self.final_state, self.workspace = out, final_state, workspace
+        self.tensors = (q, k, v, log_alpha, beta, cu_seqlens, init_state)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        self.algo = ALGO[algo]
+        self.head = (n_seqs, T, hk, hv, dk, dv)
+        self.ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
+                     self.cu_arr, _ptr(out), DTYPE[out.dtype], _ptr(final_state))
+        self.ws = (_ptr(workspace), ws_bytes)
+
+    def run(self, stream=None):
+        st = self.lib.gdn_prefill(*self.head, *self.ptrs, self.algo, *self.ws, _stream_ptr(stream))
+        if st != GDN_OK:
+            raise GdnError(st, "gdn_prefill")
+        return self.out, self.final_state
+
+    def run_phase(self, phase: str, stream=None):
+        st = self.lib.gdn_prefill_chunked_phase(PHASE[phase], *self.head, *self.ptrs, *self.ws, _stream_ptr(stream))
+        if st != GDN_OK:
+            raise GdnError(st, "gdn_prefill_chunked_phase")
+
+
+def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                log_alpha: torch.Tensor, beta: torch.Tensor, *, out: Optional[torch.Tensor] = None,
+                out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """Run ``gdn_decode_step`` (state updated in place).  Returns ``out``."""
+    lib = load_library()
+    _need(state, "state", torch.float32, 4)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(log_alpha, "log_alpha", torch.float32, 2)
+    _need(beta, "beta", torch.float32, 2)
+    n, hk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    if out is None:
+        out = torch.empty(n, hv, dv, device=q.device, dtype=out_dtype)
+    st = lib.gdn_decode_step(n, hk, hv, dk, dv, _ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                             _ptr(beta), _ptr(out), DTYPE[out.dtype], _stream_ptr(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_decode_step")
+    return out
+
+
+def device_error(stream=None) -> int:
+    """Synchronise and return the device-side error status (0 = none)."""
+    return int(load_library().gdn_device_error(_stream_ptr(stream)))

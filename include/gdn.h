@@ -1,0 +1,178 @@
+/*
+ * gdn.h: C ABI of the GB300 (sm_103a) Gated DeltaNet recurrence library.
+ *
+ * The operation ("Optimizing on-device inference for Apple Silicon",
+ * section "Qwen creates three workload shapes"): a Gated DeltaNet layer keeps
+ * one fixed-size recurrent state per value head; a learned gate decides how
+ * much of it survives each token and a delta update writes the token in.
+ * Per value head h the state S is a dv x dk fp32 matrix (the section "Keep
+ * recurrent state on chip" fixes state and gate as fp32 and q/k as bf16) and
+ * each token t does
+ *
+ *     alpha_t = exp(log_alpha_t)
+ *     S_t     = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t     = S_t q_t
+ *
+ * with value head h reading query/key head h / (hv / hk).  Long prompts may be
+ * fed in pieces: passing one call's final_state as the next call's init_state
+ * gives the same result as one call over the whole prompt (section "Bound
+ * scratch memory by chunking the prompt").
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, except the
+ *     ones whose name ends in _host.  The library allocates nothing on these
+ *     calls and keeps no state between calls, apart from one device-side
+ *     error word (see gdn_device_error).
+ *   - Every tensor is dense, row-major, with the shape given below, and its
+ *     base address is 16-byte aligned.
+ *   - q and k are already L2-normalised and q is already scaled (e.g. by
+ *     1/sqrt(dk)) by the caller; the library applies no normalisation.
+ *   - log_alpha must be <= 0 (it may be -INFINITY) and beta in [0, 1].  The
+ *     GPU paths clamp log_alpha to >= -20 (alpha >= 2.1e-9) so that decay
+ *     ratios inside a chunk stay finite; the effect is below fp32 resolution
+ *     of any state that is not already negligible.
+ *   - `stream` is a cudaStream_t passed as void* (NULL: the legacy default
+ *     stream).  Calls are asynchronous on that stream.
+ *   - Argument errors are detected on the host before anything is launched
+ *     and returned synchronously; nothing is written in that case.  A launch
+ *     failure returns GDN_ERR_CUDA.  Faults inside a kernel surface on a later
+ *     synchronisation, as with any CUDA work.
+ *   - Supported head sizes: dk == dv, and dk in {32, 64, 128}.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad cu_seqlens, ... */
+    GDN_ERR_UNSUPPORTED = 2,  /* well-formed but not implemented (head size, dtype, algo) */
+    GDN_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
+    GDN_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    GDN_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (see gdn_device_error) */
+    GDN_ERR_INTERNAL = 6,     /* a device-side consistency check failed */
+    GDN_ERR_WORKSPACE = 7     /* workspace missing or smaller than gdn_prefill_workspace_size */
+} gdn_status;
+
+typedef enum {
+    GDN_ALGO_CHUNKED = 0,  /* blocked evaluation, 64-token chunks, tcgen05 tensor cores */
+    GDN_ALGO_SCAN = 1      /* direct token-by-token scan, state held in registers */
+} gdn_algo;
+
+typedef enum {
+    GDN_DTYPE_BF16 = 0,
+    GDN_DTYPE_F32 = 1
+} gdn_dtype;
+
+/*
+ * gdn_prefill: run the recurrence over n_seqs packed sequences.
+ *
+ *   n_seqs           number of sequences (>= 1)
+ *   total_tokens     T = cu_seqlens[n_seqs] (>= 0)
+ *   hk, hv, dk, dv   query/key heads, value heads (hv % hk == 0), head sizes
+ *   q, k             bf16 [T, hk, dk]
+ *   v                bf16 [T, hv, dv]
+ *   log_alpha, beta  fp32 [T, hv]
+ *   init_state       fp32 [n_seqs, hv, dv, dk] (row = value index), or NULL for zeros
+ *   cu_seqlens       int32 [n_seqs + 1] on the device: sequence n is tokens
+ *                    [cu_seqlens[n], cu_seqlens[n+1])
+ *   cu_seqlens_host  the same n_seqs + 1 values in host memory; used to plan the
+ *                    launch without a device synchronisation.  It must start at
+ *                    0, be non-decreasing and end at total_tokens.  The kernels
+ *                    also clamp the device copy to [0, total_tokens].
+ *   out              [T, hv, dv], dtype out_dtype (GDN_DTYPE_BF16 or _F32)
+ *   final_state      fp32 [n_seqs, hv, dv, dk] or NULL.  It may be the same
+ *                    buffer as init_state (updated in place); any other overlap
+ *                    with an input is an error.
+ *   algo             GDN_ALGO_CHUNKED or GDN_ALGO_SCAN
+ *   workspace        device scratch of at least gdn_prefill_workspace_size()
+ *                    bytes (may be NULL when that size is 0), 256-byte aligned.
+ *                    Its contents on entry do not matter.
+ *   stream           cudaStream_t as void*
+ */
+GDN_API gdn_status gdn_prefill(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                       const void *q, const void *k, const void *v,
+                       const float *log_alpha, const float *beta,
+                       const float *init_state,
+                       const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                       void *out, int out_dtype, float *final_state,
+                       int algo, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gdn_prefill_chunked_phase: one of the two phases of the chunked prefill, for
+ * callers that schedule or time them separately.  gdn_prefill with
+ * GDN_ALGO_CHUNKED is exactly GDN_PHASE_PREP followed by GDN_PHASE_PASS on the
+ * same stream with the same arguments and the same workspace, whose contents
+ * must not change in between.
+ *   GDN_PHASE_PREP  per-chunk preparation, parallel over (chunk, value head):
+ *                   reads q, k, log_alpha, beta, cu_seqlens; writes the workspace.
+ *   GDN_PHASE_PASS  state passing across chunks and the outputs: reads every
+ *                   input and the workspace; writes out and final_state.
+ * Arguments, validation and errors as for gdn_prefill (algo is implied).
+ */
+typedef enum {
+    GDN_PHASE_PREP = 1,
+    GDN_PHASE_PASS = 2
+} gdn_phase;
+
+GDN_API gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                                             const void *q, const void *k, const void *v,
+                                             const float *log_alpha, const float *beta,
+                                             const float *init_state,
+                                             const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                             void *out, int out_dtype, float *final_state,
+                                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of device workspace gdn_prefill needs for this problem (0 for
+ * GDN_ALGO_SCAN).  Returns 0 and sets *status (if non-NULL) to an error code
+ * when the arguments are invalid.
+ */
+GDN_API size_t gdn_prefill_workspace_size(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                                  const int32_t *cu_seqlens_host, int algo, gdn_status *status);
+
+/*
+ * gdn_decode_step: one token for each of n independent states (batch-1 decode
+ * of n layers, or n requests), updating the states in place.
+ *
+ *   state            fp32 [n, hv, dv, dk], read and overwritten
+ *   q, k             bf16 [n, hk, dk]
+ *   v                bf16 [n, hv, dv]
+ *   log_alpha, beta  fp32 [n, hv]
+ *   out              [n, hv, dv], dtype out_dtype; must not overlap state
+ */
+GDN_API gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
+                           const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *beta,
+                           void *out, int out_dtype, void *stream);
+
+/*
+ * Synchronise `stream` and return (and clear) the device-side error word the
+ * kernels set when a bounded wait gives up (GDN_ERR_TIMEOUT) or an internal
+ * check fails (GDN_ERR_INTERNAL).  GDN_OK when nothing was recorded.
+ */
+GDN_API gdn_status gdn_device_error(void *stream);
+
+/* Static, human-readable name of a status code. */
+GDN_API const char *gdn_status_string(gdn_status status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+GDN_API int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,119 @@
+"""Host-only checks of the C ABI: the library loads, exports every symbol that
+include/gdn.h declares, and rejects invalid arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_deltanet_linear_03_gb300 import _build, gdn
+    _build.build()
+    return gdn.load_library()
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    return set(re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", text))
+
+
+def test_header_declares_the_binding_exports():
+    from gated_deltanet_linear_03_gb300 import gdn
+    assert header_symbols() == set(gdn.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in header_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.gdn_version() >= 100
+    for code in range(8):
+        s = lib.gdn_status_string(code).decode()
+        assert s.startswith("GDN_")
+    assert lib.gdn_status_string(99).decode() == "unknown gdn_status"
+
+
+def _cu(vals):
+    return (ctypes.c_int32 * len(vals))(*vals)
+
+
+FAKE = 0x10000  # an aligned address that is never dereferenced: validation fails first
+
+
+def prefill(lib, **kw):
+    a = dict(n_seqs=1, T=64, hk=1, hv=2, dk=128, dv=128, q=FAKE, k=FAKE * 2, v=FAKE * 3, la=FAKE * 4,
+             b=FAKE * 5, s0=None, cu=FAKE * 6, cu_host=_cu([0, 64]), out=FAKE * 7, odt=0, fin=None,
+             algo=1, ws=None, wsb=0)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.gdn_prefill(a["n_seqs"], a["T"], a["hk"], a["hv"], a["dk"], a["dv"], P(a["q"]), P(a["k"]),
+                           P(a["v"]), P(a["la"]), P(a["b"]), P(a["s0"]), P(a["cu"]), a["cu_host"], P(a["out"]),
+                           a["odt"], P(a["fin"]), a["algo"], P(a["ws"]), a["wsb"], None)
+
+
+def test_prefill_rejects_bad_heads(lib):
+    assert prefill(lib, hk=3, hv=4) == 1          # hv % hk
+    assert prefill(lib, dk=48, dv=48) == 2        # unsupported head size
+    assert prefill(lib, dk=128, dv=64) == 2       # dk != dv
+    assert prefill(lib, hk=0) == 1
+
+
+def test_prefill_rejects_bad_cu_seqlens(lib):
+    assert prefill(lib, cu_host=_cu([0, 65])) == 1               # does not end at T
+    assert prefill(lib, n_seqs=2, cu_host=_cu([0, 40, 30])) == 1  # decreasing
+    assert prefill(lib, cu_host=_cu([1, 64])) == 1                # does not start at 0
+    assert prefill(lib, cu_host=None) == 1
+    assert prefill(lib, cu=None) == 1
+    assert prefill(lib, n_seqs=0, cu_host=_cu([0])) == 1
+
+
+def test_prefill_rejects_bad_dtype_algo_pointers(lib):
+    assert prefill(lib, odt=7) == 2
+    assert prefill(lib, algo=5) == 2
+    assert prefill(lib, q=None) == 1
+    assert prefill(lib, q=FAKE + 4) == 3          # misaligned
+    assert prefill(lib, out=FAKE * 2) == 1        # out overlaps k
+    assert prefill(lib, fin=FAKE * 3, s0=FAKE * 40) == 1   # final_state overlaps v
+
+
+def test_chunked_requires_workspace(lib):
+    st = ctypes.c_int(-1)
+    need = lib.gdn_prefill_workspace_size(1, 64, 1, 2, 128, 128, _cu([0, 64]), 0, ctypes.byref(st))
+    assert st.value == 0
+    if need > 0:
+        assert prefill(lib, algo=0, ws=None, wsb=0) == 7
+        assert prefill(lib, algo=0, ws=FAKE * 1000, wsb=need - 1) == 7
+        assert prefill(lib, algo=0, ws=FAKE * 1000 + 16, wsb=need) == 3   # not 256-byte aligned
+
+
+def test_workspace_size_validation(lib):
+    st = ctypes.c_int(-1)
+    assert lib.gdn_prefill_workspace_size(1, 64, 1, 2, 128, 128, _cu([0, 64]), 1, ctypes.byref(st)) == 0
+    assert st.value == 0
+    assert lib.gdn_prefill_workspace_size(1, 64, 3, 2, 128, 128, _cu([0, 64]), 0, ctypes.byref(st)) == 0
+    assert st.value == 1
+    assert lib.gdn_prefill_workspace_size(1, 64, 1, 2, 128, 128, _cu([0, 64]), 9, ctypes.byref(st)) == 0
+    assert st.value == 2
+
+
+def test_decode_rejects_bad_args(lib):
+    P = ctypes.c_void_p
+
+    def dec(n=1, hk=1, hv=2, d=128, state=FAKE, q=FAKE * 2, k=FAKE * 3, v=FAKE * 4, la=FAKE * 5, b=FAKE * 6,
+            out=FAKE * 7, odt=0):
+        return lib.gdn_decode_step(n, hk, hv, d, d, P(state), P(q), P(k), P(v), P(la), P(b), P(out), odt, None)
+
+    assert dec(hk=3, hv=4) == 1
+    assert dec(d=96) == 2
+    assert dec(n=-1) == 1
+    assert dec(n=0) == 0                     # nothing to do, nothing launched
+    assert dec(state=None) == 1
+    assert dec(q=FAKE + 8) == 3
+    assert dec(odt=3) == 2
+    assert dec(out=FAKE) == 1                # out overlaps state
