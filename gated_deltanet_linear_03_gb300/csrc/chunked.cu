@@ -264,16 +264,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         const float *Ah = reinterpret_cast<const float *>(sm + PREP_A);
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-            float acc = (i == j) ? 1.f : 0.f;
+            // four partial sums keep the dependent FMA chains short
+            float a0 = (i == j) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
             for (int k4 = 0; k4 < i; k4 += 4) {   // A_ik = 0 for k >= i and tc[k] = 0 before it is set
                 const float4 a = *reinterpret_cast<const float4 *>(Ah + i * A_LD + k4);
-                acc = fmaf(-a.x, tc[k4 + 0], acc);
-                acc = fmaf(-a.y, tc[k4 + 1], acc);
-                acc = fmaf(-a.z, tc[k4 + 2], acc);
-                acc = fmaf(-a.w, tc[k4 + 3], acc);
+                a0 = fmaf(-a.x, tc[k4 + 0], a0);
+                a1 = fmaf(-a.y, tc[k4 + 1], a1);
+                a2 = fmaf(-a.z, tc[k4 + 2], a2);
+                a3 = fmaf(-a.w, tc[k4 + 3], a3);
             }
-            tc[i] = acc;
+            tc[i] = (a0 + a1) + (a2 + a3);
         }
     }
     __syncthreads();  // A is no longer read: its space takes the (Gamma T)^T tiles
@@ -434,6 +435,74 @@ __device__ __forceinline__ void pass_issue_loads(uint8_t *st, uint64_t *bar, con
     tma_load_2d(st + ST_RL, rlmap, bar, 0, (gc * hv + h) * C);
 }
 
+// Per-chunk inputs that are read with plain loads (gates, beta, this thread's v
+// row); loaded one chunk ahead so that their latency is off the state chain.
+struct ChunkInputs {
+    float la0, la1;   // log_alpha of tokens 2*lane, 2*lane+1 (raw; 0 past the end)
+    float b;          // beta of this thread's token row (warps 2, 3)
+    uint4 v[DS / 8];  // 32 bf16 of this thread's v row slice (warps 2, 3)
+};
+
+__device__ __forceinline__ void load_chunk_inputs(ChunkInputs &in, const float *__restrict__ log_alpha,
+                                                  const float *__restrict__ beta, const __nv_bfloat16 *__restrict__ v,
+                                                  int t0, int L, int hv, int h, int row0, int lane, int warp, int i) {
+    const int i0 = 2 * lane, i1 = 2 * lane + 1;
+    in.la0 = i0 < L ? log_alpha[(size_t)(t0 + i0) * hv + h] : 0.f;
+    in.la1 = i1 < L ? log_alpha[(size_t)(t0 + i1) * hv + h] : 0.f;
+    in.b = 0.f;
+#pragma unroll
+    for (int q4 = 0; q4 < DS / 8; ++q4) in.v[q4] = make_uint4(0, 0, 0, 0);
+    if (warp >= 2 && i < L) {
+        in.b = beta[(size_t)(t0 + i) * hv + h];
+        const uint4 *vp = reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + i) * hv + h) * D + row0);
+#pragma unroll
+        for (int q4 = 0; q4 < DS / 8; ++q4) in.v[q4] = vp[q4];
+    }
+}
+
+// Inclusive cumulative log-decay from already loaded pairs (see chunk_cumsum).
+__device__ __forceinline__ float2 cumsum_pairs(float la0_raw, float la1_raw, int len, int lane) {
+    const int i0 = 2 * lane, i1 = 2 * lane + 1;
+    const float la0 = i0 < len ? fminf(clamp_log_alpha(la0_raw), 0.f) : 0.f;
+    const float la1 = i1 < len ? fminf(clamp_log_alpha(la1_raw), 0.f) : 0.f;
+    const float pair = la0 + la1;
+    float incl = pair;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const float excl = incl - pair;
+    return make_float2(excl + la0, excl + la0 + la1);
+}
+
+// Outputs of one chunk: O_i = e^{g_i} (Q S^T)_i (in qs) + (R X)_i (TMEM columns 128..191).
+__device__ __forceinline__ void store_outputs(float (&qs)[DS], uint32_t tmem_row, int i, int L, int t0, int hv,
+                                              int h, int row0, void *__restrict__ out, int out_f32) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        float a[16], b[16];
+        tmem_ld16(tmem_row + 128 + half * 16, a);   // R_hi X_hi + R_lo X_hi
+        tmem_ld16(tmem_row + 160 + half * 16, b);   // R_hi X_lo
+#pragma unroll
+        for (int e = 0; e < 16; ++e) qs[half * 16 + e] += a[e] + b[e];
+    }
+    if (i < L) {
+        const size_t o = ((size_t)(t0 + i) * hv + h) * D + row0;
+        if (out_f32) {
+            float4 *op = reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + o);
+#pragma unroll
+            for (int e = 0; e < DS / 4; ++e) op[e] = make_float4(qs[4 * e], qs[4 * e + 1], qs[4 * e + 2], qs[4 * e + 3]);
+        } else {
+            uint4 *op = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(out) + o);
+#pragma unroll
+            for (int e = 0; e < DS / 8; ++e)
+                op[e] = make_uint4(pack_bf16(qs[8 * e], qs[8 * e + 1]), pack_bf16(qs[8 * e + 2], qs[8 * e + 3]),
+                                   pack_bf16(qs[8 * e + 4], qs[8 * e + 5]), pack_bf16(qs[8 * e + 6], qs[8 * e + 7]));
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads)
 state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
@@ -455,6 +524,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     const int hq = h / (hv / hk);
     const int row0 = slice * DS;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i = tid & 63;   // token row of this thread in the D1 / D4 accumulators
     const uint32_t base = smem_u32(sm);
 
     int ta, tb;
@@ -480,10 +550,11 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             tma_prefetch_desc(&plmap);
             tma_prefetch_desc(&rhmap);
             tma_prefetch_desc(&rlmap);
-        }
-        if (ok && nchunks > 0)
             pass_issue_loads(sm, &bar_tma[0], &qmap, &kmap, &phmap, &plmap, &rhmap, &rlmap, hq, ta, gc0, hv, h);
+        }
     }
+    ChunkInputs nxt;
+    if (ok && nchunks > 0) load_chunk_inputs(nxt, log_alpha, beta, v, ta, min(C, tb - ta), hv, h, row0, lane, warp, i);
 
     // state columns: thread d = tid holds S[row0 + r][d] for r < 32
     const int d = tid;
@@ -492,10 +563,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 #pragma unroll
     for (int r = 0; r < DS; ++r) S[r] = init_state ? init_state[sbase + (size_t)r * D] : 0.f;
 
-    // zero the padding rows of both R tiles once (rows 64..127 feed only unused accumulator rows)
+    // zero the padding rows of the R tiles once (rows 64..127 feed only unused accumulator rows)
     for (int x = tid; x < 4 * 512; x += kThreads) {
-        const int s = x / 1024, t = (x / 512) & 1, o = x % 512;
-        reinterpret_cast<uint4 *>(sm + s * PASS_STAGE + (t ? ST_RL : ST_RH) + 8192)[o] = make_uint4(0, 0, 0, 0);
+        const int st = x / 1024, t = (x / 512) & 1, o = x % 512;
+        reinterpret_cast<uint4 *>(sm + st * PASS_STAGE + (t ? ST_RL : ST_RH) + 8192)[o] = make_uint4(0, 0, 0, 0);
     }
 
     auto write_sop = [&]() {
@@ -517,15 +588,19 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     const uint32_t tmem = tmem_slot;
     const uint32_t tlane = (uint32_t)(32 * warp) << 16;
 
-    int c = 0;
+    float qs[DS];
+    int c = 0, prev_t0 = 0, prev_L = 0;
     for (; ok && c < nchunks; ++c) {
         const int s = c & 1;
         const int t0 = ta + c * C, L = min(C, tb - t0);
         const int gc = gc0 + c;
+        const ChunkInputs cur = nxt;
 
         if (tid == 0 && c + 1 < nchunks)
             pass_issue_loads(sm + (s ^ 1) * PASS_STAGE, &bar_tma[s ^ 1], &qmap, &kmap, &phmap, &plmap, &rhmap,
                              &rlmap, hq, t0 + C, gc + 1, hv, h);
+        if (c + 1 < nchunks)
+            load_chunk_inputs(nxt, log_alpha, beta, v, t0 + C, min(C, tb - t0 - C), hv, h, row0, lane, warp, i);
 
         ok = mbar_wait(&bar_tma[s], (c >> 1) & 1);
         ok = __syncthreads_and(ok);
@@ -540,58 +615,46 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                          smem_desc(sop + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSW), idesc, kk > 0);
             mma_commit(&bar_mma);
         }
+        // outputs of the previous chunk, while this chunk's first MMA runs
+        if (c > 0 && warp < 2) store_outputs(qs, tmem + tlane, i, prev_L, prev_t0, hv, h, row0, out, out_f32);
 
-        // gates of this chunk (every warp computes the cumulative sum for all 64 tokens)
-        const float2 g2 = chunk_cumsum(log_alpha, t0, L, hv, h, lane);
+        const float2 g2 = cumsum_pairs(cur.la0, cur.la1, L, lane);
         const float gL = g_of(g2, L - 1);
-        const int i = tid & 63;                // token row of this thread in the D1/D4 halves
         const float gi = g_of(g2, i);
-        float vrow[DS];
-        float bi = 0.f;
-        if (warp >= 2) {
-            if (i < L) {
-                bi = beta[(size_t)(t0 + i) * hv + h];
-                const uint4 *vp = reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + i) * hv + h) * D + row0);
-#pragma unroll
-                for (int q4 = 0; q4 < DS / 8; ++q4) {
-                    const uint4 x = vp[q4];
-                    vrow[q4 * 8 + 0] = bf16_lo(x.x); vrow[q4 * 8 + 1] = bf16_hi(x.x);
-                    vrow[q4 * 8 + 2] = bf16_lo(x.y); vrow[q4 * 8 + 3] = bf16_hi(x.y);
-                    vrow[q4 * 8 + 4] = bf16_lo(x.z); vrow[q4 * 8 + 5] = bf16_hi(x.z);
-                    vrow[q4 * 8 + 6] = bf16_lo(x.w); vrow[q4 * 8 + 7] = bf16_hi(x.w);
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < DS; ++r) vrow[r] = 0.f;
-            }
-        }
 
         ok = mbar_wait(&bar_mma, 0);
+        tc_fence_before();
         ok = __syncthreads_and(ok);
         if (!ok) break;
         tc_fence_after();
 
-        float qs[DS];
         {
             float a[16], b[16];
             const float eg = expf(gi);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                tmem_ld16(tmem + tlane + half * 16, a);         // x S_hi^T, columns 16*half..
+                tmem_ld16(tmem + tlane + half * 16, a);         // x S_hi^T
                 tmem_ld16(tmem + tlane + 32 + half * 16, b);    // x S_lo^T
 #pragma unroll
                 for (int e = 0; e < 16; ++e) qs[half * 16 + e] = a[e] + b[e];
             }
             if (warp >= 2) {
                 // X_i = beta_i (v_i - e^{g_i} (K S^T)_i), split into bf16 hi/lo, column i of the X tile
-                const float be = bi * eg;
+                const float bi = cur.b, be = cur.b * eg;
 #pragma unroll
-                for (int r = 0; r < DS; ++r) {
-                    const float x = bi * vrow[r] - be * qs[r];
-                    __nv_bfloat16 hi, lo;
-                    split_bf16(x, hi, lo);
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + PASS_XOP + sw128_offset(r, i)) = hi;
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + PASS_XOP + sw128_offset(DS + r, i)) = lo;
+                for (int q4 = 0; q4 < DS / 8; ++q4) {
+                    const uint4 x = cur.v[q4];
+                    const float vv[8] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y),
+                                         bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w)};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int r = q4 * 8 + e;
+                        const float xv = bi * vv[e] - be * qs[r];
+                        __nv_bfloat16 hi, lo;
+                        split_bf16(xv, hi, lo);
+                        *reinterpret_cast<__nv_bfloat16 *>(sm + PASS_XOP + sw128_offset(r, i)) = hi;
+                        *reinterpret_cast<__nv_bfloat16 *>(sm + PASS_XOP + sw128_offset(DS + r, i)) = lo;
+                    }
                 }
             } else {
 #pragma unroll
@@ -647,33 +710,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             }
         }
         write_sop();
-        // outputs: O_i = e^{g_i} (Q S^T)_i + (R X)_i for tokens i < L (warps 0, 1)
-        if (warp < 2) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float a[16], b[16];
-                tmem_ld16(tmem + tlane + 128 + half * 16, a);   // R_hi X_hi + R_lo X_hi
-                tmem_ld16(tmem + tlane + 160 + half * 16, b);   // R_hi X_lo
-#pragma unroll
-                for (int e = 0; e < 16; ++e) qs[half * 16 + e] += a[e] + b[e];
-            }
-            if (i < L) {
-                const size_t o = ((size_t)(t0 + i) * hv + h) * D + row0;
-                if (out_f32) {
-                    float4 *op = reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + o);
-#pragma unroll
-                    for (int e = 0; e < DS / 4; ++e)
-                        op[e] = make_float4(qs[4 * e], qs[4 * e + 1], qs[4 * e + 2], qs[4 * e + 3]);
-                } else {
-                    uint4 *op = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(out) + o);
-#pragma unroll
-                    for (int e = 0; e < DS / 8; ++e)
-                        op[e] = make_uint4(pack_bf16(qs[8 * e], qs[8 * e + 1]), pack_bf16(qs[8 * e + 2], qs[8 * e + 3]),
-                                           pack_bf16(qs[8 * e + 4], qs[8 * e + 5]),
-                                           pack_bf16(qs[8 * e + 6], qs[8 * e + 7]));
-                }
-            }
-        }
+        prev_t0 = t0;
+        prev_L = L;
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -686,9 +724,12 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             // let a prefetch that may still be in flight land before the CTA exits
             if (c + 1 < nchunks) mbar_wait(&bar_tma[(c + 1) & 1], ((c + 1) >> 1) & 1);
         }
-    } else if (final_state) {
+    } else {
+        if (nchunks > 0 && warp < 2) store_outputs(qs, tmem + tlane, i, prev_L, prev_t0, hv, h, row0, out, out_f32);
+        if (final_state) {
 #pragma unroll
-        for (int r = 0; r < DS; ++r) final_state[sbase + (size_t)r * D] = S[r];
+            for (int r = 0; r < DS; ++r) final_state[sbase + (size_t)r * D] = S[r];
+        }
     }
     tc_fence_before();
     __syncthreads();
