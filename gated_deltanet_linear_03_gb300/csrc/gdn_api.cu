@@ -75,6 +75,7 @@ size_t gdn_prefill_workspace_size(int n_seqs, int total_tokens, int hk, int hv, 
     gdn_status st = check_heads(hk, hv, dk, dv);
     if (st == GDN_OK) st = check_cu(n_seqs, total_tokens, cu_seqlens_host);
     if (st == GDN_OK && algo != GDN_ALGO_CHUNKED && algo != GDN_ALGO_SCAN) st = GDN_ERR_UNSUPPORTED;
+    if (st == GDN_OK && algo == GDN_ALGO_CHUNKED && dk != gdn::kChunkedHeadDim) st = GDN_ERR_UNSUPPORTED;
     if (status) *status = st;
     if (st != GDN_OK || algo == GDN_ALGO_SCAN) return 0;
     return gdn::chunked_workspace_bytes(n_seqs, cu_seqlens_host, hv, dk);
@@ -94,6 +95,7 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
     if ((st = check_cu(n_seqs, total_tokens, cu_seqlens_host)) != GDN_OK) return st;
     if (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
     if (algo != GDN_ALGO_CHUNKED && algo != GDN_ALGO_SCAN) return GDN_ERR_UNSUPPORTED;
+    if (algo == GDN_ALGO_CHUNKED && dk != gdn::kChunkedHeadDim) return GDN_ERR_UNSUPPORTED;
     if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !out)) return GDN_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, log_alpha, beta, init_state, cu_seqlens, out, final_state, workspace};

@@ -12,8 +12,9 @@ namespace gdn {
 
 // Lowest log-decay the GPU paths use; see the gdn.h note on log_alpha.
 constexpr float kLogAlphaFloor = -20.0f;
-// Chunk length of the blocked evaluation.
+// Chunk length of the blocked evaluation, and the head size its kernels implement.
 constexpr int kChunk = 64;
+constexpr int kChunkedHeadDim = 128;
 
 __device__ __forceinline__ float clamp_log_alpha(float la) { return fmaxf(la, kLogAlphaFloor); }
 

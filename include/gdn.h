@@ -37,7 +37,9 @@
  *     and returned synchronously; nothing is written in that case.  A launch
  *     failure returns GDN_ERR_CUDA.  Faults inside a kernel surface on a later
  *     synchronisation, as with any CUDA work.
- *   - Supported head sizes: dk == dv, and dk in {32, 64, 128}.
+ *   - Supported head sizes: dk == dv, and dk in {32, 64, 128} for GDN_ALGO_SCAN
+ *     and gdn_decode_step; dk == dv == 128 for GDN_ALGO_CHUNKED (other sizes
+ *     return GDN_ERR_UNSUPPORTED).
  */
 #ifndef GDN_H
 #define GDN_H

@@ -61,6 +61,7 @@ def test_prefill_rejects_bad_heads(lib):
     assert prefill(lib, hk=3, hv=4) == 1          # hv % hk
     assert prefill(lib, dk=48, dv=48) == 2        # unsupported head size
     assert prefill(lib, dk=128, dv=64) == 2       # dk != dv
+    assert prefill(lib, dk=64, dv=64, algo=0) == 2   # chunked path implements d = 128 only
     assert prefill(lib, hk=0) == 1
 
 
@@ -99,6 +100,8 @@ def test_workspace_size_validation(lib):
     assert lib.gdn_prefill_workspace_size(1, 64, 3, 2, 128, 128, _cu([0, 64]), 0, ctypes.byref(st)) == 0
     assert st.value == 1
     assert lib.gdn_prefill_workspace_size(1, 64, 1, 2, 128, 128, _cu([0, 64]), 9, ctypes.byref(st)) == 0
+    assert st.value == 2
+    assert lib.gdn_prefill_workspace_size(1, 64, 1, 2, 64, 64, _cu([0, 64]), 0, ctypes.byref(st)) == 0
     assert st.value == 2
 
 
