@@ -23,7 +23,8 @@ DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 
 # every symbol include/gdn.h declares
 EXPORTS = ("gdn_prefill", "gdn_prefill_chunked_phase", "gdn_prefill_workspace_size", "gdn_decode_step",
-           "gdn_device_error", "gdn_status_string", "gdn_version")
+           "gdn_device_error", "gdn_status_string", "gdn_version", "gdn_prefill_noalloc")
+NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024
 PHASE = {"prep": 1, "pass": 2}
 
 
@@ -50,6 +51,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdn_prefill.restype = I
     lib.gdn_prefill_chunked_phase.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, P, Z, P]
     lib.gdn_prefill_chunked_phase.restype = I
+    lib.gdn_prefill_noalloc.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, P]
+    lib.gdn_prefill_noalloc.restype = I
     lib.gdn_prefill_workspace_size.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
     lib.gdn_prefill_workspace_size.restype = Z
     lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, P]
@@ -150,6 +153,42 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
                          _ptr(final_state), ALGO[algo], _ptr(workspace), ws_bytes, _stream_ptr(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill")
+    return out, final_state
+
+
+def prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,
+                    beta: torch.Tensor, cu_seqlens: torch.Tensor, *, init_state: Optional[torch.Tensor] = None,
+                    out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16, final_state=True,
+                    cu_seqlens_host: Optional[Sequence[int]] = None, stream=None):
+    """Run ``gdn_prefill_noalloc``: the chunked prefill using the library's fixed
+    scratch instead of a workspace (for callers that cannot allocate device
+    memory; see include/gdn.h for its size limit and sharing rules).
+    Returns ``(out, final_state)``; ``out``/``final_state`` are allocated here
+    only when not passed in."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(log_alpha, "log_alpha", torch.float32, 2)
+    _need(beta, "beta", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, hk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    n_seqs = cu_seqlens.numel() - 1
+    if init_state is not None:
+        _need(init_state, "init_state", torch.float32, 4)
+    if out is None:
+        out = torch.empty(T, hv, dv, device=q.device, dtype=out_dtype)
+    if final_state is True:
+        final_state = torch.empty(n_seqs, hv, dv, dk, device=q.device, dtype=torch.float32)
+    elif final_state is False:
+        final_state = None
+    cu_arr, _ = _host_cu(cu_seqlens, cu_seqlens_host)
+    st = lib.gdn_prefill_noalloc(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                 _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out), DTYPE[out.dtype],
+                                 _ptr(final_state), _stream_ptr(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_prefill_noalloc")
     return out, final_state
 
 

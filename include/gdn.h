@@ -167,6 +167,38 @@ GDN_API gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float 
  */
 GDN_API gdn_status gdn_device_error(void *stream);
 
+/*
+ * gdn_prefill_noalloc: the chunked prefill (GDN_ALGO_CHUNKED) for callers that
+ * cannot allocate device memory, so cannot supply the workspace gdn_prefill
+ * needs: code that must not call cudaMalloc while it runs (an allocation can
+ * synchronise the device and stall other work), plugins whose host framework
+ * owns every device allocation, and small runtimes without a device allocator.
+ * The paper has no counterpart; it is a packaging of gdn_prefill.
+ *
+ * Arguments, layouts and errors as for gdn_prefill, without algo and
+ * workspace.  The scratch is one library-owned device array of
+ * GDN_NOALLOC_SCRATCH_BYTES (96 MiB), held on every GPU that loads the library
+ * until the process exits:
+ *   - problems that need more scratch than that (gdn_prefill_workspace_size
+ *     with GDN_ALGO_CHUNKED above GDN_NOALLOC_SCRATCH_BYTES; e.g. more than
+ *     4096 tokens at 32 value heads) return GDN_ERR_WORKSPACE, nothing runs;
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device, with that device current); make
+ *     that first call before any CUDA stream capture;
+ *   - every call shares the array, which keeps the last call's contents;
+ *     calls whose GPU work overlaps in time (other streams, other host
+ *     threads) race on it and must be serialised by the caller;
+ *   - it calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (96ull * 1024ull * 1024ull)
+
+GDN_API gdn_status gdn_prefill_noalloc(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                                       const void *q, const void *k, const void *v,
+                                       const float *log_alpha, const float *beta,
+                                       const float *init_state,
+                                       const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                       void *out, int out_dtype, float *final_state, void *stream);
+
 /* Static, human-readable name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status status);
 
