@@ -436,11 +436,17 @@ def run_gb300(args):
 
 
 def load_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, when one exists for this kernel."""
+    """DRAM bytes (read + write) per launch from the committed ncu capture of this kernel, or None
+    when there is none or the kernel's source changed since it was taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
-            return json.load(f).get(kernel)
+            rec = json.load(f).get(kernel)
+        src = os.path.join(ROOT, "gated_deltanet_linear_03_gb300", "csrc", rec["source"])
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["source_sha"]:
+            return None
+        return rec["bytes"]
     except Exception:
         return None
 
