@@ -97,10 +97,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return lo | (hi << 16);
 }
 
-__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
-    hi = __float2bfloat16_rn(x);
-    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+// Split 8 floats into bf16 hi and lo parts packed as two 16-byte vectors (x = hi + lo to ~16 bits).
+__device__ __forceinline__ void split8_bf16(const float *x, uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        const float2 back = __bfloat1622float2(hh);
+        const __nv_bfloat162 ll = __floats2bfloat162_rn(x[2 * e] - back.x, x[2 * e + 1] - back.y);
+        h[e] = *reinterpret_cast<const uint32_t *>(&hh);
+        l[e] = *reinterpret_cast<const uint32_t *>(&ll);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
+
 
 // Inclusive cumulative log-decay of the chunk for this warp: lane l covers
 // tokens 2l and 2l+1; tokens at or beyond `len` contribute 0 (their g equals
@@ -128,6 +139,7 @@ __device__ __forceinline__ float g_of(float2 g2, int i) {
     return (i & 1) ? b : a;
 }
 
+
 // ============================================================================
 // Kernel 1: per-chunk preparation (parallel over chunks x value heads)
 // ============================================================================
@@ -137,16 +149,77 @@ constexpr uint32_t PREP_KQ = 0;        // kb0: K rows | Q rows, kb1: K rows | Q 
 constexpr uint32_t PREP_A = 32768;     // fp32 A [64][68]; later (Gamma T)^T hi / lo
 constexpr int A_LD = 68;
 constexpr uint32_t PREP_AQK = PREP_A + 64 * A_LD * 4;   // 50176: Aqk hi, Aqk lo tiles [64 x 64] bf16
-constexpr uint32_t PREP_G = PREP_AQK + 16384;           // g [64], beta [64]
+constexpr uint32_t PREP_T = PREP_AQK + 16384;           // fp32 T = (I + A)^-1 [64][68]
+constexpr uint32_t PREP_Y = PREP_T + 64 * A_LD * 4;     // fp32 scratch [3][16][16]
+constexpr uint32_t PREP_G = PREP_Y + 3 * 256 * 4;       // g [64], beta [64]
 constexpr uint32_t PREP_SMEM = PREP_G + 512 + 1024;     // + alignment slack
 constexpr uint32_t PREP_TMEM_COLS = 128;
 
+// T = (I + A)^-1 for the strictly lower fp32 A (row stride A_LD), by 16 x 16 blocks, all 128 threads:
+//   diagonal blocks  T_II = (I + A_II)^-1            forward substitution, one column per thread
+//   below them       T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ   level by level in I (J < I in parallel)
+// T must be zero on entry.  Ends with the block synchronised.
+__device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict__ A, float *__restrict__ T,
+                                                         float *__restrict__ Y, int tid) {
+    if (tid < 64) {
+        const int j = tid, b = j >> 4, jj = j & 15;
+        const float *Ab = A + (16 * b) * A_LD + 16 * b;
+        float tc[16];
+#pragma unroll
+        for (int ii = 0; ii < 16; ++ii) {
+            float a0 = (ii == jj) ? 1.f : 0.f, a1 = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < ii; ++kk) {
+                if (kk & 1) a1 = fmaf(-Ab[ii * A_LD + kk], tc[kk], a1);
+                else a0 = fmaf(-Ab[ii * A_LD + kk], tc[kk], a0);
+            }
+            tc[ii] = a0 + a1;
+        }
+#pragma unroll
+        for (int ii = 0; ii < 16; ++ii) T[(16 * b + ii) * A_LD + j] = tc[ii];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int I = 1; I < 4; ++I) {
+        // Y_J = sum_{K=J}^{I-1} A_IK T_KJ for J < I: I * 256 elements, 2 I per thread (warp-uniform J)
+#pragma unroll
+        for (int m = 0; m < 2 * I; ++m) {
+            const int e = tid + 128 * m, J = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const float *arow = A + (16 * I + r) * A_LD;
+            float y0 = 0.f, y1 = 0.f;
+            for (int K = J; K < I; ++K) {
+#pragma unroll
+                for (int kk = 0; kk < 16; kk += 2) {
+                    y0 = fmaf(arow[16 * K + kk], T[(16 * K + kk) * A_LD + 16 * J + c], y0);
+                    y1 = fmaf(arow[16 * K + kk + 1], T[(16 * K + kk + 1) * A_LD + 16 * J + c], y1);
+                }
+            }
+            Y[J * 256 + r * 16 + c] = y0 + y1;
+        }
+        __syncthreads();
+        // T_IJ = -T_II Y_J
+#pragma unroll
+        for (int m = 0; m < 2 * I; ++m) {
+            const int e = tid + 128 * m, J = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const float *trow = T + (16 * I + r) * A_LD + 16 * I;
+            float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 16; kk += 2) {
+                t0 = fmaf(trow[kk], Y[J * 256 + kk * 16 + c], t0);
+                t1 = fmaf(trow[kk + 1], Y[J * 256 + (kk + 1) * 16 + c], t1);
+            }
+            T[(16 * I + r) * A_LD + 16 * J + c] = -(t0 + t1);
+        }
+        __syncthreads();
+    }
+}
+
 __global__ void __launch_bounds__(kThreads)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
+                  const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
                   const float *__restrict__ log_alpha, const float *__restrict__ beta,
-                  const int32_t *__restrict__ cu, int n_seqs, int total, int hk, int hv,
-                  __nv_bfloat16 *__restrict__ ws_phi, __nv_bfloat16 *__restrict__ ws_plo,
-                  __nv_bfloat16 *__restrict__ ws_rhi, __nv_bfloat16 *__restrict__ ws_rlo, unsigned int *err) {
+                  const int32_t *__restrict__ cu, int n_seqs, int total, int hk, int hv, unsigned int *err) {
     extern __shared__ uint8_t prep_raw[];
     uint8_t *sm = align1024(prep_raw);
     __shared__ uint64_t bar_tma, bar_mma;
@@ -187,6 +260,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         b_s[i0] = i0 < L ? beta[(size_t)(t0 + i0) * hv + h] : 0.f;
         b_s[i1] = i1 < L ? beta[(size_t)(t0 + i1) * hv + h] : 0.f;
     }
+    {   // T starts at zero (its strictly upper blocks stay zero)
+        float4 *t4 = reinterpret_cast<float4 *>(sm + PREP_T);
+        for (int x = tid; x < 64 * A_LD / 4; x += kThreads) t4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -197,10 +274,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     if (ok && tid == 0) {
         // D0[128 x 64] = [K ; Q] K^T  (rows 0-63: K K^T, rows 64-127: Q K^T), exact products
         const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
+        const uint64_t dkq = smem_desc(base + PREP_KQ, 16, 1024, kSW);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = base + PREP_KQ + (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16(tmem, smem_desc(off, 16, 1024, kSW), smem_desc(off, 16, 1024, kSW), idesc, kk > 0);
+            const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            mma_bf16(tmem, dkq + off, dkq + off, idesc, kk > 0);
         }
         mma_commit(&bar_mma);
     }
@@ -208,105 +286,81 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     ok = __syncthreads_and(ok);
     tc_fence_after();
 
-    if (ok) {
-        // A (fp32, strictly lower) from the K K^T rows; Aqk (split into bf16 hi/lo tiles) from Q K^T rows
+    // Warps 0-1 build A (fp32) from the K K^T rows; warps 2-3 build the Aqk tiles (split into bf16 hi/lo)
+    // from the Q K^T rows.  Then all warps solve for T and write the T operand tiles.
+    {
         const int i = tid & 63;
         float vals[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float v16[16];
-            tmem_ld16(tmem + tlane + c * 16, v16);
+        for (int c = 0; c < 4; c += 2) {
+            float a16[16], b16[16];
+            tmem_ld16x2(tmem + tlane + c * 16, tmem + tlane + (c + 1) * 16, a16, b16);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) vals[c * 16 + j] = v16[j];
+            for (int jj = 0; jj < 16; ++jj) {
+                vals[c * 16 + jj] = a16[jj];
+                vals[(c + 1) * 16 + jj] = b16[jj];
+            }
         }
         const float gi = g_s[i];
-        const bool row_ok = i < L;
-        if (tid < 64) {
+        const bool row_ok = ok && i < L;
+        if (warp < 2) {
             const float bi = b_s[i];
             float *arow = reinterpret_cast<float *>(sm + PREP_A) + i * A_LD;
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
+            for (int jj = 0; jj < 64; jj += 4) {
                 float4 a;
-                a.x = (row_ok && j + 0 < i) ? bi * expf(gi - g_s[j + 0]) * vals[j + 0] : 0.f;
-                a.y = (row_ok && j + 1 < i) ? bi * expf(gi - g_s[j + 1]) * vals[j + 1] : 0.f;
-                a.z = (row_ok && j + 2 < i) ? bi * expf(gi - g_s[j + 2]) * vals[j + 2] : 0.f;
-                a.w = (row_ok && j + 3 < i) ? bi * expf(gi - g_s[j + 3]) * vals[j + 3] : 0.f;
-                *reinterpret_cast<float4 *>(arow + j) = a;
+                a.x = (row_ok && jj + 0 < i) ? bi * __expf(gi - g_s[jj + 0]) * vals[jj + 0] : 0.f;
+                a.y = (row_ok && jj + 1 < i) ? bi * __expf(gi - g_s[jj + 1]) * vals[jj + 1] : 0.f;
+                a.z = (row_ok && jj + 2 < i) ? bi * __expf(gi - g_s[jj + 2]) * vals[jj + 2] : 0.f;
+                a.w = (row_ok && jj + 3 < i) ? bi * __expf(gi - g_s[jj + 3]) * vals[jj + 3] : 0.f;
+                *reinterpret_cast<float4 *>(arow + jj) = a;
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 64; j += 8) {
-                uint32_t hh[4], ll[4];
+            for (int jj = 0; jj < 64; jj += 8) {
+                float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float x0 = (row_ok && j + e <= i) ? expf(gi - g_s[j + e]) * vals[j + e] : 0.f;
-                    const float x1 = (row_ok && j + e + 1 <= i) ? expf(gi - g_s[j + e + 1]) * vals[j + e + 1] : 0.f;
-                    __nv_bfloat16 a0, b0, a1, b1;
-                    split_bf16(x0, a0, b0);
-                    split_bf16(x1, a1, b1);
-                    hh[e / 2] = (uint32_t)__bfloat16_as_ushort(a0) | ((uint32_t)__bfloat16_as_ushort(a1) << 16);
-                    ll[e / 2] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
-                }
-                const uint32_t off = sw128_offset(i, j);
-                *reinterpret_cast<uint4 *>(sm + PREP_AQK + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-                *reinterpret_cast<uint4 *>(sm + PREP_AQK + 8192 + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                for (int e = 0; e < 8; ++e)
+                    x[e] = (row_ok && jj + e <= i) ? __expf(gi - g_s[jj + e]) * vals[jj + e] : 0.f;
+                uint4 hi, lo;
+                split8_bf16(x, hi, lo);
+                const uint32_t off = sw128_offset(i, jj);
+                *reinterpret_cast<uint4 *>(sm + PREP_AQK + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + PREP_AQK + 8192 + off) = lo;
             }
         }
     }
     __syncthreads();
 
-    // T = (I + A)^-1, one column per thread (threads 0..63): T_ij = [i == j] - sum_{k<i} A_ik T_kj
-    const int j = tid;
-    float tc[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) tc[i] = 0.f;
-    if (ok && tid < 64) {
-        const float *Ah = reinterpret_cast<const float *>(sm + PREP_A);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            // four partial sums keep the dependent FMA chains short
-            float a0 = (i == j) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int k4 = 0; k4 < i; k4 += 4) {   // A_ik = 0 for k >= i and tc[k] = 0 before it is set
-                const float4 a = *reinterpret_cast<const float4 *>(Ah + i * A_LD + k4);
-                a0 = fmaf(-a.x, tc[k4 + 0], a0);
-                a1 = fmaf(-a.y, tc[k4 + 1], a1);
-                a2 = fmaf(-a.z, tc[k4 + 2], a2);
-                a3 = fmaf(-a.w, tc[k4 + 3], a3);
-            }
-            tc[i] = (a0 + a1) + (a2 + a3);
-        }
-    }
-    __syncthreads();  // A is no longer read: its space takes the (Gamma T)^T tiles
+    float *Tm = reinterpret_cast<float *>(sm + PREP_T);
+    solve_unit_lower_blocked(reinterpret_cast<const float *>(sm + PREP_A), Tm,
+                             reinterpret_cast<float *>(sm + PREP_Y), tid);
+    // (A is no longer read: its space takes the (Gamma T)^T tiles.)
 
-    // operand tiles, row j = column j of T: T^T hi/lo (for R) and (Gamma T)^T hi/lo (for P)
-    if (ok && tid < 64) {
+    // Operand tiles: row j of T^T (for R) and of (Gamma T)^T (for P) is column j of T, split into bf16 hi/lo.
+    // Thread t writes row j = t / 2, columns i in [32 (t % 2), 32 (t % 2) + 32).
+    if (ok) {
+        const int j = tid >> 1, i0 = (tid & 1) * 32;
         const float gl = g_s[L - 1];
         uint8_t *tth = sm + PREP_KQ + 8192, *ttl = sm + PREP_KQ + 24576;   // over the Q rows
         uint8_t *gth = sm + PREP_A, *gtl = sm + PREP_A + 8192;
 #pragma unroll
-        for (int c8 = 0; c8 < 64; c8 += 8) {
-            uint32_t th[4], tl[4], hh[4], ll[4];
+        for (int c8 = 0; c8 < 32; c8 += 8) {
+            float t8[8], g8[8];
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const int i0 = c8 + e, i1 = c8 + e + 1;
-                __nv_bfloat16 a0, b0, a1, b1;
-                split_bf16(tc[i0], a0, b0);
-                split_bf16(tc[i1], a1, b1);
-                th[e / 2] = (uint32_t)__bfloat16_as_ushort(a0) | ((uint32_t)__bfloat16_as_ushort(a1) << 16);
-                tl[e / 2] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
-                const float x0 = i0 < L ? expf(gl - g_s[i0]) * tc[i0] : 0.f;
-                const float x1 = i1 < L ? expf(gl - g_s[i1]) * tc[i1] : 0.f;
-                split_bf16(x0, a0, b0);
-                split_bf16(x1, a1, b1);
-                hh[e / 2] = (uint32_t)__bfloat16_as_ushort(a0) | ((uint32_t)__bfloat16_as_ushort(a1) << 16);
-                ll[e / 2] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
+            for (int e = 0; e < 8; ++e) {
+                const int ii = i0 + c8 + e;
+                t8[e] = Tm[ii * A_LD + j];
+                g8[e] = ii < L ? __expf(gl - g_s[ii]) * t8[e] : 0.f;
             }
-            const uint32_t off = sw128_offset(j, c8);
-            *reinterpret_cast<uint4 *>(tth + off) = make_uint4(th[0], th[1], th[2], th[3]);
-            *reinterpret_cast<uint4 *>(ttl + off) = make_uint4(tl[0], tl[1], tl[2], tl[3]);
-            *reinterpret_cast<uint4 *>(gth + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-            *reinterpret_cast<uint4 *>(gtl + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+            const uint32_t off = sw128_offset(j, i0 + c8);
+            uint4 hi, lo;
+            split8_bf16(t8, hi, lo);
+            *reinterpret_cast<uint4 *>(tth + off) = hi;
+            *reinterpret_cast<uint4 *>(ttl + off) = lo;
+            split8_bf16(g8, hi, lo);
+            *reinterpret_cast<uint4 *>(gth + off) = hi;
+            *reinterpret_cast<uint4 *>(gtl + off) = lo;
         }
     }
     fence_proxy_async_smem();
@@ -317,29 +371,25 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     if (ok && tid == 0) {
         // P = K^T (Gamma T): A = K tile read MN-major (M = dk = 128), B = (Gamma T)^T hi then lo
         const uint32_t idp = idesc_bf16_f32(128, 64, true, false);
-        const uint32_t gth = base + PREP_A, gtl = base + PREP_A + 8192;
+        const uint64_t dk_mn = smem_desc(base + PREP_KQ, 16384, 1024, kSW);
+        const uint64_t dgth = smem_desc(base + PREP_A, 16, 1024, kSW);
+        const uint64_t dgtl = smem_desc(base + PREP_A + 8192, 16, 1024, kSW);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem + 64, smem_desc(base + PREP_KQ + kk * 2048, 16384, 1024, kSW),
-                     smem_desc(gth + kk * 32, 16, 1024, kSW), idp, kk > 0);
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem + 64, dk_mn + 128 * kk, dgth + 2 * kk, idp, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem + 64, smem_desc(base + PREP_KQ + kk * 2048, 16384, 1024, kSW),
-                     smem_desc(gtl + kk * 32, 16, 1024, kSW), idp, 1);
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem + 64, dk_mn + 128 * kk, dgtl + 2 * kk, idp, 1);
         // R = Aqk T (M = 64): Aqk_hi T_hi + Aqk_hi T_lo + Aqk_lo T_hi
         const uint32_t idr = idesc_bf16_f32(64, 64, false, false);
-        const uint32_t ah = base + PREP_AQK, al = base + PREP_AQK + 8192;
-        const uint32_t th = base + PREP_KQ + 8192, tl = base + PREP_KQ + 24576;
+        const uint64_t dah = smem_desc(base + PREP_AQK, 16, 1024, kSW);
+        const uint64_t dal = smem_desc(base + PREP_AQK + 8192, 16, 1024, kSW);
+        const uint64_t dth = smem_desc(base + PREP_KQ + 8192, 16, 1024, kSW);
+        const uint64_t dtl = smem_desc(base + PREP_KQ + 24576, 16, 1024, kSW);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem, smem_desc(ah + kk * 32, 16, 1024, kSW), smem_desc(th + kk * 32, 16, 1024, kSW), idr,
-                     kk > 0);
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem, dah + 2 * kk, dth + 2 * kk, idr, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem, smem_desc(ah + kk * 32, 16, 1024, kSW), smem_desc(tl + kk * 32, 16, 1024, kSW), idr, 1);
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem, dah + 2 * kk, dtl + 2 * kk, idr, 1);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem, smem_desc(al + kk * 32, 16, 1024, kSW), smem_desc(th + kk * 32, 16, 1024, kSW), idr, 1);
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem, dal + 2 * kk, dth + 2 * kk, idr, 1);
         mma_commit(&bar_mma);
     }
     if (ok) ok = mbar_wait(&bar_mma, 1);
@@ -347,55 +397,51 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     tc_fence_after();
 
     if (ok) {
-        // P rows: lane d = tid holds P[d][0..63]; written as bf16 hi / lo rows of 128 bytes
-        const size_t prow = ((size_t)gc * hv + h) * D + tid;
-        uint4 *dh = reinterpret_cast<uint4 *>(ws_phi + prow * C);
-        uint4 *dl = reinterpret_cast<uint4 *>(ws_plo + prow * C);
+        // Stage P (rows d = lane, 64 columns) and R (rows 16*warp + lane for lane < 16, M = 64 accumulator) as
+        // bf16 hi / lo tiles in the same 128B-swizzled layout the TMA maps use, over operand tiles that the
+        // finished MMAs no longer read, then store each tile with one bulk tensor store.
+        uint8_t *sph = sm + PREP_KQ, *spl = sm + PREP_KQ + 16384;     // 16 KiB each
+        uint8_t *srh = sm + PREP_A, *srl = sm + PREP_A + 8192;        // 8 KiB each
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float v16[16];
-            tmem_ld16(tmem + tlane + 64 + c * 16, v16);
+        for (int c = 0; c < 4; c += 2) {
+            float a[16], b[16];
+            tmem_ld16x2(tmem + tlane + 64 + c * 16, tmem + tlane + 64 + (c + 1) * 16, a, b);
 #pragma unroll
-            for (int q8 = 0; q8 < 2; ++q8) {
-                uint32_t hh[4], ll[4];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    __nv_bfloat16 a0, b0, a1, b1;
-                    split_bf16(v16[q8 * 8 + e], a0, b0);
-                    split_bf16(v16[q8 * 8 + e + 1], a1, b1);
-                    hh[e / 2] = (uint32_t)__bfloat16_as_ushort(a0) | ((uint32_t)__bfloat16_as_ushort(a1) << 16);
-                    ll[e / 2] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
-                }
-                dh[c * 2 + q8] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-                dl[c * 2 + q8] = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+            for (int q = 0; q < 4; ++q) {
+                uint4 hi, lo;
+                split8_bf16(q < 2 ? a + 8 * q : b + 8 * (q - 2), hi, lo);
+                const uint32_t off = sw128_offset(tid, c * 16 + 8 * q);
+                *reinterpret_cast<uint4 *>(sph + off) = hi;
+                *reinterpret_cast<uint4 *>(spl + off) = lo;
             }
         }
-        // R rows (M = 64 accumulator): row 16*warp + lane sits in lane 32*warp + lane for lane < 16
         const int r = 16 * warp + lane;
-        const size_t rrow = ((size_t)gc * hv + h) * C + r;
-        uint4 *rh = reinterpret_cast<uint4 *>(ws_rhi + rrow * C);
-        uint4 *rl = reinterpret_cast<uint4 *>(ws_rlo + rrow * C);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float v16[16];
-            tmem_ld16(tmem + tlane + c * 16, v16);
+        for (int c = 0; c < 4; c += 2) {
+            float a[16], b[16];
+            tmem_ld16x2(tmem + tlane + c * 16, tmem + tlane + (c + 1) * 16, a, b);
             if (lane < 16) {
 #pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8) {
-                    uint32_t hh[4], ll[4];
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        __nv_bfloat16 a0, b0, a1, b1;
-                        split_bf16(v16[q8 * 8 + e], a0, b0);
-                        split_bf16(v16[q8 * 8 + e + 1], a1, b1);
-                        hh[e / 2] = (uint32_t)__bfloat16_as_ushort(a0) | ((uint32_t)__bfloat16_as_ushort(a1) << 16);
-                        ll[e / 2] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
-                    }
-                    rh[c * 2 + q8] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-                    rl[c * 2 + q8] = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                for (int q = 0; q < 4; ++q) {
+                    uint4 hi, lo;
+                    split8_bf16(q < 2 ? a + 8 * q : b + 8 * (q - 2), hi, lo);
+                    const uint32_t off = sw128_offset(r, c * 16 + 8 * q);
+                    *reinterpret_cast<uint4 *>(srh + off) = hi;
+                    *reinterpret_cast<uint4 *>(srl + off) = lo;
                 }
             }
         }
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (ok && tid == 0) {
+        const int prow = (gc * hv + h) * D, rrow = (gc * hv + h) * C;
+        tma_store_2d(&phmap, sm + PREP_KQ, 0, prow);
+        tma_store_2d(&plmap, sm + PREP_KQ + 16384, 0, prow);
+        tma_store_2d(&rhmap, sm + PREP_A, 0, rrow);
+        tma_store_2d(&rlmap, sm + PREP_A + 8192, 0, rrow);
+        tma_store_commit();
+        tma_store_wait_read();
     } else if (tid == 0) {
         raise_error(err, kErrTimeout);
     }
@@ -408,7 +454,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 // ============================================================================
 // Kernel 2: state passing + outputs (sequential over chunks)
 // ============================================================================
-// One pipeline stage: Q|K 32 KiB, P_hi 16, P_lo 16, R_hi 16, R_lo 16 KiB (the R tiles hold 64 rows
+// One pipeline stage: Q|K 32 KiB, P_hi 16, P_lo 16, R_hi 16, R_lo 16 KiB (each R tile holds 64 rows
 // loaded per chunk and 64 zero rows, so that R feeds an M = 128 MMA whose upper rows are unused).
 constexpr uint32_t PASS_STAGE = 98304;
 constexpr uint32_t ST_QK = 0, ST_PH = 32768, ST_PL = 49152, ST_RH = 65536, ST_RL = 81920;
@@ -416,7 +462,15 @@ constexpr uint32_t PASS_SOP = 2 * PASS_STAGE;      // [S_hi ; S_lo] tile, 2 k-bl
 constexpr uint32_t PASS_XOP = PASS_SOP + 16384;    // [X_hi ; X_lo] tile [64 x 64] bf16
 constexpr uint32_t PASS_SMEM = PASS_XOP + 8192 + 1024;
 constexpr uint32_t kStageTx = 32768 + 16384 + 16384 + 8192 + 8192;
-constexpr uint32_t PASS_TMEM_COLS = 256;
+constexpr uint32_t PASS_TMEM_COLS = 512;
+// TMEM columns (each accumulator 64 columns: 32 for the S_hi / X_hi part, 32 for the S_lo / X_lo part):
+//   [Q;K] [S_hi;S_lo]^T  (M = 128 token rows: Q rows in lanes 0-63, K rows in 64-127), as four partial
+//                        accumulators of two K steps each, summed when read: a chain of small MMAs into
+//                        one accumulator serialises on the accumulator, independent ones overlap;
+//   P X                  (M = 128 = dk), as two partial accumulators (P_hi and P_lo);
+//   R X                  (M = 128, rows 0-63 valid), double-buffered by chunk parity so that a chunk's
+//                        outputs can be read while the next chunk's R X is computed.
+constexpr uint32_t TM_D1 = 0, TM_PX = 256, TM_RX = 384;
 
 __device__ __forceinline__ void pass_issue_loads(uint8_t *st, uint64_t *bar, const CUtensorMap *qmap,
                                                  const CUtensorMap *kmap, const CUtensorMap *phmap,
@@ -435,28 +489,31 @@ __device__ __forceinline__ void pass_issue_loads(uint8_t *st, uint64_t *bar, con
     tma_load_2d(st + ST_RL, rlmap, bar, 0, (gc * hv + h) * C);
 }
 
+constexpr int kPassThreads = 256;   // 8 warps: warps w and w + 4 share TMEM lane quadrant w % 4
+constexpr int DG = DS / 2;          // state rows per thread (the two warp groups split the 32 rows)
+
 // Per-chunk inputs that are read with plain loads (gates, beta, this thread's v
-// row); loaded one chunk ahead so that their latency is off the state chain.
+// row piece); loaded one chunk ahead so that their latency is off the state chain.
 struct ChunkInputs {
     float la0, la1;   // log_alpha of tokens 2*lane, 2*lane+1 (raw; 0 past the end)
-    float b;          // beta of this thread's token row (warps 2, 3)
-    uint4 v[DS / 8];  // 32 bf16 of this thread's v row slice (warps 2, 3)
+    float b;          // beta of this thread's token row (K-row threads)
+    uint4 v[DG / 8];  // 16 bf16 of this thread's v row piece (K-row threads)
 };
 
 __device__ __forceinline__ void load_chunk_inputs(ChunkInputs &in, const float *__restrict__ log_alpha,
                                                   const float *__restrict__ beta, const __nv_bfloat16 *__restrict__ v,
-                                                  int t0, int L, int hv, int h, int row0, int lane, int warp, int i) {
+                                                  int t0, int L, int hv, int h, int rowg, int lane, bool krow, int i) {
     const int i0 = 2 * lane, i1 = 2 * lane + 1;
     in.la0 = i0 < L ? log_alpha[(size_t)(t0 + i0) * hv + h] : 0.f;
     in.la1 = i1 < L ? log_alpha[(size_t)(t0 + i1) * hv + h] : 0.f;
     in.b = 0.f;
 #pragma unroll
-    for (int q4 = 0; q4 < DS / 8; ++q4) in.v[q4] = make_uint4(0, 0, 0, 0);
-    if (warp >= 2 && i < L) {
+    for (int q4 = 0; q4 < DG / 8; ++q4) in.v[q4] = make_uint4(0, 0, 0, 0);
+    if (krow && i < L) {
         in.b = beta[(size_t)(t0 + i) * hv + h];
-        const uint4 *vp = reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + i) * hv + h) * D + row0);
+        const uint4 *vp = reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + i) * hv + h) * D + rowg);
 #pragma unroll
-        for (int q4 = 0; q4 < DS / 8; ++q4) in.v[q4] = vp[q4];
+        for (int q4 = 0; q4 < DG / 8; ++q4) in.v[q4] = vp[q4];
     }
 }
 
@@ -476,34 +533,36 @@ __device__ __forceinline__ float2 cumsum_pairs(float la0_raw, float la1_raw, int
     return make_float2(excl + la0, excl + la0 + la1);
 }
 
-// Outputs of one chunk: O_i = e^{g_i} (Q S^T)_i (in qs) + (R X)_i (TMEM columns 128..191).
-__device__ __forceinline__ void store_outputs(float (&qs)[DS], uint32_t tmem_row, int i, int L, int t0, int hv,
-                                              int h, int row0, void *__restrict__ out, int out_f32) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        float a[16], b[16];
-        tmem_ld16(tmem_row + 128 + half * 16, a);   // R_hi X_hi + R_lo X_hi
-        tmem_ld16(tmem_row + 160 + half * 16, b);   // R_hi X_lo
-#pragma unroll
-        for (int e = 0; e < 16; ++e) qs[half * 16 + e] += a[e] + b[e];
-    }
+// Outputs of one chunk for this thread's token and 16 value rows (Q-row threads):
+// O_i = e^{g_i} (Q S^T)_i (in qs) + (R X)_i ((R_hi + R_lo) X_hi, and (R_hi + R_lo) X_lo).
+__device__ __forceinline__ void store_outputs(float (&qs)[DG], uint32_t tmem_rx, int grp, int i, int L, int t0,
+                                              int hv, int h, int rowg, void *__restrict__ out, int out_f32) {
+    float a[16], b[16];
+    tmem_ld16x2(tmem_rx + grp * 16, tmem_rx + 32 + grp * 16, a, b);
     if (i < L) {
-        const size_t o = ((size_t)(t0 + i) * hv + h) * D + row0;
+#pragma unroll
+        for (int e = 0; e < DG; ++e) qs[e] += a[e] + b[e];
+        const size_t o = ((size_t)(t0 + i) * hv + h) * D + rowg;
         if (out_f32) {
             float4 *op = reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + o);
 #pragma unroll
-            for (int e = 0; e < DS / 4; ++e) op[e] = make_float4(qs[4 * e], qs[4 * e + 1], qs[4 * e + 2], qs[4 * e + 3]);
+            for (int e = 0; e < DG / 4; ++e) op[e] = make_float4(qs[4 * e], qs[4 * e + 1], qs[4 * e + 2], qs[4 * e + 3]);
         } else {
             uint4 *op = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(out) + o);
 #pragma unroll
-            for (int e = 0; e < DS / 8; ++e)
+            for (int e = 0; e < DG / 8; ++e)
                 op[e] = make_uint4(pack_bf16(qs[8 * e], qs[8 * e + 1]), pack_bf16(qs[8 * e + 2], qs[8 * e + 3]),
                                    pack_bf16(qs[8 * e + 4], qs[8 * e + 5]), pack_bf16(qs[8 * e + 6], qs[8 * e + 7]));
         }
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
+// Thread roles (256 threads).  TMEM lane quadrant quad = warp % 4, row group grp = warp / 4 (which 16 of
+// the CTA's 32 value rows).  Lane l of quadrant quad is accumulator row 32 quad + l: for [Q;K] S^T and
+// R X that row is a token (Q rows for quad 0-1, K rows for quad 2-3); for P X it is state column d.
+// Q-row threads, which are off the X computation, issue: thread 0 the [Q;K] S^T and P X MMAs, thread
+// 128 the R X MMAs, thread 32 the TMA loads.
+__global__ void __launch_bounds__(kPassThreads, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
                   const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
@@ -514,7 +573,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                   unsigned int *err) {
     extern __shared__ uint8_t pass_raw[];
     uint8_t *sm = align1024(pass_raw);
-    __shared__ uint64_t bar_tma[2], bar_mma;
+    __shared__ uint64_t bar_tma[2], bar_d1, bar_px, bar_rx;
     __shared__ uint32_t tmem_slot;
 
     constexpr int SLICES = D / DS;
@@ -524,7 +583,12 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     const int hq = h / (hv / hk);
     const int row0 = slice * DS;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int i = tid & 63;   // token row of this thread in the D1 / D4 accumulators
+    const int quad = warp & 3, grp = warp >> 2;
+    const int lrow = 32 * quad + lane;     // TMEM lane of this thread
+    const int d = lrow;                    // state column (dk index) in P X
+    const int i = lrow & 63;               // token row in [Q;K] S^T and R X
+    const bool krow = quad >= 2;           // lanes 64..127 hold the K rows
+    const int rowg = row0 + grp * DG;      // first value row of this thread's group
     const uint32_t base = smem_u32(sm);
 
     int ta, tb;
@@ -533,6 +597,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     const int gc0 = first_chunk_of(cu, n, total);
     bool ok = gc0 + nchunks <= nch;
     if (!ok && tid == 0) raise_error(err, kErrInternal);
+    const bool started = ok && nchunks > 0;   // chunk 0's tiles are requested below
 
     if (warp == 0) {
         tmem_alloc(&tmem_slot, PASS_TMEM_COLS);
@@ -541,43 +606,45 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     if (tid == 0) {
         mbar_init(&bar_tma[0], 1);
         mbar_init(&bar_tma[1], 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_d1, 1);
+        mbar_init(&bar_px, 1);
+        mbar_init(&bar_rx, 1);
         fence_mbar_init();
-        if (ok && nchunks > 0) {
-            tma_prefetch_desc(&qmap);
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&phmap);
-            tma_prefetch_desc(&plmap);
-            tma_prefetch_desc(&rhmap);
-            tma_prefetch_desc(&rlmap);
-            pass_issue_loads(sm, &bar_tma[0], &qmap, &kmap, &phmap, &plmap, &rhmap, &rlmap, hq, ta, gc0, hv, h);
-        }
     }
-    ChunkInputs nxt;
-    if (ok && nchunks > 0) load_chunk_inputs(nxt, log_alpha, beta, v, ta, min(C, tb - ta), hv, h, row0, lane, warp, i);
-
-    // state columns: thread d = tid holds S[row0 + r][d] for r < 32
-    const int d = tid;
-    float S[DS];
-    const size_t sbase = (((size_t)n * hv + h) * D + row0) * D + d;
-#pragma unroll
-    for (int r = 0; r < DS; ++r) S[r] = init_state ? init_state[sbase + (size_t)r * D] : 0.f;
-
     // zero the padding rows of the R tiles once (rows 64..127 feed only unused accumulator rows)
-    for (int x = tid; x < 4 * 512; x += kThreads) {
+    for (int x = tid; x < 4 * 512; x += kPassThreads) {
         const int st = x / 1024, t = (x / 512) & 1, o = x % 512;
         reinterpret_cast<uint4 *>(sm + st * PASS_STAGE + (t ? ST_RL : ST_RH) + 8192)[o] = make_uint4(0, 0, 0, 0);
     }
+    __syncthreads();
+    if (tid == 32 && started) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&phmap);
+        tma_prefetch_desc(&plmap);
+        tma_prefetch_desc(&rhmap);
+        tma_prefetch_desc(&rlmap);
+        pass_issue_loads(sm, &bar_tma[0], &qmap, &kmap, &phmap, &plmap, &rhmap, &rlmap, hq, ta, gc0, hv, h);
+    }
+    ChunkInputs nxt;
+    if (started) load_chunk_inputs(nxt, log_alpha, beta, v, ta, min(C, tb - ta), hv, h, rowg, lane, krow, i);
 
-    auto write_sop = [&]() {
-        const int kb = d >> 6, col = d & 63;
-        uint8_t *t = sm + PASS_SOP + kb * 8192;
+    // state columns: thread (d, grp) holds S[rowg + r][d] for r < 16
+    float S[DG];
+    const size_t sbase = (((size_t)n * hv + h) * D + rowg) * D + d;
 #pragma unroll
-        for (int r = 0; r < DS; ++r) {
-            __nv_bfloat16 hi, lo;
-            split_bf16(S[r], hi, lo);
-            *reinterpret_cast<__nv_bfloat16 *>(t + sw128_offset(r, col)) = hi;
-            *reinterpret_cast<__nv_bfloat16 *>(t + sw128_offset(DS + r, col)) = lo;
+    for (int r = 0; r < DG; ++r) S[r] = init_state ? init_state[sbase + (size_t)r * D] : 0.f;
+
+    // The state operand [S_hi ; S_lo] is stored MN-major: row d (the dk index, K of the MMA) holds the 64
+    // values n = 0..31 (S_hi rows) and 32..63 (S_lo rows); this thread writes its 16 rows as two 16-byte
+    // pieces of each half.
+    auto write_sop = [&]() {
+#pragma unroll
+        for (int j = 0; j < DG / 8; ++j) {
+            uint4 hi, lo;
+            split8_bf16(&S[8 * j], hi, lo);
+            *reinterpret_cast<uint4 *>(sm + PASS_SOP + sw128_offset(d, grp * DG + 8 * j)) = hi;
+            *reinterpret_cast<uint4 *>(sm + PASS_SOP + sw128_offset(d, DS + grp * DG + 8 * j)) = lo;
         }
     };
     write_sop();
@@ -586,149 +653,174 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    const uint32_t tlane = (uint32_t)(32 * warp) << 16;
+    const uint32_t tlane = (uint32_t)(32 * quad) << 16;
 
-    float qs[DS];
+    // Shared-memory descriptors, built once by the issuing thread; a K step adds a byte offset >> 4 to
+    // the start field (all tiles sit far below 256 KiB, so the 14-bit field never carries).
+    uint64_t dQK0 = 0, dPH0 = 0, dPL0 = 0, dRH0 = 0, dRL0 = 0, dSOP = 0, dXOP = 0;
+    if (tid == 0 || tid == 128) {
+        dQK0 = smem_desc(base + ST_QK, 16, 1024, kSW);
+        dPH0 = smem_desc(base + ST_PH, 16, 1024, kSW);
+        dPL0 = smem_desc(base + ST_PL, 16, 1024, kSW);
+        dRH0 = smem_desc(base + ST_RH, 16, 1024, kSW);
+        dRL0 = smem_desc(base + ST_RL, 16, 1024, kSW);
+        dSOP = smem_desc(base + PASS_SOP, 8192, 1024, kSW);   // MN-major B: 16 K-rows per step = 2048 B
+        dXOP = smem_desc(base + PASS_XOP, 8192, 1024, kSW);
+    }
+    constexpr uint64_t kStageStep = PASS_STAGE >> 4;
+    constexpr uint32_t idb = idesc_bf16_f32(128, 64, false, true);   // A K-major, B MN-major, N = 64
+
+    float qs[DG];
     int c = 0, prev_t0 = 0, prev_L = 0;
     for (; ok && c < nchunks; ++c) {
         const int s = c & 1;
+        const uint32_t par = c & 1;
         const int t0 = ta + c * C, L = min(C, tb - t0);
         const int gc = gc0 + c;
         const ChunkInputs cur = nxt;
+        const uint64_t so = s * kStageStep;
 
-        if (tid == 0 && c + 1 < nchunks)
-            pass_issue_loads(sm + (s ^ 1) * PASS_STAGE, &bar_tma[s ^ 1], &qmap, &kmap, &phmap, &plmap, &rhmap,
-                             &rlmap, hq, t0 + C, gc + 1, hv, h);
-        if (c + 1 < nchunks)
-            load_chunk_inputs(nxt, log_alpha, beta, v, t0 + C, min(C, tb - t0 - C), hv, h, row0, lane, warp, i);
-
-        ok = mbar_wait(&bar_tma[s], (c >> 1) & 1);
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
         if (tid == 0) {
-            // D1[128 x 64] = [Q ; K] [S_hi ; S_lo]^T
-            const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
-            const uint32_t qk = base + s * PASS_STAGE + ST_QK, sop = base + PASS_SOP;
+            // D1[128 x 64] = [Q ; K] [S_hi ; S_lo]^T, once this chunk's tiles have landed
+            if (mbar_wait(&bar_tma[s], (c >> 1) & 1)) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem, smem_desc(qk + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSW),
-                         smem_desc(sop + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSW), idesc, kk > 0);
-            mma_commit(&bar_mma);
+                for (int kk = 0; kk < 8; ++kk) {   // K steps 2p, 2p+1 go to partial accumulator p
+                    const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                    mma_bf16(tmem + TM_D1 + 64 * (kk >> 1), dQK0 + so + off, dSOP + 128 * kk, idb, kk & 1);
+                }
+                mma_commit(&bar_d1);
+            } else {
+                ok = false;
+            }
+        } else if (tid == 32 && c + 1 < nchunks) {
+            // next chunk's tiles go to the other stage once its last reader (the previous R X) is done
+            if (c == 0 || mbar_wait(&bar_rx, par ^ 1))
+                pass_issue_loads(sm + (s ^ 1) * PASS_STAGE, &bar_tma[s ^ 1], &qmap, &kmap, &phmap, &plmap, &rhmap,
+                                 &rlmap, hq, t0 + C, gc + 1, hv, h);
+            else
+                ok = false;
         }
-        // outputs of the previous chunk, while this chunk's first MMA runs
-        if (c > 0 && warp < 2) store_outputs(qs, tmem + tlane, i, prev_L, prev_t0, hv, h, row0, out, out_f32);
+        if (c + 1 < nchunks)
+            load_chunk_inputs(nxt, log_alpha, beta, v, t0 + C, min(C, tb - t0 - C), hv, h, rowg, lane, krow, i);
 
         const float2 g2 = cumsum_pairs(cur.la0, cur.la1, L, lane);
         const float gL = g_of(g2, L - 1);
-        const float gi = g_of(g2, i);
+        const float eg = __expf(g_of(g2, i));
 
-        ok = mbar_wait(&bar_mma, 0);
-        tc_fence_before();
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
+        if (!mbar_wait(&bar_d1, par)) ok = false;
         tc_fence_after();
-
+        float qcur[DG];   // e^{g_i} (Q S^T)_i of this chunk (Q-row threads)
         {
-            float a[16], b[16];
-            const float eg = expf(gi);
+            float a[16], b[16];   // x S_hi^T and x S_lo^T, this group's 16 rows (sum of the partials)
+            tmem_ld16x2(tmem + tlane + TM_D1 + grp * 16, tmem + tlane + TM_D1 + 32 + grp * 16, a, b);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld16(tmem + tlane + half * 16, a);         // x S_hi^T
-                tmem_ld16(tmem + tlane + 32 + half * 16, b);    // x S_lo^T
+            for (int p = 1; p < 4; ++p) {
+                float a2[16], b2[16];
+                tmem_ld16x2(tmem + tlane + TM_D1 + 64 * p + grp * 16, tmem + tlane + TM_D1 + 64 * p + 32 + grp * 16,
+                            a2, b2);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) qs[half * 16 + e] = a[e] + b[e];
+                for (int e = 0; e < 16; ++e) {
+                    a[e] += a2[e];
+                    b[e] += b2[e];
+                }
             }
-            if (warp >= 2) {
-                // X_i = beta_i (v_i - e^{g_i} (K S^T)_i), split into bf16 hi/lo, column i of the X tile
+            if (krow) {
+                // X_i = beta_i (v_i - e^{g_i} (K S^T)_i), split into bf16 hi/lo.  The X tile is stored
+                // MN-major: row i (the token, K of the MMA) holds n = 0..31 (X_hi) and 32..63 (X_lo).
                 const float bi = cur.b, be = cur.b * eg;
 #pragma unroll
-                for (int q4 = 0; q4 < DS / 8; ++q4) {
+                for (int q4 = 0; q4 < DG / 8; ++q4) {
                     const uint4 x = cur.v[q4];
                     const float vv[8] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y),
                                          bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w)};
+                    float xv[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int r = q4 * 8 + e;
-                        const float xv = bi * vv[e] - be * qs[r];
-                        __nv_bfloat16 hi, lo;
-                        split_bf16(xv, hi, lo);
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + PASS_XOP + sw128_offset(r, i)) = hi;
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + PASS_XOP + sw128_offset(DS + r, i)) = lo;
-                    }
+                    for (int e = 0; e < 8; ++e) xv[e] = bi * vv[e] - be * (a[q4 * 8 + e] + b[q4 * 8 + e]);
+                    uint4 hi, lo;
+                    split8_bf16(xv, hi, lo);
+                    *reinterpret_cast<uint4 *>(sm + PASS_XOP + sw128_offset(i, grp * DG + 8 * q4)) = hi;
+                    *reinterpret_cast<uint4 *>(sm + PASS_XOP + sw128_offset(i, DS + grp * DG + 8 * q4)) = lo;
                 }
             } else {
 #pragma unroll
-                for (int r = 0; r < DS; ++r) qs[r] *= eg;       // e^{g_i} (Q S^T)_i
+                for (int r = 0; r < DG; ++r) qcur[r] = eg * (a[r] + b[r]);
+                // the previous chunk's R X must be complete before the next R X is issued (after the barrier
+                // below), so that waiting for it here can never see a later phase of the same barrier
+                if (c > 0 && !mbar_wait(&bar_rx, par ^ 1)) ok = false;
             }
         }
+        // X tile complete
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
 
         if (tid == 0) {
-            const uint32_t ph = base + s * PASS_STAGE + ST_PH, pl = base + s * PASS_STAGE + ST_PL;
-            const uint32_t rh = base + s * PASS_STAGE + ST_RH, rl = base + s * PASS_STAGE + ST_RL;
-            const uint32_t xop = base + PASS_XOP;
-            const uint32_t id64 = idesc_bf16_f32(128, 64, false, false);
-            const uint32_t id32 = idesc_bf16_f32(128, 32, false, false);
-            // D3[dk x 64] = P_hi [X_hi ; X_lo]^T  (+ P_lo X_hi^T into the first 32 columns)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 64, smem_desc(ph + kk * 32, 16, 1024, kSW), smem_desc(xop + kk * 32, 16, 1024, kSW),
-                         id64, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 64, smem_desc(pl + kk * 32, 16, 1024, kSW), smem_desc(xop + kk * 32, 16, 1024, kSW),
-                         id32, 1);
-            // D4[64(+64 pad) x 64] = R_hi [X_hi ; X_lo]^T  (+ R_lo X_hi^T into the first 32 columns)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 128, smem_desc(rh + kk * 32, 16, 1024, kSW), smem_desc(xop + kk * 32, 16, 1024, kSW),
-                         id64, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 128, smem_desc(rl + kk * 32, 16, 1024, kSW), smem_desc(xop + kk * 32, 16, 1024, kSW),
-                         id32, 1);
-            mma_commit(&bar_mma);
-        }
-        ok = mbar_wait(&bar_mma, 1);
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        tc_fence_after();
-
-        // state: S[r][d] <- e^{g_L} S[r][d] + D3[d][r] + D3[d][32 + r]
-        const float eL = expf(gL);
-        {
-            float a[16], b[16];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld16(tmem + tlane + 64 + half * 16, a);
-                tmem_ld16(tmem + tlane + 96 + half * 16, b);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) S[half * 16 + e] = fmaf(eL, S[half * 16 + e], a[e] + b[e]);
+            for (int kk = 0; kk < 4; ++kk) {   // P X (dk x 64): P_hi [X_hi ; X_lo]^T and P_lo [X_hi ; X_lo]^T
+                mma_bf16(tmem + TM_PX, dPH0 + so + 2 * kk, dXOP + 128 * kk, idb, kk > 0);
+                mma_bf16(tmem + TM_PX + 64, dPL0 + so + 2 * kk, dXOP + 128 * kk, idb, kk > 0);
             }
+            mma_commit(&bar_px);             // the state update waits only for this
+        } else if (tid == 128) {
+            const uint32_t rx = tmem + TM_RX + 64 * par;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)   // R X (64 (+64 pad) x 64) = R_hi [X_hi ; X_lo]^T
+                mma_bf16(rx, dRH0 + so + 2 * kk, dXOP + 128 * kk, idb, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)   //   + R_lo [X_hi ; X_lo]^T
+                mma_bf16(rx, dRL0 + so + 2 * kk, dXOP + 128 * kk, idb, 1);
+            mma_commit(&bar_rx);
+        }
+        // Q-row threads: outputs of the previous chunk (its R X sits in the other buffer) while P X runs
+        if (!krow && c > 0) {
+            store_outputs(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, prev_t0, hv, h, rowg, out,
+                          out_f32);
+        }
+        if (!krow) {
+#pragma unroll
+            for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
+        }
+
+        // state: S[r][d] <- e^{g_L} S[r][d] + (P X)[d][r] + (P X)[d][32 + r]   (this group's 16 rows)
+        if (!mbar_wait(&bar_px, par)) ok = false;
+        tc_fence_after();
+        {
+            const float eL = __expf(gL);
+            float a[16], b[16], a2[16], b2[16];
+            tmem_ld16x2(tmem + tlane + TM_PX + grp * 16, tmem + tlane + TM_PX + 32 + grp * 16, a, b);
+            tmem_ld16x2(tmem + tlane + TM_PX + 64 + grp * 16, tmem + tlane + TM_PX + 96 + grp * 16, a2, b2);
+#pragma unroll
+            for (int e = 0; e < DG; ++e) S[e] = fmaf(eL, S[e], (a[e] + b[e]) + (a2[e] + b2[e]));
         }
         write_sop();
         prev_t0 = t0;
         prev_L = L;
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        ok = __syncthreads_and(ok);
         tc_fence_after();
     }
 
     if (!ok) {
-        if (tid == 0) {
+        // the loop stopped after chunk c - 1; its prefetch of chunk c may still be in flight
+        if (tid == 0 && started) {
             raise_error(err, kErrTimeout);
-            // let a prefetch that may still be in flight land before the CTA exits
-            if (c + 1 < nchunks) mbar_wait(&bar_tma[(c + 1) & 1], ((c + 1) >> 1) & 1);
+            if (c < nchunks) mbar_wait(&bar_tma[c & 1], (c >> 1) & 1);
         }
     } else {
-        if (nchunks > 0 && warp < 2) store_outputs(qs, tmem + tlane, i, prev_L, prev_t0, hv, h, row0, out, out_f32);
+        if (nchunks > 0 && !krow) {
+            const uint32_t lp = (nchunks - 1) & 1;
+            const bool done = mbar_wait(&bar_rx, lp);
+            tc_fence_after();
+            if (done)
+                store_outputs(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32);
+            else
+                raise_error(err, kErrTimeout);
+        }
         if (final_state) {
 #pragma unroll
-            for (int r = 0; r < DS; ++r) final_state[sbase + (size_t)r * D] = S[r];
+            for (int r = 0; r < DG; ++r) final_state[sbase + (size_t)r * D] = S[r];
         }
     }
     tc_fence_before();
@@ -814,14 +906,14 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
 
     if ((phases & 1) && nch > 0) {
         dim3 grid((unsigned)nch, (unsigned)p.hv);
-        chunk_prep_kernel<<<grid, kThreads, PREP_SMEM, p.stream>>>(qmap, kmap, p.log_alpha, p.beta, p.cu_seqlens,
-                                                                   p.n_seqs, p.total_tokens, p.hk, p.hv, phi, plo,
-                                                                   rhi, rlo, p.err);
+        chunk_prep_kernel<<<grid, kThreads, PREP_SMEM, p.stream>>>(qmap, kmap, phmap, plmap, rhmap, rlmap,
+                                                                   p.log_alpha, p.beta, p.cu_seqlens, p.n_seqs,
+                                                                   p.total_tokens, p.hk, p.hv, p.err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
         const unsigned grid2 = (unsigned)(p.n_seqs * p.hv * (D / DS));
-        state_pass_kernel<<<grid2, kThreads, PASS_SMEM, p.stream>>>(
+        state_pass_kernel<<<grid2, kPassThreads, PASS_SMEM, p.stream>>>(
             qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.n_seqs,
             p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state, p.err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
