@@ -113,14 +113,13 @@ __device__ __forceinline__ void split8_bf16(const float *x, uint4 &hi, uint4 &lo
 }
 
 
-// Inclusive cumulative log-decay of the chunk for this warp: lane l covers
-// tokens 2l and 2l+1; tokens at or beyond `len` contribute 0 (their g equals
-// g_{len-1}).  Returns the two g values of the lane.
-__device__ __forceinline__ float2 chunk_cumsum(const float *__restrict__ log_alpha, int t0, int len, int hv, int h,
-                                               int lane) {
+// Inclusive cumulative log-decay of a chunk for this warp: lane l holds the raw log_alpha of tokens 2l
+// and 2l+1 (anything for tokens at or beyond `len`, which contribute 0, so their g equals g_{len-1}).
+// log_alpha is clamped to [-20, 0].  Returns the two g values of the lane.
+__device__ __forceinline__ float2 cumsum_pairs(float la0_raw, float la1_raw, int len, int lane) {
     const int i0 = 2 * lane, i1 = 2 * lane + 1;
-    const float la0 = i0 < len ? fminf(clamp_log_alpha(log_alpha[(size_t)(t0 + i0) * hv + h]), 0.f) : 0.f;
-    const float la1 = i1 < len ? fminf(clamp_log_alpha(log_alpha[(size_t)(t0 + i1) * hv + h]), 0.f) : 0.f;
+    const float la0 = i0 < len ? fminf(clamp_log_alpha(la0_raw), 0.f) : 0.f;
+    const float la1 = i1 < len ? fminf(clamp_log_alpha(la1_raw), 0.f) : 0.f;
     const float pair = la0 + la1;
     float incl = pair;
 #pragma unroll
@@ -132,7 +131,7 @@ __device__ __forceinline__ float2 chunk_cumsum(const float *__restrict__ log_alp
     return make_float2(excl + la0, excl + la0 + la1);
 }
 
-// g_i of token i from the per-lane pairs produced by chunk_cumsum.
+// g_i of token i from the per-lane pairs produced by cumsum_pairs.
 __device__ __forceinline__ float g_of(float2 g2, int i) {
     const float a = __shfl_sync(0xffffffffu, g2.x, i >> 1);
     const float b = __shfl_sync(0xffffffffu, g2.y, i >> 1);
@@ -144,22 +143,26 @@ __device__ __forceinline__ float g_of(float2 g2, int i) {
 // Kernel 1: per-chunk preparation (parallel over chunks x value heads)
 // ============================================================================
 // Shared memory (offsets from a 1 KiB-aligned base):
-constexpr uint32_t PREP_KQ = 0;        // kb0: K rows | Q rows, kb1: K rows | Q rows (32 KiB);
-                                       // the Q halves later hold T^T hi / lo
-constexpr uint32_t PREP_A = 32768;     // fp32 A [64][68]; later (Gamma T)^T hi / lo
+constexpr uint32_t PREP_KQ = 0;        // kb0: K rows | Q rows, kb1: K rows | Q rows (32 KiB).  Once [K;Q]K^T
+                                       // is done the Q halves hold T (fp32), then the T^T hi / lo tiles.
+constexpr uint32_t PREP_A = 32768;     // fp32 A [64][68]; later (Gamma T)^T hi / lo, then R hi / lo
 constexpr int A_LD = 68;
 constexpr uint32_t PREP_AQK = PREP_A + 64 * A_LD * 4;   // 50176: Aqk hi, Aqk lo tiles [64 x 64] bf16
-constexpr uint32_t PREP_T = PREP_AQK + 16384;           // fp32 T = (I + A)^-1 [64][68]
-constexpr uint32_t PREP_Y = PREP_T + 64 * A_LD * 4;     // fp32 scratch [3][16][16]
+constexpr uint32_t PREP_Y = PREP_AQK + 16384;           // fp32 scratch [3][16][16]
 constexpr uint32_t PREP_G = PREP_Y + 3 * 256 * 4;       // g [64], beta [64]
-constexpr uint32_t PREP_SMEM = PREP_G + 512 + 1024;     // + alignment slack
+constexpr uint32_t PREP_SMEM = PREP_G + 512 + 1024;     // + alignment slack: 3 CTAs per SM
 constexpr uint32_t PREP_TMEM_COLS = 128;
+
+// Row ii of T (fp32, 64 columns): rows 0-31 over the Q half of k-block 0, rows 32-63 over that of k-block 1.
+__device__ __forceinline__ float *t_row(uint8_t *sm, int ii) {
+    return reinterpret_cast<float *>(sm + PREP_KQ + (ii < 32 ? 8192 : 24576)) + (ii & 31) * 64;
+}
 
 // T = (I + A)^-1 for the strictly lower fp32 A (row stride A_LD), by 16 x 16 blocks, all 128 threads:
 //   diagonal blocks  T_II = (I + A_II)^-1            forward substitution, one column per thread
 //   below them       T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ   level by level in I (J < I in parallel)
 // T must be zero on entry.  Ends with the block synchronised.
-__device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict__ A, float *__restrict__ T,
+__device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict__ A, uint8_t *sm,
                                                          float *__restrict__ Y, int tid) {
     if (tid < 64) {
         const int j = tid, b = j >> 4, jj = j & 15;
@@ -176,7 +179,7 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
             tc[ii] = a0 + a1;
         }
 #pragma unroll
-        for (int ii = 0; ii < 16; ++ii) T[(16 * b + ii) * A_LD + j] = tc[ii];
+        for (int ii = 0; ii < 16; ++ii) t_row(sm, 16 * b + ii)[j] = tc[ii];
     }
     __syncthreads();
 #pragma unroll
@@ -188,10 +191,11 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
             const float *arow = A + (16 * I + r) * A_LD;
             float y0 = 0.f, y1 = 0.f;
             for (int K = J; K < I; ++K) {
+                const float *t0 = t_row(sm, 16 * K) + 16 * J + c;   // the 16 rows of block K are contiguous
 #pragma unroll
                 for (int kk = 0; kk < 16; kk += 2) {
-                    y0 = fmaf(arow[16 * K + kk], T[(16 * K + kk) * A_LD + 16 * J + c], y0);
-                    y1 = fmaf(arow[16 * K + kk + 1], T[(16 * K + kk + 1) * A_LD + 16 * J + c], y1);
+                    y0 = fmaf(arow[16 * K + kk], t0[kk * 64], y0);
+                    y1 = fmaf(arow[16 * K + kk + 1], t0[(kk + 1) * 64], y1);
                 }
             }
             Y[J * 256 + r * 16 + c] = y0 + y1;
@@ -201,14 +205,14 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
 #pragma unroll
         for (int m = 0; m < 2 * I; ++m) {
             const int e = tid + 128 * m, J = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const float *trow = T + (16 * I + r) * A_LD + 16 * I;
+            float *trow = t_row(sm, 16 * I + r);
             float t0 = 0.f, t1 = 0.f;
 #pragma unroll
             for (int kk = 0; kk < 16; kk += 2) {
-                t0 = fmaf(trow[kk], Y[J * 256 + kk * 16 + c], t0);
-                t1 = fmaf(trow[kk + 1], Y[J * 256 + (kk + 1) * 16 + c], t1);
+                t0 = fmaf(trow[16 * I + kk], Y[J * 256 + kk * 16 + c], t0);
+                t1 = fmaf(trow[16 * I + kk + 1], Y[J * 256 + (kk + 1) * 16 + c], t1);
             }
-            T[(16 * I + r) * A_LD + 16 * J + c] = -(t0 + t1);
+            trow[16 * J + c] = -(t0 + t1);
         }
         __syncthreads();
     }
@@ -252,17 +256,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     }
     float *g_s = reinterpret_cast<float *>(sm + PREP_G);  // [64]
     float *b_s = g_s + 64;                                // [64]
-    if (warp == 0) {
-        const float2 g2 = chunk_cumsum(log_alpha, t0, L, hv, h, lane);
-        g_s[2 * lane] = g2.x;
-        g_s[2 * lane + 1] = g2.y;
+    // warp 1 loads this chunk's gates now; their cumulative sum is formed while the TMA and MMA run
+    float la0 = 0.f, la1 = 0.f, bt0 = 0.f, bt1 = 0.f;
+    if (warp == 1) {
         const int i0 = 2 * lane, i1 = 2 * lane + 1;
-        b_s[i0] = i0 < L ? beta[(size_t)(t0 + i0) * hv + h] : 0.f;
-        b_s[i1] = i1 < L ? beta[(size_t)(t0 + i1) * hv + h] : 0.f;
-    }
-    {   // T starts at zero (its strictly upper blocks stay zero)
-        float4 *t4 = reinterpret_cast<float4 *>(sm + PREP_T);
-        for (int x = tid; x < 64 * A_LD / 4; x += kThreads) t4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i0 < L) {
+            la0 = log_alpha[(size_t)(t0 + i0) * hv + h];
+            bt0 = beta[(size_t)(t0 + i0) * hv + h];
+        }
+        if (i1 < L) {
+            la1 = log_alpha[(size_t)(t0 + i1) * hv + h];
+            bt1 = beta[(size_t)(t0 + i1) * hv + h];
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -282,9 +287,24 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         }
         mma_commit(&bar_mma);
     }
+    if (warp == 1) {
+        const float2 g2 = cumsum_pairs(la0, la1, L, lane);
+        g_s[2 * lane] = g2.x;
+        g_s[2 * lane + 1] = g2.y;
+        b_s[2 * lane] = bt0;
+        b_s[2 * lane + 1] = bt1;
+    }
     if (ok) ok = mbar_wait(&bar_mma, 0);
     ok = __syncthreads_and(ok);
     tc_fence_after();
+    {   // T (over the Q rows, which [K;Q]K^T no longer needs) starts at zero; its upper blocks stay zero
+        float4 *t0q = reinterpret_cast<float4 *>(sm + PREP_KQ + 8192);
+        float4 *t1q = reinterpret_cast<float4 *>(sm + PREP_KQ + 24576);
+        for (int x = tid; x < 512; x += kThreads) {
+            t0q[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+            t1q[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
 
     // Warps 0-1 build A (fp32) from the K K^T rows; warps 2-3 build the Aqk tiles (split into bf16 hi/lo)
     // from the Q K^T rows.  Then all warps solve for T and write the T operand tiles.
@@ -332,35 +352,40 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     }
     __syncthreads();
 
-    float *Tm = reinterpret_cast<float *>(sm + PREP_T);
-    solve_unit_lower_blocked(reinterpret_cast<const float *>(sm + PREP_A), Tm,
-                             reinterpret_cast<float *>(sm + PREP_Y), tid);
+    solve_unit_lower_blocked(reinterpret_cast<const float *>(sm + PREP_A), sm, reinterpret_cast<float *>(sm + PREP_Y),
+                             tid);
     // (A is no longer read: its space takes the (Gamma T)^T tiles.)
 
     // Operand tiles: row j of T^T (for R) and of (Gamma T)^T (for P) is column j of T, split into bf16 hi/lo.
-    // Thread t writes row j = t / 2, columns i in [32 (t % 2), 32 (t % 2) + 32).
-    if (ok) {
+    // Thread t covers row j = t / 2, columns i in [32 (t % 2), 32 (t % 2) + 32).  T is read into registers
+    // first, because the T^T tiles then overwrite it.
+    {
         const int j = tid >> 1, i0 = (tid & 1) * 32;
-        const float gl = g_s[L - 1];
-        uint8_t *tth = sm + PREP_KQ + 8192, *ttl = sm + PREP_KQ + 24576;   // over the Q rows
-        uint8_t *gth = sm + PREP_A, *gtl = sm + PREP_A + 8192;
+        float tv[32];
 #pragma unroll
-        for (int c8 = 0; c8 < 32; c8 += 8) {
-            float t8[8], g8[8];
+        for (int e = 0; e < 32; ++e) tv[e] = t_row(sm, i0 + e)[j];
+        __syncthreads();
+        if (ok) {
+            const float gl = g_s[L - 1];
+            uint8_t *tth = sm + PREP_KQ + 8192, *ttl = sm + PREP_KQ + 24576;   // over T
+            uint8_t *gth = sm + PREP_A, *gtl = sm + PREP_A + 8192;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int ii = i0 + c8 + e;
-                t8[e] = Tm[ii * A_LD + j];
-                g8[e] = ii < L ? __expf(gl - g_s[ii]) * t8[e] : 0.f;
+            for (int c8 = 0; c8 < 32; c8 += 8) {
+                float g8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int ii = i0 + c8 + e;
+                    g8[e] = ii < L ? __expf(gl - g_s[ii]) * tv[c8 + e] : 0.f;
+                }
+                const uint32_t off = sw128_offset(j, i0 + c8);
+                uint4 hi, lo;
+                split8_bf16(tv + c8, hi, lo);
+                *reinterpret_cast<uint4 *>(tth + off) = hi;
+                *reinterpret_cast<uint4 *>(ttl + off) = lo;
+                split8_bf16(g8, hi, lo);
+                *reinterpret_cast<uint4 *>(gth + off) = hi;
+                *reinterpret_cast<uint4 *>(gtl + off) = lo;
             }
-            const uint32_t off = sw128_offset(j, i0 + c8);
-            uint4 hi, lo;
-            split8_bf16(t8, hi, lo);
-            *reinterpret_cast<uint4 *>(tth + off) = hi;
-            *reinterpret_cast<uint4 *>(ttl + off) = lo;
-            split8_bf16(g8, hi, lo);
-            *reinterpret_cast<uint4 *>(gth + off) = hi;
-            *reinterpret_cast<uint4 *>(gtl + off) = lo;
         }
     }
     fence_proxy_async_smem();
@@ -517,21 +542,6 @@ __device__ __forceinline__ void load_chunk_inputs(ChunkInputs &in, const float *
     }
 }
 
-// Inclusive cumulative log-decay from already loaded pairs (see chunk_cumsum).
-__device__ __forceinline__ float2 cumsum_pairs(float la0_raw, float la1_raw, int len, int lane) {
-    const int i0 = 2 * lane, i1 = 2 * lane + 1;
-    const float la0 = i0 < len ? fminf(clamp_log_alpha(la0_raw), 0.f) : 0.f;
-    const float la1 = i1 < len ? fminf(clamp_log_alpha(la1_raw), 0.f) : 0.f;
-    const float pair = la0 + la1;
-    float incl = pair;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    const float excl = incl - pair;
-    return make_float2(excl + la0, excl + la0 + la1);
-}
 
 // Outputs of one chunk for this thread's token and 16 value rows (Q-row threads):
 // O_i = e^{g_i} (Q S^T)_i (in qs) + (R X)_i ((R_hi + R_lo) X_hi, and (R_hi + R_lo) X_lo).

@@ -9,18 +9,22 @@
 // this direct scan or the blocked form is faster depends on the model
 // dimensions, the workload and the hardware, so the library ships both.
 //
-// Mapping on sm_103a: one CTA of 128 threads owns 32 consecutive value rows of
+// Mapping on sm_103a: one CTA of 128 threads owns 16 consecutive value rows of
 // one (sequence, value head) state; thread (r, c) holds row r, columns
-// [c*D/4, (c+1)*D/4) in registers.  Inputs for the next 64 tokens are staged
-// into shared memory with cp.async while the current 64 are scanned; outputs
-// are staged and written back as coalesced rows.
+// [c*D/8, (c+1)*D/8) in registers, and a row's dot products are finished with
+// three shuffle levels.  Small slices give more CTAs (two or more per SM), whose
+// warps hide each other's latency on the token-serial chain.  Inputs for the
+// next 64 tokens are staged into shared memory with cp.async while the current
+// 64 are scanned (k.q of each token is formed once while staging); outputs are
+// staged and written back as coalesced rows.
 #include "gdn_internal.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kRows = 32;   // value rows per CTA
+constexpr int kRows = 16;   // value rows per CTA
+constexpr int kTPR = kThreads / kRows;   // threads per row
 constexpr int kTB = 64;     // tokens per staged block
 
 template <int D>
@@ -30,6 +34,7 @@ struct ScanSmem {
     __nv_bfloat16 v[2][kTB][kRows];
     float la[2][kTB];
     float b[2][kTB];
+    float kq[kTB];
     float o[kTB][kRows];
 };
 
@@ -77,7 +82,7 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
                     const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
                     void *__restrict__ out, int out_f32, float *__restrict__ final_state) {
-    constexpr int COLS = D / 4;           // state columns per thread
+    constexpr int COLS = D / kTPR;        // state columns per thread
     constexpr int SLICES = D / kRows;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ScanSmem<D> &sm = *reinterpret_cast<ScanSmem<D> *>(smem_raw);
@@ -87,7 +92,7 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
     const int n = blockIdx.x / (SLICES * hv);
     const int hq = h / (hv / hk);
     const int row0 = slice * kRows;
-    const int r = threadIdx.x >> 2, c = threadIdx.x & 3;
+    const int r = threadIdx.x / kTPR, c = threadIdx.x % kTPR;
 
     const long tbeg = min(max((long)cu_seqlens[n], 0L), (long)total_tokens);
     const long tend = min(max((long)cu_seqlens[n + 1], tbeg), (long)total_tokens);
@@ -123,39 +128,50 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
         cp_async_commit();
         cp_async_wait_prev();
         __syncthreads();
+        // k.q of every token of the block, once: 16 lanes per token, 8 tokens per round.  Every warp runs
+        // the same number of rounds (the shuffles need all 32 lanes); tokens past nt compute nothing.
+        for (int t0k = 0; t0k < nt; t0k += kThreads / 16) {
+            const int t = t0k + (threadIdx.x >> 4), l = threadIdx.x & 15;
+            float acc = 0.f;
+            if (t < nt) {
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j)
+                    acc = fmaf(__bfloat162float(sm.k[buf][t][l + 16 * j]), __bfloat162float(sm.q[buf][t][l + 16 * j]),
+                               acc);
+            }
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (l == 0 && t < nt) sm.kq[t] = acc;
+        }
+        __syncthreads();
 
         for (int t = 0; t < nt; ++t) {
             float kk[COLS], qq[COLS];
-            const uint4 *kp = reinterpret_cast<const uint4 *>(&sm.k[buf][t][c * COLS]);
-            const uint4 *qp = reinterpret_cast<const uint4 *>(&sm.q[buf][t][c * COLS]);
+            // this thread's COLS bf16 of k and q, 4 at a time (8-byte loads)
+            const uint2 *kp = reinterpret_cast<const uint2 *>(&sm.k[buf][t][c * COLS]);
+            const uint2 *qp = reinterpret_cast<const uint2 *>(&sm.q[buf][t][c * COLS]);
 #pragma unroll
-            for (int j = 0; j < COLS / 8; ++j) {
-                const uint4 a = kp[j], b = qp[j];
-                kk[8 * j + 0] = bf16_lo(a.x); kk[8 * j + 1] = bf16_hi(a.x);
-                kk[8 * j + 2] = bf16_lo(a.y); kk[8 * j + 3] = bf16_hi(a.y);
-                kk[8 * j + 4] = bf16_lo(a.z); kk[8 * j + 5] = bf16_hi(a.z);
-                kk[8 * j + 6] = bf16_lo(a.w); kk[8 * j + 7] = bf16_hi(a.w);
-                qq[8 * j + 0] = bf16_lo(b.x); qq[8 * j + 1] = bf16_hi(b.x);
-                qq[8 * j + 2] = bf16_lo(b.y); qq[8 * j + 3] = bf16_hi(b.y);
-                qq[8 * j + 4] = bf16_lo(b.z); qq[8 * j + 5] = bf16_hi(b.z);
-                qq[8 * j + 6] = bf16_lo(b.w); qq[8 * j + 7] = bf16_hi(b.w);
+            for (int j = 0; j < COLS / 4; ++j) {
+                const uint2 a = kp[j], b = qp[j];
+                kk[4 * j + 0] = bf16_lo(a.x); kk[4 * j + 1] = bf16_hi(a.x);
+                kk[4 * j + 2] = bf16_lo(a.y); kk[4 * j + 3] = bf16_hi(a.y);
+                qq[4 * j + 0] = bf16_lo(b.x); qq[4 * j + 1] = bf16_hi(b.x);
+                qq[4 * j + 2] = bf16_lo(b.y); qq[4 * j + 3] = bf16_hi(b.y);
             }
-            float sk[4] = {0.f, 0.f, 0.f, 0.f}, sq[4] = {0.f, 0.f, 0.f, 0.f}, kq[4] = {0.f, 0.f, 0.f, 0.f};
+            float sk[4] = {0.f, 0.f, 0.f, 0.f}, sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < COLS; ++j) {
                 sk[j & 3] = fmaf(S[j], kk[j], sk[j & 3]);
                 sq[j & 3] = fmaf(S[j], qq[j], sq[j & 3]);
-                kq[j & 3] = fmaf(kk[j], qq[j], kq[j & 3]);
             }
             float a0 = (sk[0] + sk[1]) + (sk[2] + sk[3]);
             float a1 = (sq[0] + sq[1]) + (sq[2] + sq[3]);
-            float a2 = (kq[0] + kq[1]) + (kq[2] + kq[3]);
-            a0 += __shfl_xor_sync(0xffffffffu, a0, 1);
-            a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
-            a2 += __shfl_xor_sync(0xffffffffu, a2, 1);
-            a0 += __shfl_xor_sync(0xffffffffu, a0, 2);
-            a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
-            a2 += __shfl_xor_sync(0xffffffffu, a2, 2);
+#pragma unroll
+            for (int off = 1; off < kTPR; off <<= 1) {
+                a0 += __shfl_xor_sync(0xffffffffu, a0, off);
+                a1 += __shfl_xor_sync(0xffffffffu, a1, off);
+            }
+            const float a2 = sm.kq[t];
             const float alpha = expf(clamp_log_alpha(sm.la[buf][t]));
             const float bt = sm.b[buf][t];
             const float u = bt * (__bfloat162float(sm.v[buf][t][r]) - alpha * a0);
