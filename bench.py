@@ -16,7 +16,8 @@ Also measured and reported on the same line:
     of the dominant kernel (algorithmic FLOPs / duration against the measured
     bf16 tensor peak);
   * the 30-layer batch-1 decode step (us per step and HBM GB/s of the state
-    read+write, rotating 5 replicas of the 60 MiB state);
+    read+write, rotating 5 replicas of the 60 MiB state), as one batched
+    launch per step and as 30 single-layer launches per step;
   * the direct-scan prefill on the same 4K workload (the scan vs. blocks
     comparison);
   * e2e: the same prefill metric through the public call with host buffers
@@ -258,6 +259,65 @@ def time_decode(dev, stream, steps=256, n_rep=5):
     return s.elapsed_time(e) * 1e3 / steps
 
 
+def time_decode_per_layer(dev, stream, steps=64, n_rep=5):
+    """The same 30-layer decode step issued as 30 single-layer launches (one per layer, as a model that
+    interleaves the recurrence with its other layers would), captured in one CUDA graph."""
+    import torch
+    from gated_deltanet_linear_03_gb300 import gdn, synth
+    di = synth.decode_30(steps=steps)
+    states = [di.state.to(dev) for _ in range(n_rep)]
+    q, k, v = di.q.to(dev), di.k.to(dev), di.v.to(dev)
+    la, b = di.log_alpha.to(dev), di.beta.to(dev)
+    out = torch.empty(DECODE_LAYERS, HV, D, dtype=torch.bfloat16, device=dev)
+
+    def step(i):
+        st = states[i % n_rep]
+        for l in range(DECODE_LAYERS):
+            gdn.decode_step(st[l:l + 1], q[i, l:l + 1], k[i, l:l + 1], v[i, l:l + 1], la[i, l:l + 1],
+                            b[i, l:l + 1], out=out[l:l + 1], stream=stream)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(steps):
+            step(i)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        graph.replay()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) * 1e3 / steps
+
+
+def run_each_kernel_once(args):
+    """Two passes of every kernel of the path on the bench workload (chunk preparation, state pass,
+    direct scan, 30-layer decode), nothing timed: the target for profiler captures."""
+    import torch
+    from gated_deltanet_linear_03_gb300 import gdn, synth
+    dev = torch.device("cuda", 0)
+    gdn.load_library()
+    _, _, plans, cu_host = make_prefill_replicas(1, dev)
+    t = plans[0].tensors
+    plan_scan = gdn.PrefillPlan(t[0], t[1], t[2], t[3], t[4], t[5], algo="scan", cu_seqlens_host=cu_host)
+    di = synth.decode_30(steps=2)
+    st = di.state.to(dev)
+    dq, dk_, dv = di.q.to(dev), di.k.to(dev), di.v.to(dev)
+    dla, db = di.log_alpha.to(dev), di.beta.to(dev)
+    for i in range(2):
+        plans[0].run_phase("prep")
+        plans[0].run_phase("pass")
+        plan_scan.run()
+        gdn.decode_step(st, dq[i], dk_[i], dv[i], dla[i], db[i])
+    err = gdn.device_error()
+    print(json.dumps({"profile_target": "prep, pass, scan, decode x 2", "device_error": err}))
+    return 0 if err == 0 else 1
+
+
 def time_scan(plan_scan, stream, iters=5):
     import torch
     with torch.cuda.stream(stream):
@@ -390,6 +450,7 @@ def run_gb300(args):
             soak(lambda: plans[0].run(stream=stream), 1.5)
         total_ms, prep_ms, pass_ms = time_prefill_steps(plans, args.steps, args.warmup, stream)
         decode_us = time_decode(dev, stream)
+        decode_layer_us = time_decode_per_layer(dev, stream)
         scan_ms = time_scan(plan_scan, stream)
     clocks = clk.summary()
     e2e_tps, h2d, d2h = time_e2e(host, cu_host, dev, stream, max(3, min(args.steps, 20)))
@@ -426,7 +487,11 @@ def run_gb300(args):
                    "us_per_step": decode_us, "hbm_gbs": dec_gbs,
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                 "frac": dec_gbs / peaks["hbm_gbs"], "traffic": load_traffic("decode_step_kernel")},
-                   "l2": "5 rotating state replicas (300 MiB)", "launch": "256 steps replayed as one CUDA graph"},
+                   "l2": "5 rotating state replicas (300 MiB)", "launch": "256 steps replayed as one CUDA graph",
+                   "per_layer_launches": {"us_per_step": decode_layer_us,
+                                          "hbm_gbs": DECODE_STATE_BYTES / (decode_layer_us * 1e-6) / 1e9,
+                                          "launch": "30 single-layer launches per step, 64 steps in one "
+                                                    "CUDA graph"}},
         "scan": {"tok_per_s": T_TOKENS / (scan_ms * 1e-3), "ms": scan_ms,
                  "fp32_tflops": FLOPS_SCAN * T_TOKENS * HV / (scan_ms * 1e-3) / 1e12},
         "e2e": {"value": e2e_units / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -466,7 +531,11 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--each-kernel-once", action="store_true",
+                    help="run every kernel of the path twice on the bench workload, untimed (profiler target)")
     args = ap.parse_args(argv)
+    if args.each_kernel_once:
+        return run_each_kernel_once(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
