@@ -273,13 +273,21 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    // shared-memory descriptors of every MMA operand (uniform values, built outside divergent code)
+    const uint64_t dkq = smem_desc(base + PREP_KQ, 16, 1024, kSW);          // [K;Q] K-major
+    const uint64_t dk_mn = smem_desc(base + PREP_KQ, 16384, 1024, kSW);     // K read MN-major
+    const uint64_t dgth = smem_desc(base + PREP_A, 16, 1024, kSW);          // (Gamma T)^T hi
+    const uint64_t dgtl = smem_desc(base + PREP_A + 8192, 16, 1024, kSW);   //                lo
+    const uint64_t dah = smem_desc(base + PREP_AQK, 16, 1024, kSW);         // Aqk hi
+    const uint64_t dal = smem_desc(base + PREP_AQK + 8192, 16, 1024, kSW);  //     lo
+    const uint64_t dth = smem_desc(base + PREP_KQ + 8192, 16, 1024, kSW);   // T^T hi
+    const uint64_t dtl = smem_desc(base + PREP_KQ + 24576, 16, 1024, kSW);  //     lo
 
     bool ok = mbar_wait(&bar_tma, 0);
     ok = __syncthreads_and(ok);
     if (ok && tid == 0) {
         // D0[128 x 64] = [K ; Q] K^T  (rows 0-63: K K^T, rows 64-127: Q K^T), exact products
-        const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
-        const uint64_t dkq = smem_desc(base + PREP_KQ, 16, 1024, kSW);
+        constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
@@ -395,20 +403,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 
     if (ok && tid == 0) {
         // P = K^T (Gamma T): A = K tile read MN-major (M = dk = 128), B = (Gamma T)^T hi then lo
-        const uint32_t idp = idesc_bf16_f32(128, 64, true, false);
-        const uint64_t dk_mn = smem_desc(base + PREP_KQ, 16384, 1024, kSW);
-        const uint64_t dgth = smem_desc(base + PREP_A, 16, 1024, kSW);
-        const uint64_t dgtl = smem_desc(base + PREP_A + 8192, 16, 1024, kSW);
+        constexpr uint32_t idp = idesc_bf16_f32(128, 64, true, false);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem + 64, dk_mn + 128 * kk, dgth + 2 * kk, idp, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem + 64, dk_mn + 128 * kk, dgtl + 2 * kk, idp, 1);
         // R = Aqk T (M = 64): Aqk_hi T_hi + Aqk_hi T_lo + Aqk_lo T_hi
-        const uint32_t idr = idesc_bf16_f32(64, 64, false, false);
-        const uint64_t dah = smem_desc(base + PREP_AQK, 16, 1024, kSW);
-        const uint64_t dal = smem_desc(base + PREP_AQK + 8192, 16, 1024, kSW);
-        const uint64_t dth = smem_desc(base + PREP_KQ + 8192, 16, 1024, kSW);
-        const uint64_t dtl = smem_desc(base + PREP_KQ + 24576, 16, 1024, kSW);
+        constexpr uint32_t idr = idesc_bf16_f32(64, 64, false, false);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem, dah + 2 * kk, dth + 2 * kk, idr, kk > 0);
 #pragma unroll
@@ -487,15 +488,14 @@ constexpr uint32_t PASS_SOP = 2 * PASS_STAGE;      // [S_hi ; S_lo] tile, 2 k-bl
 constexpr uint32_t PASS_XOP = PASS_SOP + 16384;    // [X_hi ; X_lo] tile [64 x 64] bf16
 constexpr uint32_t PASS_SMEM = PASS_XOP + 8192 + 1024;
 constexpr uint32_t kStageTx = 32768 + 16384 + 16384 + 8192 + 8192;
-constexpr uint32_t PASS_TMEM_COLS = 512;
+constexpr uint32_t PASS_TMEM_COLS = 256;
 // TMEM columns (each accumulator 64 columns: 32 for the S_hi / X_hi part, 32 for the S_lo / X_lo part):
-//   [Q;K] [S_hi;S_lo]^T  (M = 128 token rows: Q rows in lanes 0-63, K rows in 64-127), as four partial
-//                        accumulators of two K steps each, summed when read: a chain of small MMAs into
-//                        one accumulator serialises on the accumulator, independent ones overlap;
-//   P X                  (M = 128 = dk), as two partial accumulators (P_hi and P_lo);
+//   [Q;K] [S_hi;S_lo]^T  (M = 128 token rows: Q rows in lanes 0-63, K rows in 64-127);
+//   P X                  (M = 128 = dk), P_hi X and P_lo X accumulated together;
 //   R X                  (M = 128, rows 0-63 valid), double-buffered by chunk parity so that a chunk's
 //                        outputs can be read while the next chunk's R X is computed.
-constexpr uint32_t TM_D1 = 0, TM_PX = 256, TM_RX = 384;
+// A chain of MMAs into one accumulator runs as fast as independent ones, so each product has one.
+constexpr uint32_t TM_D1 = 0, TM_PX = 64, TM_RX = 128;
 
 __device__ __forceinline__ void pass_issue_loads(uint8_t *st, uint64_t *bar, const CUtensorMap *qmap,
                                                  const CUtensorMap *kmap, const CUtensorMap *phmap,
@@ -515,6 +515,9 @@ __device__ __forceinline__ void pass_issue_loads(uint8_t *st, uint64_t *bar, con
 }
 
 constexpr int kPassThreads = 256;   // 8 warps: warps w and w + 4 share TMEM lane quadrant w % 4
+// MMA issuers: thread 0 (a Q-row warp, idle until the X barrier) issues [Q;K] S^T; lanes 0 of warps 2 and 3
+// (K-row warps, idle between the X barrier and the state update) issue P X and R X.
+constexpr int kPxIssuer = 64, kRxIssuer = 96;
 constexpr int DG = DS / 2;          // state rows per thread (the two warp groups split the 32 rows)
 
 // Per-chunk inputs that are read with plain loads (gates, beta, this thread's v
@@ -570,8 +573,9 @@ __device__ __forceinline__ void store_outputs(float (&qs)[DG], uint32_t tmem_rx,
 // Thread roles (256 threads).  TMEM lane quadrant quad = warp % 4, row group grp = warp / 4 (which 16 of
 // the CTA's 32 value rows).  Lane l of quadrant quad is accumulator row 32 quad + l: for [Q;K] S^T and
 // R X that row is a token (Q rows for quad 0-1, K rows for quad 2-3); for P X it is state column d.
-// Q-row threads, which are off the X computation, issue: thread 0 the [Q;K] S^T and P X MMAs, thread
-// 128 the R X MMAs, thread 32 the TMA loads.
+// Thread 0 issues the [Q;K] S^T MMAs and thread 32 the TMA loads (both Q-row threads, which have nothing
+// to do before the X barrier); threads kPxIssuer and kRxIssuer (K-row threads, which have nothing to do
+// between the X barrier and the state update) issue P X and R X.
 __global__ void __launch_bounds__(kPassThreads, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
@@ -583,7 +587,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                   unsigned int *err) {
     extern __shared__ uint8_t pass_raw[];
     uint8_t *sm = align1024(pass_raw);
-    __shared__ uint64_t bar_tma[2], bar_d1, bar_px, bar_rx;
+    __shared__ uint64_t bar_tma[2], bar_d1, bar_px, bar_rx[2];
     __shared__ uint32_t tmem_slot;
 
     constexpr int SLICES = D / DS;
@@ -618,7 +622,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         mbar_init(&bar_tma[1], 1);
         mbar_init(&bar_d1, 1);
         mbar_init(&bar_px, 1);
-        mbar_init(&bar_rx, 1);
+        mbar_init(&bar_rx[0], 1);
+        mbar_init(&bar_rx[1], 1);
         fence_mbar_init();
     }
     // zero the padding rows of the R tiles once (rows 64..127 feed only unused accumulator rows)
@@ -665,20 +670,20 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     const uint32_t tmem = tmem_slot;
     const uint32_t tlane = (uint32_t)(32 * quad) << 16;
 
-    // Shared-memory descriptors, built once by the issuing thread; a K step adds a byte offset >> 4 to
-    // the start field (all tiles sit far below 256 KiB, so the 14-bit field never carries).
-    uint64_t dQK0 = 0, dPH0 = 0, dPL0 = 0, dRH0 = 0, dRL0 = 0, dSOP = 0, dXOP = 0;
-    if (tid == 0 || tid == 128) {
-        dQK0 = smem_desc(base + ST_QK, 16, 1024, kSW);
-        dPH0 = smem_desc(base + ST_PH, 16, 1024, kSW);
-        dPL0 = smem_desc(base + ST_PL, 16, 1024, kSW);
-        dRH0 = smem_desc(base + ST_RH, 16, 1024, kSW);
-        dRL0 = smem_desc(base + ST_RL, 16, 1024, kSW);
-        dSOP = smem_desc(base + PASS_SOP, 8192, 1024, kSW);   // MN-major B: 16 K-rows per step = 2048 B
-        dXOP = smem_desc(base + PASS_XOP, 8192, 1024, kSW);
-    }
+    // Shared-memory descriptors (the same for every thread, built outside divergent code); a K step adds a
+    // byte offset >> 4 to the start field (all tiles sit far below 256 KiB, so the 14-bit field never carries).
+    const uint64_t dQK0 = smem_desc(base + ST_QK, 16, 1024, kSW);
+    const uint64_t dPH0 = smem_desc(base + ST_PH, 16, 1024, kSW);
+    const uint64_t dPL0 = smem_desc(base + ST_PL, 16, 1024, kSW);
+    const uint64_t dRH0 = smem_desc(base + ST_RH, 16, 1024, kSW);
+    const uint64_t dRL0 = smem_desc(base + ST_RL, 16, 1024, kSW);
+    const uint64_t dSOP = smem_desc(base + PASS_SOP, 8192, 1024, kSW);   // MN-major B: 16 K-rows = 2048 B
+    const uint64_t dXOP = smem_desc(base + PASS_XOP, 8192, 1024, kSW);
     constexpr uint64_t kStageStep = PASS_STAGE >> 4;
     constexpr uint32_t idb = idesc_bf16_f32(128, 64, false, true);   // A K-major, B MN-major, N = 64
+
+    // Chunk c's R X is committed to bar_rx[c & 1]; this is the parity of its completion there.
+    auto rx_parity = [](int cc) { return (uint32_t)((cc >> 1) & 1); };
 
     float qs[DG];
     int c = 0, prev_t0 = 0, prev_L = 0;
@@ -694,17 +699,17 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             // D1[128 x 64] = [Q ; K] [S_hi ; S_lo]^T, once this chunk's tiles have landed
             if (mbar_wait(&bar_tma[s], (c >> 1) & 1)) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {   // K steps 2p, 2p+1 go to partial accumulator p
+                for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    mma_bf16(tmem + TM_D1 + 64 * (kk >> 1), dQK0 + so + off, dSOP + 128 * kk, idb, kk & 1);
+                    mma_bf16(tmem + TM_D1, dQK0 + so + off, dSOP + 128 * kk, idb, kk > 0);
                 }
                 mma_commit(&bar_d1);
             } else {
                 ok = false;
             }
         } else if (tid == 32 && c + 1 < nchunks) {
-            // next chunk's tiles go to the other stage once its last reader (the previous R X) is done
-            if (c == 0 || mbar_wait(&bar_rx, par ^ 1))
+            // next chunk's tiles go to the other stage once its last reader (the R X of chunk c - 1) is done
+            if (c == 0 || mbar_wait(&bar_rx[par ^ 1], rx_parity(c - 1)))
                 pass_issue_loads(sm + (s ^ 1) * PASS_STAGE, &bar_tma[s ^ 1], &qmap, &kmap, &phmap, &plmap, &rhmap,
                                  &rlmap, hq, t0 + C, gc + 1, hv, h);
             else
@@ -717,46 +722,28 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         const float gL = g_of(g2, L - 1);
         const float eg = __expf(g_of(g2, i));
 
-        if (!mbar_wait(&bar_d1, par)) ok = false;
-        tc_fence_after();
-        float qcur[DG];   // e^{g_i} (Q S^T)_i of this chunk (Q-row threads)
-        {
-            float a[16], b[16];   // x S_hi^T and x S_lo^T, this group's 16 rows (sum of the partials)
+        if (krow) {
+            // X_i = beta_i (v_i - e^{g_i} (K S^T)_i), split into bf16 hi/lo.  The X tile is stored MN-major:
+            // row i (the token, K of the MMA) holds n = 0..31 (X_hi) and 32..63 (X_lo).  It is rewritten only
+            // after the previous chunk's R X, its last reader, is complete.
+            if (!mbar_wait(&bar_d1, par)) ok = false;
+            if (c > 0 && !mbar_wait(&bar_rx[par ^ 1], rx_parity(c - 1))) ok = false;
+            tc_fence_after();
+            float a[16], b[16];   // x S_hi^T and x S_lo^T, this group's 16 rows
             tmem_ld16x2(tmem + tlane + TM_D1 + grp * 16, tmem + tlane + TM_D1 + 32 + grp * 16, a, b);
+            const float bi = cur.b, be = cur.b * eg;
 #pragma unroll
-            for (int p = 1; p < 4; ++p) {
-                float a2[16], b2[16];
-                tmem_ld16x2(tmem + tlane + TM_D1 + 64 * p + grp * 16, tmem + tlane + TM_D1 + 64 * p + 32 + grp * 16,
-                            a2, b2);
+            for (int q4 = 0; q4 < DG / 8; ++q4) {
+                const uint4 x = cur.v[q4];
+                const float vv[8] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y),
+                                     bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w)};
+                float xv[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    a[e] += a2[e];
-                    b[e] += b2[e];
-                }
-            }
-            if (krow) {
-                // X_i = beta_i (v_i - e^{g_i} (K S^T)_i), split into bf16 hi/lo.  The X tile is stored
-                // MN-major: row i (the token, K of the MMA) holds n = 0..31 (X_hi) and 32..63 (X_lo).
-                const float bi = cur.b, be = cur.b * eg;
-#pragma unroll
-                for (int q4 = 0; q4 < DG / 8; ++q4) {
-                    const uint4 x = cur.v[q4];
-                    const float vv[8] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y),
-                                         bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w)};
-                    float xv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) xv[e] = bi * vv[e] - be * (a[q4 * 8 + e] + b[q4 * 8 + e]);
-                    uint4 hi, lo;
-                    split8_bf16(xv, hi, lo);
-                    *reinterpret_cast<uint4 *>(sm + PASS_XOP + sw128_offset(i, grp * DG + 8 * q4)) = hi;
-                    *reinterpret_cast<uint4 *>(sm + PASS_XOP + sw128_offset(i, DS + grp * DG + 8 * q4)) = lo;
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < DG; ++r) qcur[r] = eg * (a[r] + b[r]);
-                // the previous chunk's R X must be complete before the next R X is issued (after the barrier
-                // below), so that waiting for it here can never see a later phase of the same barrier
-                if (c > 0 && !mbar_wait(&bar_rx, par ^ 1)) ok = false;
+                for (int e = 0; e < 8; ++e) xv[e] = bi * vv[e] - be * (a[q4 * 8 + e] + b[q4 * 8 + e]);
+                uint4 hi, lo;
+                split8_bf16(xv, hi, lo);
+                *reinterpret_cast<uint4 *>(sm + PASS_XOP + sw128_offset(i, grp * DG + 8 * q4)) = hi;
+                *reinterpret_cast<uint4 *>(sm + PASS_XOP + sw128_offset(i, DS + grp * DG + 8 * q4)) = lo;
             }
         }
         // X tile complete
@@ -765,14 +752,14 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         __syncthreads();
         tc_fence_after();
 
-        if (tid == 0) {
+        if (tid == kPxIssuer) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {   // P X (dk x 64): P_hi [X_hi ; X_lo]^T and P_lo [X_hi ; X_lo]^T
+            for (int kk = 0; kk < 4; ++kk) {   // P X (dk x 64) = P_hi [X_hi ; X_lo]^T + P_lo [X_hi ; X_lo]^T
                 mma_bf16(tmem + TM_PX, dPH0 + so + 2 * kk, dXOP + 128 * kk, idb, kk > 0);
-                mma_bf16(tmem + TM_PX + 64, dPL0 + so + 2 * kk, dXOP + 128 * kk, idb, kk > 0);
+                mma_bf16(tmem + TM_PX, dPL0 + so + 2 * kk, dXOP + 128 * kk, idb, 1);
             }
             mma_commit(&bar_px);             // the state update waits only for this
-        } else if (tid == 128) {
+        } else if (tid == kRxIssuer) {
             const uint32_t rx = tmem + TM_RX + 64 * par;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)   // R X (64 (+64 pad) x 64) = R_hi [X_hi ; X_lo]^T
@@ -780,14 +767,27 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)   //   + R_lo [X_hi ; X_lo]^T
                 mma_bf16(rx, dRL0 + so + 2 * kk, dXOP + 128 * kk, idb, 1);
-            mma_commit(&bar_rx);
-        }
-        // Q-row threads: outputs of the previous chunk (its R X sits in the other buffer) while P X runs
-        if (!krow && c > 0) {
-            store_outputs(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, prev_t0, hv, h, rowg, out,
-                          out_f32);
+            mma_commit(&bar_rx[par]);
         }
         if (!krow) {
+            // Q-row threads, off the state chain while P X runs: e^{g_i} (Q S^T)_i of this chunk (D1 is
+            // rewritten only after the end-of-chunk barrier), then the previous chunk's outputs, whose R X
+            // sits in the other buffer.
+            if (!mbar_wait(&bar_d1, par)) ok = false;
+            tc_fence_after();
+            float qcur[DG];
+            {
+                float a[16], b[16];
+                tmem_ld16x2(tmem + tlane + TM_D1 + grp * 16, tmem + tlane + TM_D1 + 32 + grp * 16, a, b);
+#pragma unroll
+                for (int r = 0; r < DG; ++r) qcur[r] = eg * (a[r] + b[r]);
+            }
+            if (c > 0) {
+                if (!mbar_wait(&bar_rx[par ^ 1], rx_parity(c - 1))) ok = false;
+                tc_fence_after();
+                store_outputs(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, prev_t0, hv, h, rowg, out,
+                              out_f32);
+            }
 #pragma unroll
             for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
         }
@@ -797,11 +797,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         tc_fence_after();
         {
             const float eL = __expf(gL);
-            float a[16], b[16], a2[16], b2[16];
+            float a[16], b[16];
             tmem_ld16x2(tmem + tlane + TM_PX + grp * 16, tmem + tlane + TM_PX + 32 + grp * 16, a, b);
-            tmem_ld16x2(tmem + tlane + TM_PX + 64 + grp * 16, tmem + tlane + TM_PX + 96 + grp * 16, a2, b2);
 #pragma unroll
-            for (int e = 0; e < DG; ++e) S[e] = fmaf(eL, S[e], (a[e] + b[e]) + (a2[e] + b2[e]));
+            for (int e = 0; e < DG; ++e) S[e] = fmaf(eL, S[e], a[e] + b[e]);
         }
         write_sop();
         prev_t0 = t0;
@@ -821,7 +820,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     } else {
         if (nchunks > 0 && !krow) {
             const uint32_t lp = (nchunks - 1) & 1;
-            const bool done = mbar_wait(&bar_rx, lp);
+            const bool done = mbar_wait(&bar_rx[lp], rx_parity(nchunks - 1));
             tc_fence_after();
             if (done)
                 store_outputs(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32);
@@ -905,10 +904,9 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
 
     CUtensorMap qmap{}, kmap{}, phmap{}, plmap{}, rhmap{}, rlmap{};
     if (p.total_tokens > 0 && nch > 0) {
-        const uint64_t T = (uint64_t)p.total_tokens;
+        const uint64_t T = (uint64_t)p.total_tokens, QK = (uint64_t)p.hk * D;
         const uint64_t rows_p = (uint64_t)nch * p.hv * D, rows_r = (uint64_t)nch * p.hv * C;
-        if (!make_map(&qmap, p.q, T, (uint64_t)p.hk * D, (uint64_t)p.hk * D, 64) ||
-            !make_map(&kmap, p.k, T, (uint64_t)p.hk * D, (uint64_t)p.hk * D, 64) ||
+        if (!make_map(&qmap, p.q, T, QK, QK, 64) || !make_map(&kmap, p.k, T, QK, QK, 64) ||
             !make_map(&phmap, phi, rows_p, C, C, 128) || !make_map(&plmap, plo, rows_p, C, C, 128) ||
             !make_map(&rhmap, rhi, rows_r, C, C, 64) || !make_map(&rlmap, rlo, rows_r, C, C, 64))
             return cudaErrorInvalidValue;

@@ -10,9 +10,11 @@
 // dimensions, the workload and the hardware, so the library ships both.
 //
 // Mapping on sm_103a: one CTA of 128 threads owns 16 consecutive value rows of
-// one (sequence, value head) state; thread (r, c) holds row r, columns
-// [c*D/8, (c+1)*D/8) in registers, and a row's dot products are finished with
-// three shuffle levels.  Small slices give more CTAs (two or more per SM), whose
+// one (sequence, value head) state; thread (r, c) holds D/8 columns of row r in
+// registers, in groups of four: columns 4(c + 8m) .. 4(c + 8m) + 3 for
+// m = 0 .. D/32 - 1, so that the 8 threads of a row read consecutive 8-byte
+// words of a staged k or q row (no bank conflicts); a row's dot products are
+// finished with three shuffle levels.  Small slices give more CTAs (two or more per SM), whose
 // warps hide each other's latency on the token-serial chain.  Inputs for the
 // next 64 tokens are staged into shared memory with cp.async while the current
 // 64 are scanned (k.q of each token is formed once while staging); outputs are
@@ -97,12 +99,13 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
     const long tbeg = min(max((long)cu_seqlens[n], 0L), (long)total_tokens);
     const long tend = min(max((long)cu_seqlens[n + 1], tbeg), (long)total_tokens);
 
+    // S[4m + e] is column 4(c + kTPR m) + e of row r
     float S[COLS];
-    const size_t srow = (((size_t)n * hv + h) * D + row0 + r) * D + c * COLS;
+    const size_t srow = (((size_t)n * hv + h) * D + row0 + r) * D + 4 * c;
     if (init_state) {
 #pragma unroll
         for (int j = 0; j < COLS; j += 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(init_state + srow + j);
+            const float4 x = *reinterpret_cast<const float4 *>(init_state + srow + kTPR * j);
             S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
         }
     } else {
@@ -147,12 +150,12 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
 
         for (int t = 0; t < nt; ++t) {
             float kk[COLS], qq[COLS];
-            // this thread's COLS bf16 of k and q, 4 at a time (8-byte loads)
-            const uint2 *kp = reinterpret_cast<const uint2 *>(&sm.k[buf][t][c * COLS]);
-            const uint2 *qp = reinterpret_cast<const uint2 *>(&sm.q[buf][t][c * COLS]);
+            // this thread's COLS bf16 of k and q, 4 at a time (8-byte loads, word c + kTPR j of the row)
+            const uint2 *kp = reinterpret_cast<const uint2 *>(&sm.k[buf][t][0]) + c;
+            const uint2 *qp = reinterpret_cast<const uint2 *>(&sm.q[buf][t][0]) + c;
 #pragma unroll
             for (int j = 0; j < COLS / 4; ++j) {
-                const uint2 a = kp[j], b = qp[j];
+                const uint2 a = kp[kTPR * j], b = qp[kTPR * j];
                 kk[4 * j + 0] = bf16_lo(a.x); kk[4 * j + 1] = bf16_hi(a.x);
                 kk[4 * j + 2] = bf16_lo(a.y); kk[4 * j + 3] = bf16_hi(a.y);
                 qq[4 * j + 0] = bf16_lo(b.x); qq[4 * j + 1] = bf16_hi(b.x);
@@ -194,7 +197,7 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
     if (final_state) {
 #pragma unroll
         for (int j = 0; j < COLS; j += 4)
-            *reinterpret_cast<float4 *>(final_state + srow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            *reinterpret_cast<float4 *>(final_state + srow + kTPR * j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
 }
 
