@@ -149,8 +149,8 @@ constexpr uint32_t PREP_A = 32768;     // fp32 A [64][68]; later (Gamma T)^T hi 
 constexpr int A_LD = 68;
 constexpr uint32_t PREP_AQK = PREP_A + 64 * A_LD * 4;   // 50176: Aqk hi, Aqk lo tiles [64 x 64] bf16
 constexpr uint32_t PREP_Y = PREP_AQK + 16384;           // fp32 scratch [3][16][16]
-constexpr uint32_t PREP_G = PREP_Y + 3 * 256 * 4;       // g [64], beta [64]
-constexpr uint32_t PREP_SMEM = PREP_G + 512 + 1024;     // + alignment slack: 3 CTAs per SM
+constexpr uint32_t PREP_G = PREP_Y + 3 * 256 * 4;       // g [64], beta [64], Gamma = e^{g_L - g} [64]
+constexpr uint32_t PREP_SMEM = PREP_G + 768 + 1024;     // + alignment slack: 3 CTAs per SM
 constexpr uint32_t PREP_TMEM_COLS = 128;
 
 // Row ii of T (fp32, 64 columns): rows 0-31 over the Q half of k-block 0, rows 32-63 over that of k-block 1.
@@ -161,6 +161,9 @@ __device__ __forceinline__ float *t_row(uint8_t *sm, int ii) {
 // T = (I + A)^-1 for the strictly lower fp32 A (row stride A_LD), by 16 x 16 blocks, all 128 threads:
 //   diagonal blocks  T_II = (I + A_II)^-1            forward substitution, one column per thread
 //   below them       T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ   level by level in I (J < I in parallel)
+// In the block products each thread owns a strip of two adjacent columns of one row: four consecutive
+// elements of the left factor come in one 16-byte load (the same address for the lanes of a row) and each
+// row of the right factor in one 8-byte load, so a pair of FMAs costs about one shared-memory load.
 // T must be zero on entry.  Ends with the block synchronised.
 __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict__ A, uint8_t *sm,
                                                          float *__restrict__ Y, int tid) {
@@ -170,13 +173,16 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
         float tc[16];
 #pragma unroll
         for (int ii = 0; ii < 16; ++ii) {
-            float a0 = (ii == jj) ? 1.f : 0.f, a1 = 0.f;
+            float acc[4] = {(ii == jj) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kk = 0; kk < ii; ++kk) {
-                if (kk & 1) a1 = fmaf(-Ab[ii * A_LD + kk], tc[kk], a1);
-                else a0 = fmaf(-Ab[ii * A_LD + kk], tc[kk], a0);
+            for (int k4 = 0; k4 < ii; k4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Ab + ii * A_LD + k4);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (k4 + e < ii) acc[e] = fmaf(-av[e], tc[k4 + e], acc[e]);
             }
-            tc[ii] = a0 + a1;
+            tc[ii] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
 #pragma unroll
         for (int ii = 0; ii < 16; ++ii) t_row(sm, 16 * b + ii)[j] = tc[ii];
@@ -184,35 +190,58 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
     __syncthreads();
 #pragma unroll
     for (int I = 1; I < 4; ++I) {
-        // Y_J = sum_{K=J}^{I-1} A_IK T_KJ for J < I: I * 256 elements, 2 I per thread (warp-uniform J)
+        // Y_J = sum_{K=J}^{I-1} A_IK T_KJ for J < I: I x 128 two-column strips, I per thread (warp-uniform J)
 #pragma unroll
-        for (int m = 0; m < 2 * I; ++m) {
-            const int e = tid + 128 * m, J = e >> 8, r = (e >> 4) & 15, c = e & 15;
+        for (int m = 0; m < I; ++m) {
+            const int e = tid + 128 * m, J = e >> 7, r = (e >> 3) & 15, c = (e & 7) * 2;
             const float *arow = A + (16 * I + r) * A_LD;
-            float y0 = 0.f, y1 = 0.f;
+            float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
             for (int K = J; K < I; ++K) {
-                const float *t0 = t_row(sm, 16 * K) + 16 * J + c;   // the 16 rows of block K are contiguous
+                const float *tb = t_row(sm, 16 * K) + 16 * J + c;   // the 16 rows of block K are contiguous
 #pragma unroll
-                for (int kk = 0; kk < 16; kk += 2) {
-                    y0 = fmaf(arow[16 * K + kk], t0[kk * 64], y0);
-                    y1 = fmaf(arow[16 * K + kk + 1], t0[(kk + 1) * 64], y1);
+                for (int k4 = 0; k4 < 16; k4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(arow + 16 * K + k4);
+                    const float2 t0 = *reinterpret_cast<const float2 *>(tb + (k4 + 0) * 64);
+                    const float2 t1 = *reinterpret_cast<const float2 *>(tb + (k4 + 1) * 64);
+                    const float2 t2 = *reinterpret_cast<const float2 *>(tb + (k4 + 2) * 64);
+                    const float2 t3 = *reinterpret_cast<const float2 *>(tb + (k4 + 3) * 64);
+                    y0 = fmaf(a4.x, t0.x, y0);
+                    y1 = fmaf(a4.x, t0.y, y1);
+                    z0 = fmaf(a4.y, t1.x, z0);
+                    z1 = fmaf(a4.y, t1.y, z1);
+                    y0 = fmaf(a4.z, t2.x, y0);
+                    y1 = fmaf(a4.z, t2.y, y1);
+                    z0 = fmaf(a4.w, t3.x, z0);
+                    z1 = fmaf(a4.w, t3.y, z1);
                 }
             }
-            Y[J * 256 + r * 16 + c] = y0 + y1;
+            *reinterpret_cast<float2 *>(Y + J * 256 + r * 16 + c) = make_float2(y0 + z0, y1 + z1);
         }
         __syncthreads();
         // T_IJ = -T_II Y_J
 #pragma unroll
-        for (int m = 0; m < 2 * I; ++m) {
-            const int e = tid + 128 * m, J = e >> 8, r = (e >> 4) & 15, c = e & 15;
+        for (int m = 0; m < I; ++m) {
+            const int e = tid + 128 * m, J = e >> 7, r = (e >> 3) & 15, c = (e & 7) * 2;
             float *trow = t_row(sm, 16 * I + r);
-            float t0 = 0.f, t1 = 0.f;
+            const float *yb = Y + J * 256 + c;
+            float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < 16; kk += 2) {
-                t0 = fmaf(trow[16 * I + kk], Y[J * 256 + kk * 16 + c], t0);
-                t1 = fmaf(trow[16 * I + kk + 1], Y[J * 256 + (kk + 1) * 16 + c], t1);
+            for (int k4 = 0; k4 < 16; k4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(trow + 16 * I + k4);
+                const float2 t0 = *reinterpret_cast<const float2 *>(yb + (k4 + 0) * 16);
+                const float2 t1 = *reinterpret_cast<const float2 *>(yb + (k4 + 1) * 16);
+                const float2 t2 = *reinterpret_cast<const float2 *>(yb + (k4 + 2) * 16);
+                const float2 t3 = *reinterpret_cast<const float2 *>(yb + (k4 + 3) * 16);
+                y0 = fmaf(a4.x, t0.x, y0);
+                y1 = fmaf(a4.x, t0.y, y1);
+                z0 = fmaf(a4.y, t1.x, z0);
+                z1 = fmaf(a4.y, t1.y, z1);
+                y0 = fmaf(a4.z, t2.x, y0);
+                y1 = fmaf(a4.z, t2.y, y1);
+                z0 = fmaf(a4.w, t3.x, z0);
+                z1 = fmaf(a4.w, t3.y, z1);
             }
-            trow[16 * J + c] = -(t0 + t1);
+            *reinterpret_cast<float2 *>(trow + 16 * J + c) = make_float2(-(y0 + z0), -(y1 + z1));
         }
         __syncthreads();
     }
@@ -256,6 +285,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     }
     float *g_s = reinterpret_cast<float *>(sm + PREP_G);  // [64]
     float *b_s = g_s + 64;                                // [64]
+    float *gam_s = g_s + 128;                             // [64], 0 past the chunk's end
     // warp 1 loads this chunk's gates now; their cumulative sum is formed while the TMA and MMA run
     float la0 = 0.f, la1 = 0.f, bt0 = 0.f, bt1 = 0.f;
     if (warp == 1) {
@@ -297,10 +327,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     }
     if (warp == 1) {
         const float2 g2 = cumsum_pairs(la0, la1, L, lane);
+        const float gl = g_of(g2, L - 1);
         g_s[2 * lane] = g2.x;
         g_s[2 * lane + 1] = g2.y;
         b_s[2 * lane] = bt0;
         b_s[2 * lane + 1] = bt1;
+        gam_s[2 * lane] = 2 * lane < L ? __expf(gl - g2.x) : 0.f;
+        gam_s[2 * lane + 1] = 2 * lane + 1 < L ? __expf(gl - g2.y) : 0.f;
     }
     if (ok) ok = mbar_wait(&bar_mma, 0);
     ok = __syncthreads_and(ok);
@@ -315,18 +348,29 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     }
 
     // Warps 0-1 build A (fp32) from the K K^T rows; warps 2-3 build the Aqk tiles (split into bf16 hi/lo)
-    // from the Q K^T rows.  Then all warps solve for T and write the T operand tiles.
+    // from the Q K^T rows.  Then all warps solve for T and write the T operand tiles.  Rows 0-31 (warps 0
+    // and 2) have nothing left of the diagonal past column 31: they read and decay only columns 0-31.  The
+    // solve never reads A on or above the diagonal, so A is written only below it; the Aqk tiles feed an
+    // MMA and are written in full (zeros above the diagonal).
     {
         const int i = tid & 63;
+        const bool low_rows = (warp & 1) == 0;   // rows 0-31 (warp-uniform)
         float vals[64];
-#pragma unroll
-        for (int c = 0; c < 4; c += 2) {
+        {
             float a16[16], b16[16];
-            tmem_ld16x2(tmem + tlane + c * 16, tmem + tlane + (c + 1) * 16, a16, b16);
+            tmem_ld16x2(tmem + tlane, tmem + tlane + 16, a16, b16);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
-                vals[c * 16 + jj] = a16[jj];
-                vals[(c + 1) * 16 + jj] = b16[jj];
+                vals[jj] = a16[jj];
+                vals[16 + jj] = b16[jj];
+            }
+            if (!low_rows) {
+                tmem_ld16x2(tmem + tlane + 32, tmem + tlane + 48, a16, b16);
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    vals[32 + jj] = a16[jj];
+                    vals[48 + jj] = b16[jj];
+                }
             }
         }
         const float gi = g_s[i];
@@ -336,6 +380,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             float *arow = reinterpret_cast<float *>(sm + PREP_A) + i * A_LD;
 #pragma unroll
             for (int jj = 0; jj < 64; jj += 4) {
+                if (jj >= 32 && low_rows) break;
                 float4 a;
                 a.x = (row_ok && jj + 0 < i) ? bi * __expf(gi - g_s[jj + 0]) * vals[jj + 0] : 0.f;
                 a.y = (row_ok && jj + 1 < i) ? bi * __expf(gi - g_s[jj + 1]) * vals[jj + 1] : 0.f;
@@ -346,12 +391,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         } else {
 #pragma unroll
             for (int jj = 0; jj < 64; jj += 8) {
-                float x[8];
+                uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
+                if (jj < 32 || !low_rows) {
+                    float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    x[e] = (row_ok && jj + e <= i) ? __expf(gi - g_s[jj + e]) * vals[jj + e] : 0.f;
-                uint4 hi, lo;
-                split8_bf16(x, hi, lo);
+                    for (int e = 0; e < 8; ++e)
+                        x[e] = (row_ok && jj + e <= i) ? __expf(gi - g_s[jj + e]) * vals[jj + e] : 0.f;
+                    split8_bf16(x, hi, lo);
+                }
                 const uint32_t off = sw128_offset(i, jj);
                 *reinterpret_cast<uint4 *>(sm + PREP_AQK + off) = hi;
                 *reinterpret_cast<uint4 *>(sm + PREP_AQK + 8192 + off) = lo;
@@ -365,26 +412,23 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     // (A is no longer read: its space takes the (Gamma T)^T tiles.)
 
     // Operand tiles: row j of T^T (for R) and of (Gamma T)^T (for P) is column j of T, split into bf16 hi/lo.
-    // Thread t covers row j = t / 2, columns i in [32 (t % 2), 32 (t % 2) + 32).  T is read into registers
-    // first, because the T^T tiles then overwrite it.
+    // Thread t covers row j = t % 64, columns i in [32 (t / 64), 32 (t / 64) + 32) (the lanes of a warp read
+    // 32 consecutive words of a row of T).  T is read into registers first, because the T^T tiles then
+    // overwrite it.
     {
-        const int j = tid >> 1, i0 = (tid & 1) * 32;
+        const int j = tid & 63, i0 = (tid >> 6) * 32;
         float tv[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) tv[e] = t_row(sm, i0 + e)[j];
         __syncthreads();
         if (ok) {
-            const float gl = g_s[L - 1];
             uint8_t *tth = sm + PREP_KQ + 8192, *ttl = sm + PREP_KQ + 24576;   // over T
             uint8_t *gth = sm + PREP_A, *gtl = sm + PREP_A + 8192;
 #pragma unroll
             for (int c8 = 0; c8 < 32; c8 += 8) {
                 float g8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int ii = i0 + c8 + e;
-                    g8[e] = ii < L ? __expf(gl - g_s[ii]) * tv[c8 + e] : 0.f;
-                }
+                for (int e = 0; e < 8; ++e) g8[e] = gam_s[i0 + c8 + e] * tv[c8 + e];
                 const uint32_t off = sw128_offset(j, i0 + c8);
                 uint4 hi, lo;
                 split8_bf16(tv + c8, hi, lo);
