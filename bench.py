@@ -318,6 +318,63 @@ def run_each_kernel_once(args):
     return 0 if err == 0 else 1
 
 
+def run_crossover(args):
+    """Short-to-long prefill sweep: device time per call of the direct scan and of the chunked path (and, for
+    a few tokens, of that many batched decode steps) for N sequences of T tokens each, continuing from a
+    nonzero state as a speculative verify or a prompt segment would.  Each call is replayed from a CUDA
+    graph, so host launch overhead is not counted.  Prints one JSON line per (N, T)."""
+    import torch
+    from gated_deltanet_linear_03_gb300 import gdn, synth
+    dev = torch.device("cuda", 0)
+    gdn.load_library()
+    stream = torch.cuda.Stream(dev)
+
+    def graph_us(fn, reps=20):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(reps):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
+            s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            g.replay()
+            e0.record(stream)
+        torch.cuda.synchronize()
+        return s0.elapsed_time(e0) * 1e3 / reps
+
+    for n in (1, 8):
+        for t in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096):
+            inp = synth.prefill_inputs([t] * n, seed=1005, init_std=0.02)
+            d = [x.to(dev) for x in (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.cu_seqlens)]
+            s0 = inp.init_state.to(dev)
+            cu = inp.cu_seqlens.tolist()
+            row = {"n_seqs": n, "tokens_per_seq": t}
+            for algo in ("scan", "chunked"):
+                plan = gdn.PrefillPlan(*d, init_state=s0, algo=algo, cu_seqlens_host=cu)
+                row[algo + "_us"] = graph_us(lambda: plan.run(stream=stream))
+            if t <= 8:
+                st = s0.clone()
+                q = d[0].view(n, t, HK, D).transpose(0, 1).contiguous()
+                k = d[1].view(n, t, HK, D).transpose(0, 1).contiguous()
+                v = d[2].view(n, t, HV, D).transpose(0, 1).contiguous()
+                la = d[3].view(n, t, HV).transpose(0, 1).contiguous()
+                b = d[4].view(n, t, HV).transpose(0, 1).contiguous()
+                out = torch.empty(n, HV, D, dtype=torch.bfloat16, device=dev)
+
+                def steps():
+                    for i in range(t):
+                        gdn.decode_step(st, q[i], k[i], v[i], la[i], b[i], out=out, stream=stream)
+                row["decode_steps_us"] = graph_us(steps)
+            row["best"] = min((k for k in row if k.endswith("_us")), key=lambda k: row[k])[:-3]
+            print(json.dumps(row), flush=True)
+    return 0
+
+
 def time_scan(plan_scan, stream, iters=5):
     import torch
     with torch.cuda.stream(stream):
@@ -533,9 +590,13 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--each-kernel-once", action="store_true",
                     help="run every kernel of the path twice on the bench workload, untimed (profiler target)")
+    ap.add_argument("--crossover", action="store_true",
+                    help="sweep short to long sequences: scan vs chunked (vs decode steps) device time per call")
     args = ap.parse_args(argv)
     if args.each_kernel_once:
         return run_each_kernel_once(args)
+    if args.crossover:
+        return run_crossover(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

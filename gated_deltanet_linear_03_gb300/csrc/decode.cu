@@ -144,7 +144,173 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
     }
 }
 
+// Short-sequence prefill: the decode step's row streaming applied to every token of a short sequence
+// (a speculative verify, a prompt segment of a few tokens).  Each state row is read once, carried through
+// the sequence's tokens in registers and written once; the tokens' q, k, v and gates are staged in shared
+// memory up front.  One CTA covers kShortRows(D) value rows of one (sequence, head); the per-token math
+// is the decode step's:  sk = s.k, sq = s.q, u = beta (v - alpha sk), s' = alpha s + u k, o = alpha sq + u (k.q).
+constexpr int kShortMaxTokens = kShortScanTokens;
+
+template <int D>
+__host__ __device__ constexpr int short_warps() { return D == 32 ? 1 : 4; }
+template <int D>
+__host__ __device__ constexpr int short_rows() { return short_warps<D>() * (32 / (D / 4)) * kRowsPerGroup; }   // 32, 64, 32
+
+template <int D>
+struct __align__(16) ShortSmem {
+    __nv_bfloat16 k[kShortMaxTokens][D];
+    __nv_bfloat16 q[kShortMaxTokens][D];
+    __nv_bfloat16 v[kShortMaxTokens][short_rows<D>()];
+    float alpha[kShortMaxTokens];
+    float beta[kShortMaxTokens];
+    float kq[kShortMaxTokens];
+};
+
+template <int D>
+__global__ void __launch_bounds__(short_warps<D>() * 32)
+short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__restrict__ q,
+                     const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
+                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
+                     const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
+                     void *__restrict__ out, int out_f32, float *__restrict__ final_state) {
+    constexpr int LPR = D / 4, GROUPS = 32 / LPR, ROWS = short_rows<D>(), SLICES = D / ROWS;
+    constexpr int NT = short_warps<D>() * 32;
+    constexpr int PER = (16 / LPR) > 0 ? (16 / LPR) : 1;
+    __shared__ ShortSmem<D> sm;
+
+    const int slice = blockIdx.x % SLICES;
+    const int h = (blockIdx.x / SLICES) % hv;
+    const int n = blockIdx.x / (SLICES * hv);
+    const int hq = h / (hv / hk);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int group = lane / LPR, gl = lane % LPR;
+    const int row_in_head = slice * ROWS + (warp * GROUPS + group) * kRowsPerGroup;   // first of 8 rows
+    const long tbeg = min(max((long)cu_seqlens[n], 0L), (long)total_tokens);
+    const long tend = min(max((long)cu_seqlens[n + 1], tbeg), (long)total_tokens);
+    const int L = (int)min(tend - tbeg, (long)kShortMaxTokens);   // the host sends only L <= kShortMaxTokens
+
+    // stage the tokens: q, k rows of head hq (16-byte pieces), v of this CTA's rows, gates
+    for (int i = tid; i < L * (D / 8); i += NT) {
+        const int t = i / (D / 8), c = i % (D / 8);
+        const size_t g = ((size_t)(tbeg + t) * hk + hq) * D + c * 8;
+        *reinterpret_cast<uint4 *>(&sm.k[t][c * 8]) = *reinterpret_cast<const uint4 *>(k + g);
+        *reinterpret_cast<uint4 *>(&sm.q[t][c * 8]) = *reinterpret_cast<const uint4 *>(q + g);
+    }
+    for (int i = tid; i < L * (ROWS / 8); i += NT) {
+        const int t = i / (ROWS / 8), c = i % (ROWS / 8);
+        *reinterpret_cast<uint4 *>(&sm.v[t][c * 8]) =
+            *reinterpret_cast<const uint4 *>(v + ((size_t)(tbeg + t) * hv + h) * D + slice * ROWS + c * 8);
+    }
+    for (int t = tid; t < L; t += NT) {
+        sm.alpha[t] = __expf(clamp_log_alpha(log_alpha[(size_t)(tbeg + t) * hv + h]));
+        sm.beta[t] = beta[(size_t)(tbeg + t) * hv + h];
+    }
+
+    // this lane group's 8 state rows, 4 columns per lane
+    const size_t head = (size_t)n * hv + h;
+    float4 s[kRowsPerGroup];
+    float4 *srow = final_state ? reinterpret_cast<float4 *>(final_state + (head * D + row_in_head) * D) + gl
+                               : nullptr;
+    if (init_state) {
+        const float4 *irow = reinterpret_cast<const float4 *>(init_state + (head * D + row_in_head) * D) + gl;
+#pragma unroll
+        for (int i = 0; i < kRowsPerGroup; ++i) s[i] = irow[(size_t)i * (D / 4)];
+    } else {
+#pragma unroll
+        for (int i = 0; i < kRowsPerGroup; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    // k.q of every token, one lane group per token (all warps run the same number of rounds)
+    for (int t0 = 0; t0 < L; t0 += short_warps<D>() * GROUPS) {
+        const int t = t0 + warp * GROUPS + group;
+        float x = 0.f;
+        if (t < L) {
+            const uint2 kr = *reinterpret_cast<const uint2 *>(&sm.k[t][gl * 4]);
+            const uint2 qr = *reinterpret_cast<const uint2 *>(&sm.q[t][gl * 4]);
+            x = bf16_lo(kr.x) * bf16_lo(qr.x) + bf16_hi(kr.x) * bf16_hi(qr.x) + bf16_lo(kr.y) * bf16_lo(qr.y) +
+                bf16_hi(kr.y) * bf16_hi(qr.y);
+        }
+#pragma unroll
+        for (int off = LPR / 2; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+        if (gl == 0 && t < L) sm.kq[t] = x;
+    }
+    __syncthreads();
+
+    const int my_base = gl * 16 / LPR;
+    const int group_lane0 = group * LPR;
+    const int vrow0 = (warp * GROUPS + group) * kRowsPerGroup;   // within the CTA's rows
+    for (int t = 0; t < L; ++t) {
+        const uint2 kr = *reinterpret_cast<const uint2 *>(&sm.k[t][gl * 4]);
+        const uint2 qr = *reinterpret_cast<const uint2 *>(&sm.q[t][gl * 4]);
+        const float kv[4] = {bf16_lo(kr.x), bf16_hi(kr.x), bf16_lo(kr.y), bf16_hi(kr.y)};
+        const float qv[4] = {bf16_lo(qr.x), bf16_hi(qr.x), bf16_lo(qr.y), bf16_hi(qr.y)};
+        const float alpha = sm.alpha[t], b = sm.beta[t], kq = sm.kq[t];
+        float part[16];
+#pragma unroll
+        for (int i = 0; i < kRowsPerGroup; ++i) {
+            part[i] = s[i].x * kv[0] + s[i].y * kv[1] + s[i].z * kv[2] + s[i].w * kv[3];
+            part[8 + i] = s[i].x * qv[0] + s[i].y * qv[1] + s[i].z * qv[2] + s[i].w * qv[3];
+        }
+        reduce16<LPR>(part, lane);
+        float u[kRowsPerGroup];
+#pragma unroll
+        for (int i = 0; i < kRowsPerGroup; ++i) {
+            const int src_k = group_lane0 + (i * LPR) / 16;
+            float mine = 0.f;
+#pragma unroll
+            for (int j = 0; j < PER; ++j)
+                if (my_base + j == i) mine = part[j];
+            const float sk = __shfl_sync(0xffffffffu, mine, src_k);
+            u[i] = b * (__bfloat162float(sm.v[t][vrow0 + i]) - alpha * sk);
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPerGroup; ++i) {
+            s[i].x = alpha * s[i].x + u[i] * kv[0];
+            s[i].y = alpha * s[i].y + u[i] * kv[1];
+            s[i].z = alpha * s[i].z + u[i] * kv[2];
+            s[i].w = alpha * s[i].w + u[i] * kv[3];
+        }
+        // the holder lane of sq_i writes o_i (with 32 lanes per row two lanes hold each sum: the even one)
+        if (LPR != 32 || (lane & 1) == 0) {
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                const int idx = my_base + j;
+                if (idx >= 8 && idx < 16) {
+                    const int i = idx - 8;
+                    const float o = alpha * part[j] + u[i] * kq;
+                    const size_t oi = ((size_t)(tbeg + t) * hv + h) * D + row_in_head + i;
+                    if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
+                    else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(o);
+                }
+            }
+        }
+    }
+    if (srow) {
+#pragma unroll
+        for (int i = 0; i < kRowsPerGroup; ++i) srow[(size_t)i * (D / 4)] = s[i];
+    }
+}
+
+template <int D>
+cudaError_t launch_short_d(const PrefillProblem &p) {
+    const unsigned grid = (unsigned)(p.n_seqs * p.hv * (D / short_rows<D>()));
+    short_prefill_kernel<D><<<grid, short_warps<D>() * 32, 0, p.stream>>>(
+        p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.out,
+        p.out_f32, p.final_state);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_short_prefill(const PrefillProblem &p) {
+    if (p.n_seqs == 0) return cudaSuccess;
+    switch (p.d) {
+        case 32: return launch_short_d<32>(p);
+        case 64: return launch_short_d<64>(p);
+        case 128: return launch_short_d<128>(p);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_decode(const DecodeProblem &p) {
     const long total_rows = (long)p.n * p.hv * p.d;

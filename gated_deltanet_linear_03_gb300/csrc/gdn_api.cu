@@ -36,6 +36,28 @@ gdn_status check_cu(int n_seqs, int total_tokens, const int32_t *cu_host) {
     return GDN_OK;
 }
 
+// The algorithm GDN_ALGO_AUTO resolves to (arguments already validated); see gdn_prefill_algo in gdn.h.
+int resolve_auto(int n_seqs, int hv, int dk, const int32_t *cu_host) {
+    if (dk != gdn::kChunkedHeadDim) return GDN_ALGO_SCAN;
+    int max_len = 0;
+    for (int i = 0; i < n_seqs; ++i) max_len = cu_host[i + 1] - cu_host[i] > max_len ? cu_host[i + 1] - cu_host[i] : max_len;
+    if (max_len <= 16) return GDN_ALGO_SCAN;
+    if (max_len <= 32 && (long)n_seqs * hv <= 64) return GDN_ALGO_SCAN;
+    return GDN_ALGO_CHUNKED;
+}
+
+// Multiprocessors of the current device (cached per device; 1 if the query fails).
+int sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
 unsigned int *device_error_ptr() {
     static unsigned int *ptr = nullptr;
     static int dev_cached = -1;
@@ -70,10 +92,16 @@ const char *gdn_status_string(gdn_status s) {
     return "unknown gdn_status";
 }
 
+int gdn_prefill_algo(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv, const int32_t *cu_seqlens_host) {
+    if (check_heads(hk, hv, dk, dv) != GDN_OK || check_cu(n_seqs, total_tokens, cu_seqlens_host) != GDN_OK) return -1;
+    return resolve_auto(n_seqs, hv, dk, cu_seqlens_host);
+}
+
 size_t gdn_prefill_workspace_size(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
                                   const int32_t *cu_seqlens_host, int algo, gdn_status *status) {
     gdn_status st = check_heads(hk, hv, dk, dv);
     if (st == GDN_OK) st = check_cu(n_seqs, total_tokens, cu_seqlens_host);
+    if (st == GDN_OK && algo == GDN_ALGO_AUTO) algo = resolve_auto(n_seqs, hv, dk, cu_seqlens_host);
     if (st == GDN_OK && algo != GDN_ALGO_CHUNKED && algo != GDN_ALGO_SCAN) st = GDN_ERR_UNSUPPORTED;
     if (st == GDN_OK && algo == GDN_ALGO_CHUNKED && dk != gdn::kChunkedHeadDim) st = GDN_ERR_UNSUPPORTED;
     if (status) *status = st;
@@ -94,6 +122,7 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
     if (st != GDN_OK) return st;
     if ((st = check_cu(n_seqs, total_tokens, cu_seqlens_host)) != GDN_OK) return st;
     if (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
+    if (algo == GDN_ALGO_AUTO) algo = resolve_auto(n_seqs, hv, dk, cu_seqlens_host);
     if (algo != GDN_ALGO_CHUNKED && algo != GDN_ALGO_SCAN) return GDN_ERR_UNSUPPORTED;
     if (algo == GDN_ALGO_CHUNKED && dk != gdn::kChunkedHeadDim) return GDN_ERR_UNSUPPORTED;
     if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
@@ -144,7 +173,21 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
     p.err = device_error_ptr();
     p.stream = static_cast<cudaStream_t>(stream);
     if (!p.err) return GDN_ERR_CUDA;
-    const cudaError_t e = (algo == GDN_ALGO_SCAN) ? gdn::launch_scan_prefill(p) : gdn::launch_chunked_prefill(p, phases);
+    cudaError_t e;
+    if (algo == GDN_ALGO_SCAN) {
+        // Two mappings of the direct scan.  The register scan (16 rows per CTA, three CTAs per SM) has the
+        // shorter per-token chain; the row-streaming mapping needs half the CTAs and wins for short
+        // sequences once the register scan would need more than one wave of CTAs.
+        int max_len = 0;
+        for (int i = 0; i < n_seqs; ++i)
+            max_len = cu_seqlens_host[i + 1] - cu_seqlens_host[i] > max_len ? cu_seqlens_host[i + 1] - cu_seqlens_host[i]
+                                                                               : max_len;
+        const long scan_ctas = (long)n_seqs * hv * (dk / 16);
+        e = max_len <= gdn::kShortScanTokens && scan_ctas > 3L * sm_count() ? gdn::launch_short_prefill(p)
+                                                                             : gdn::launch_scan_prefill(p);
+    } else {
+        e = gdn::launch_chunked_prefill(p, phases);
+    }
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

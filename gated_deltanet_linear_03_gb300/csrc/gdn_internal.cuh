@@ -57,6 +57,10 @@ struct DecodeProblem {
 
 cudaError_t launch_decode(const DecodeProblem &p);
 cudaError_t launch_scan_prefill(const PrefillProblem &p);
+// The direct scan for batches whose longest sequence has at most kShortScanTokens tokens: state rows
+// streamed once through all of a sequence's tokens (the decode step's mapping).
+constexpr int kShortScanTokens = 32;
+cudaError_t launch_short_prefill(const PrefillProblem &p);
 // phases: bit 0 = per-chunk preparation, bit 1 = state passing + outputs
 cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases);
 size_t chunked_workspace_bytes(int n_seqs, const int32_t *cu_host, int hv, int d);

@@ -18,12 +18,12 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_OK = 0
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIGNMENT",
                 4: "GDN_ERR_CUDA", 5: "GDN_ERR_TIMEOUT", 6: "GDN_ERR_INTERNAL", 7: "GDN_ERR_WORKSPACE"}
-ALGO = {"chunked": 0, "scan": 1}
+ALGO = {"chunked": 0, "scan": 1, "auto": 2}
 DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 
 # every symbol include/gdn.h declares
 EXPORTS = ("gdn_prefill", "gdn_prefill_chunked_phase", "gdn_prefill_workspace_size", "gdn_decode_step",
-           "gdn_device_error", "gdn_status_string", "gdn_version", "gdn_prefill_noalloc")
+           "gdn_device_error", "gdn_status_string", "gdn_version", "gdn_prefill_noalloc", "gdn_prefill_algo")
 NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024
 PHASE = {"prep": 1, "pass": 2}
 
@@ -55,6 +55,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdn_prefill_noalloc.restype = I
     lib.gdn_prefill_workspace_size.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
     lib.gdn_prefill_workspace_size.restype = Z
+    lib.gdn_prefill_algo.argtypes = [I, I, I, I, I, I, P]
+    lib.gdn_prefill_algo.restype = I
     lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, P]
     lib.gdn_decode_step.restype = I
     lib.gdn_device_error.argtypes = [P]
@@ -98,6 +100,17 @@ def _host_cu(cu_seqlens: torch.Tensor, cu_host) -> Tuple[ctypes.Array, list]:
     vals = [int(x) for x in (cu_host if cu_host is not None else cu_seqlens.cpu().tolist())]
     arr = (ctypes.c_int32 * len(vals))(*vals)
     return arr, vals
+
+
+def resolve_algo(n_seqs: int, total_tokens: int, hk: int, hv: int, dk: int, dv: int,
+                 cu_seqlens_host: Sequence[int]) -> str:
+    """The algorithm ``algo="auto"`` runs for this problem (``gdn_prefill_algo``)."""
+    lib = load_library()
+    arr = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+    a = lib.gdn_prefill_algo(n_seqs, total_tokens, hk, hv, dk, dv, arr)
+    if a < 0:
+        raise GdnError(1, "gdn_prefill_algo")
+    return {v: k for k, v in ALGO.items()}[a]
 
 
 def workspace_size(n_seqs: int, total_tokens: int, hk: int, hv: int, dk: int, dv: int,

@@ -70,7 +70,11 @@ typedef enum {
 
 typedef enum {
     GDN_ALGO_CHUNKED = 0,  /* blocked evaluation, 64-token chunks, tcgen05 tensor cores */
-    GDN_ALGO_SCAN = 1      /* direct token-by-token scan, state held in registers */
+    GDN_ALGO_SCAN = 1,     /* direct token-by-token scan, state held in registers; when no sequence
+                              has more than 32 tokens and the batch needs more than one wave of
+                              16-row CTAs, each state row is instead streamed once through all of
+                              its sequence's tokens (the decode step's mapping) */
+    GDN_ALGO_AUTO = 2      /* the faster of the two for this problem, chosen on the host (gdn_prefill_algo) */
 } gdn_algo;
 
 typedef enum {
@@ -98,7 +102,7 @@ typedef enum {
  *   final_state      fp32 [n_seqs, hv, dv, dk] or NULL.  It may be the same
  *                    buffer as init_state (updated in place); any other overlap
  *                    with an input is an error.
- *   algo             GDN_ALGO_CHUNKED or GDN_ALGO_SCAN
+ *   algo             GDN_ALGO_CHUNKED, GDN_ALGO_SCAN or GDN_ALGO_AUTO
  *   workspace        device scratch of at least gdn_prefill_workspace_size()
  *                    bytes (may be NULL when that size is 0), 256-byte aligned.
  *                    Its contents on entry do not matter.
@@ -138,12 +142,32 @@ GDN_API gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_to
                                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Bytes of device workspace gdn_prefill needs for this problem (0 for
- * GDN_ALGO_SCAN).  Returns 0 and sets *status (if non-NULL) to an error code
- * when the arguments are invalid.
+ * Bytes of device workspace gdn_prefill needs for this problem (0 when the
+ * algorithm is, or GDN_ALGO_AUTO resolves to, GDN_ALGO_SCAN).  Returns 0 and
+ * sets *status (if non-NULL) to an error code when the arguments are invalid.
  */
 GDN_API size_t gdn_prefill_workspace_size(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
                                   const int32_t *cu_seqlens_host, int algo, gdn_status *status);
+
+/*
+ * gdn_prefill_algo: the algorithm GDN_ALGO_AUTO resolves to for this problem
+ * (GDN_ALGO_CHUNKED or GDN_ALGO_SCAN), or -1 when the arguments are invalid.
+ * "Optimizing on-device inference for Apple Silicon", section "Qwen creates
+ * three workload shapes": whether the direct scan or the blocked form is
+ * faster depends on the model dimensions, the workload and the hardware.  The
+ * rule is a host-side function of the sequence lengths and head count, fitted
+ * to a sweep of both paths on GB300 (N sequences of T tokens, d = 128, 32
+ * value heads):
+ *   - the scan when the longest sequence has at most 16 tokens, or at most 32
+ *     tokens with n_seqs * hv <= 64 (the chunked path pays a fixed cost of
+ *     about 16 us for one short sequence and 45 us for eight);
+ *   - the scan whenever dk != 128 (the chunked path implements d = 128 only);
+ *   - the chunked path otherwise.
+ * It needs no CUDA call.  gdn_prefill and gdn_prefill_workspace_size apply the
+ * same rule, so a workspace sized for GDN_ALGO_AUTO fits what gdn_prefill runs.
+ */
+GDN_API int gdn_prefill_algo(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                             const int32_t *cu_seqlens_host);
 
 /*
  * gdn_decode_step: one token for each of n independent states (batch-1 decode

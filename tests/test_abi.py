@@ -120,3 +120,36 @@ def test_decode_rejects_bad_args(lib):
     assert dec(q=FAKE + 8) == 3
     assert dec(odt=3) == 2
     assert dec(out=FAKE) == 1                # out overlaps state
+
+
+def test_auto_algo_rule(lib):
+    """gdn_prefill_algo: the scan for short sequences (<= 16 tokens, or <= 32 with at most 64 (sequence,
+    head) pairs) and whenever d != 128, the chunked path otherwise; -1 for invalid arguments."""
+    algo = lambda n, hv, d, cu: lib.gdn_prefill_algo(n, cu[-1], 1, hv, d, d, _cu(cu))
+    assert algo(1, 32, 128, [0, 16]) == 1
+    assert algo(1, 32, 128, [0, 32]) == 1
+    assert algo(1, 32, 128, [0, 33]) == 0
+    assert algo(8, 32, 128, [0, 2, 4, 6, 8, 10, 12, 14, 16]) == 1
+    assert algo(8, 32, 128, list(range(0, 9 * 24, 24))) == 0    # 256 (sequence, head) pairs of 24 tokens
+    assert algo(2, 32, 128, [0, 1, 30]) == 1                     # 64 pairs, longest 29
+    assert algo(1, 32, 128, [0, 4096]) == 0
+    assert algo(1, 4, 64, [0, 4096]) == 1                        # chunked implements d = 128 only
+    assert algo(1, 32, 128, [0, 5]) == 1
+    assert lib.gdn_prefill_algo(1, 64, 3, 2, 128, 128, _cu([0, 64])) == -1   # hv % hk
+    assert lib.gdn_prefill_algo(1, 64, 1, 2, 128, 128, _cu([0, 63])) == -1   # cu does not end at T
+
+
+def test_auto_workspace_matches_resolved_algo(lib):
+    st = ctypes.c_int(-1)
+    for cu in ([0, 16], [0, 200], [0, 64, 200]):
+        n = len(cu) - 1
+        resolved = lib.gdn_prefill_algo(n, cu[-1], 1, 32, 128, 128, _cu(cu))
+        want = lib.gdn_prefill_workspace_size(n, cu[-1], 1, 32, 128, 128, _cu(cu), resolved, ctypes.byref(st))
+        got = lib.gdn_prefill_workspace_size(n, cu[-1], 1, 32, 128, 128, _cu(cu), 2, ctypes.byref(st))
+        assert st.value == 0 and got == want
+        assert (got == 0) == (resolved == 1)
+
+
+def test_auto_requires_workspace_only_when_chunked(lib):
+    # 200 tokens resolves to the chunked path, which needs a workspace
+    assert prefill(lib, T=200, cu_host=_cu([0, 200]), algo=2, ws=None, wsb=0) == 7
