@@ -52,9 +52,10 @@ def _load():
             lib = ctypes.CDLL(build())
             P = ctypes.c_void_p
             I = ctypes.c_int
-            lib.gdn_oracle_prefill.argtypes = [I, P, I, I, I, I, P, P, P, P, P, P, P, P, I]
-            lib.gdn_oracle_prefill_chunked.argtypes = [I, P, I, I, I, I, P, P, P, P, P, P, P, P, I, I]
-            lib.gdn_oracle_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I]
+            Dbl = ctypes.c_double
+            lib.gdn_oracle_prefill.argtypes = [I, P, I, I, I, I, P, P, P, P, P, P, P, P, I, Dbl, I]
+            lib.gdn_oracle_prefill_chunked.argtypes = [I, P, I, I, I, I, P, P, P, P, P, P, P, P, I, I, Dbl, I]
+            lib.gdn_oracle_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, Dbl, I]
             for f in (lib.gdn_oracle_prefill, lib.gdn_oracle_prefill_chunked, lib.gdn_oracle_decode_step):
                 f.restype = I
             lib.gdn_oracle_max_threads.restype = I
@@ -87,8 +88,11 @@ def _shapes(q, k, v):
 
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, n_threads=None,
-            want_out=True):
-    """Sequential fp64 scan.  Returns (out [T,hv,dv] fp64 or None, final_state [N,hv,dv,dk] fp64)."""
+            want_out=True, qk_norm=False, q_scale=1.0):
+    """Sequential fp64 scan.  Returns (out [T,hv,dv] fp64 or None, final_state [N,hv,dv,dk] fp64).
+
+    ``qk_norm``: L2-normalise every q and k head vector first (x / sqrt(|x|^2 + 1e-6)); q is then
+    multiplied by ``q_scale``."""
     q, k, v = _f32(q), _f32(k), _f32(v)
     la, b = _f32(log_alpha), _f32(beta)
     T, hk, dk, hv, dv = _shapes(q, k, v)
@@ -101,14 +105,14 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, n_threads=
     fin = np.zeros((N, hv, dv, dk), np.float64)
     rc = _load().gdn_oracle_prefill(N, _ptr(cu), hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v),
                                     _ptr(la), _ptr(b), _ptr(s0), _ptr(out), _ptr(fin),
-                                    int(n_threads or max_threads()))
+                                    int(bool(qk_norm)), float(q_scale), int(n_threads or max_threads()))
     if rc:
         raise RuntimeError(f"gdn_oracle_prefill failed: {rc}")
     return out, fin
 
 
 def prefill_chunked(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, chunk,
-                    n_threads=None):
+                    n_threads=None, qk_norm=False, q_scale=1.0):
     """Blocked fp64 evaluation with chunk size ``chunk``; same return as :func:`prefill`."""
     q, k, v = _f32(q), _f32(k), _f32(v)
     la, b = _f32(log_alpha), _f32(beta)
@@ -120,13 +124,14 @@ def prefill_chunked(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, ch
     fin = np.zeros((N, hv, dv, dk), np.float64)
     rc = _load().gdn_oracle_prefill_chunked(N, _ptr(cu), hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v),
                                             _ptr(la), _ptr(b), _ptr(s0), _ptr(out), _ptr(fin),
-                                            int(chunk), int(n_threads or max_threads()))
+                                            int(chunk), int(bool(qk_norm)), float(q_scale),
+                                            int(n_threads or max_threads()))
     if rc:
         raise RuntimeError(f"gdn_oracle_prefill_chunked failed: {rc}")
     return out, fin
 
 
-def decode_step(state, q, k, v, log_alpha, beta, *, n_threads=None):
+def decode_step(state, q, k, v, log_alpha, beta, *, n_threads=None, qk_norm=False, q_scale=1.0):
     """One token per state.  state [n,hv,dv,dk]; q,k [n,hk,dk]; v [n,hv,dv]; gates [n,hv].
 
     Returns (out [n,hv,dv] fp64, new_state fp64); the input array is not modified.
@@ -139,7 +144,8 @@ def decode_step(state, q, k, v, log_alpha, beta, *, n_threads=None):
         raise ValueError("state must be [n, hv, dv, dk]")
     out = np.zeros((n, hv, dv), np.float64)
     rc = _load().gdn_oracle_decode_step(n, hk, hv, dk, dv, _ptr(st), _ptr(q), _ptr(k), _ptr(v),
-                                        _ptr(la), _ptr(b), _ptr(out), int(n_threads or max_threads()))
+                                        _ptr(la), _ptr(b), _ptr(out), int(bool(qk_norm)), float(q_scale),
+                                        int(n_threads or max_threads()))
     if rc:
         raise RuntimeError(f"gdn_oracle_decode_step failed: {rc}")
     return out, st

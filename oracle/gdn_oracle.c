@@ -26,6 +26,14 @@
  *     S <- alpha_t S + beta_t (v_t - alpha_t S k_t) k_t^T .
  * Value head h reads query/key head h / (hv / hk).
  *
+ * Query/key preparation (optional, qk_norm != 0): the pages' decode path fuses
+ * "query and key preparation" into its kernels ("Optimizing on-device
+ * inference for Apple Silicon", section "Reduce intermediate and state
+ * traffic"); the benchmark spec describes q and k as L2-normalised with q
+ * scaled by 1/sqrt(dk).  With qk_norm each head vector x of q and k is
+ * replaced by x / sqrt(sum_j x_j^2 + 1e-6) before the recurrence; in every
+ * case q is then multiplied by q_scale (1 leaves q as given).
+ *
  * Layouts (row-major): q,k [T, hk, dk]; v [T, hv, dv]; log_alpha, beta
  * [T, hv]; state [n_seqs, hv, dv, dk] (row = value index); out [T, hv, dv].
  * cu_seqlens [n_seqs + 1] holds token offsets of the packed sequences.
@@ -50,25 +58,44 @@ static int check_common(int n_seqs, const int32_t *cu, int hk, int hv, int dk, i
     return 0;
 }
 
+/* Query/key preparation of one token (see the header), in fp64. */
+static void prep_qk(const float *q, const float *k, int dk, int qk_norm, double q_scale,
+                    double *qd, double *kd)
+{
+    double sq = 0.0, sk = 0.0;
+    for (int j = 0; j < dk; ++j) {
+        qd[j] = (double)q[j];
+        kd[j] = (double)k[j];
+        sq += qd[j] * qd[j];
+        sk += kd[j] * kd[j];
+    }
+    const double fq = q_scale * (qk_norm ? 1.0 / sqrt(sq + 1e-6) : 1.0);
+    const double fk = qk_norm ? 1.0 / sqrt(sk + 1e-6) : 1.0;
+    for (int j = 0; j < dk; ++j) {
+        qd[j] *= fq;
+        kd[j] *= fk;
+    }
+}
+
 /* One token of the recurrence on one (sequence, head) state, fp64. */
-static void token_update(double *S, int dk, int dv, const float *q, const float *k,
+static void token_update(double *S, int dk, int dv, const double *q, const double *k,
                          const float *v, double log_alpha, double beta, double *o,
                          double *sk)
 {
     const double alpha = exp(log_alpha);   /* log_alpha = -inf gives alpha = 0 */
     for (int i = 0; i < dv; ++i) {
         double acc = 0.0;
-        for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * (double)k[j];
+        for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * k[j];
         sk[i] = acc;
     }
     for (int i = 0; i < dv; ++i) {
         const double u = beta * ((double)v[i] - alpha * sk[i]);
         for (int j = 0; j < dk; ++j)
-            S[(size_t)i * dk + j] = alpha * S[(size_t)i * dk + j] + u * (double)k[j];
+            S[(size_t)i * dk + j] = alpha * S[(size_t)i * dk + j] + u * k[j];
     }
     for (int i = 0; i < dv; ++i) {
         double acc = 0.0;
-        for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * (double)q[j];
+        for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * q[j];
         o[i] = acc;
     }
 }
@@ -77,7 +104,7 @@ int gdn_oracle_prefill(int n_seqs, const int32_t *cu_seqlens, int hk, int hv, in
                        const float *q, const float *k, const float *v,
                        const float *log_alpha, const float *beta,
                        const double *init_state, double *out, double *final_state,
-                       int n_threads)
+                       int qk_norm, double q_scale, int n_threads)
 {
     int rc = check_common(n_seqs, cu_seqlens, hk, hv, dk, dv);
     if (rc) return rc;
@@ -89,15 +116,15 @@ int gdn_oracle_prefill(int n_seqs, const int32_t *cu_seqlens, int hk, int hv, in
 #pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
     for (long unit = 0; unit < n_units; ++unit) {
         const int n = (int)(unit / hv), h = (int)(unit % hv), hq = h / group;
-        double *S = (double *)malloc(sizeof(double) * ((size_t)dv * dk + 2 * (size_t)dv));
+        double *S = (double *)malloc(sizeof(double) * ((size_t)dv * dk + 2 * (size_t)dv + 2 * (size_t)dk));
         if (!S) { failed = 1; continue; }
-        double *sk = S + (size_t)dv * dk, *o = sk + dv;
+        double *sk = S + (size_t)dv * dk, *o = sk + dv, *qd = o + dv, *kd = qd + dk;
         const size_t soff = ((size_t)n * hv + h) * dv * dk;
         if (init_state) memcpy(S, init_state + soff, sizeof(double) * dv * dk);
         else memset(S, 0, sizeof(double) * dv * dk);
         for (int t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
-            token_update(S, dk, dv, q + ((size_t)t * hk + hq) * dk, k + ((size_t)t * hk + hq) * dk,
-                         v + ((size_t)t * hv + h) * dv, log_alpha[(size_t)t * hv + h],
+            prep_qk(q + ((size_t)t * hk + hq) * dk, k + ((size_t)t * hk + hq) * dk, dk, qk_norm, q_scale, qd, kd);
+            token_update(S, dk, dv, qd, kd, v + ((size_t)t * hv + h) * dv, log_alpha[(size_t)t * hv + h],
                          beta[(size_t)t * hv + h], o, sk);
             if (out) memcpy(out + ((size_t)t * hv + h) * dv, o, sizeof(double) * dv);
         }
@@ -115,7 +142,7 @@ int gdn_oracle_prefill(int n_seqs, const int32_t *cu_seqlens, int hk, int hv, in
 int gdn_oracle_decode_step(int n, int hk, int hv, int dk, int dv, double *state,
                            const float *q, const float *k, const float *v,
                            const float *log_alpha, const float *beta, double *out,
-                           int n_threads)
+                           int qk_norm, double q_scale, int n_threads)
 {
     if (n < 0 || hk <= 0 || hv <= 0 || dk <= 0 || dv <= 0 || hv % hk) return -1;
     const int group = hv / hk;
@@ -125,11 +152,12 @@ int gdn_oracle_decode_step(int n, int hk, int hv, int dk, int dv, double *state,
 #pragma omp parallel for schedule(static) num_threads(n_threads)
     for (long unit = 0; unit < n_units; ++unit) {
         const int b = (int)(unit / hv), h = (int)(unit % hv), hq = h / group;
-        double *tmp = (double *)malloc(sizeof(double) * 2 * (size_t)dv);
+        double *tmp = (double *)malloc(sizeof(double) * (2 * (size_t)dv + 2 * (size_t)dk));
         if (!tmp) { failed = 1; continue; }
+        double *qd = tmp + 2 * (size_t)dv, *kd = qd + dk;
         double *S = state + ((size_t)b * hv + h) * dv * dk;
-        token_update(S, dk, dv, q + ((size_t)b * hk + hq) * dk, k + ((size_t)b * hk + hq) * dk,
-                     v + ((size_t)b * hv + h) * dv, log_alpha[(size_t)b * hv + h],
+        prep_qk(q + ((size_t)b * hk + hq) * dk, k + ((size_t)b * hk + hq) * dk, dk, qk_norm, q_scale, qd, kd);
+        token_update(S, dk, dv, qd, kd, v + ((size_t)b * hv + h) * dv, log_alpha[(size_t)b * hv + h],
                      beta[(size_t)b * hv + h], tmp + dv, tmp);
         if (out) memcpy(out + ((size_t)b * hv + h) * dv, tmp + dv, sizeof(double) * dv);
         free(tmp);
@@ -162,7 +190,7 @@ int gdn_oracle_prefill_chunked(int n_seqs, const int32_t *cu_seqlens, int hk, in
                                int dv, const float *q, const float *k, const float *v,
                                const float *log_alpha, const float *beta,
                                const double *init_state, double *out, double *final_state,
-                               int chunk, int n_threads)
+                               int chunk, int qk_norm, double q_scale, int n_threads)
 {
     int rc = check_common(n_seqs, cu_seqlens, hk, hv, dk, dv);
     if (rc) return rc;
@@ -193,10 +221,8 @@ int gdn_oracle_prefill_chunked(int n_seqs, const int32_t *cu_seqlens, int hk, in
             double bet[L > 0 ? L : 1];
             for (int i = 0; i < L; ++i) {
                 const size_t t = (size_t)t0 + i;
-                for (int j = 0; j < dk; ++j) {
-                    Kc[(size_t)i * dk + j] = k[(t * hk + hq) * dk + j];
-                    Qc[(size_t)i * dk + j] = q[(t * hk + hq) * dk + j];
-                }
+                prep_qk(q + (t * hk + hq) * dk, k + (t * hk + hq) * dk, dk, qk_norm, q_scale,
+                        Qc + (size_t)i * dk, Kc + (size_t)i * dk);
                 for (int j = 0; j < dv; ++j) Vc[(size_t)i * dv + j] = v[(t * hv + h) * dv + j];
                 g[i] = (i ? g[i - 1] : 0.0) + (double)log_alpha[t * hv + h];
                 bet[i] = beta[t * hv + h];

@@ -249,6 +249,79 @@ def test_parallel_form_brute_force():
             np.testing.assert_allclose(fin[0, 0], St, atol=1e-12)
 
 
+# ---------------------------------------------------------------- query/key preparation (qk_norm, q_scale)
+
+def test_qk_norm_single_token_by_hand():
+    """dk = 2, S0 = 0, one token: S = beta v k_n^T and o = S q_n with k_n = k / sqrt(|k|^2 + 1e-6)."""
+    q = np.array([[[1.0, 2.0]]], np.float32)
+    k = np.array([[[3.0, 4.0]]], np.float32)
+    v = np.array([[[2.0, -1.0, 0.5]]], np.float32)
+    la = np.array([[0.0]], np.float32)
+    b = np.array([[0.5]], np.float32)
+    scale = 0.25
+    out, fin = oracle.prefill(q, k, v, la, b, one_seq(1), qk_norm=True, q_scale=scale)
+    kn = np.array([3.0, 4.0]) / math.sqrt(25.0 + 1e-6)
+    qn = np.array([1.0, 2.0]) / math.sqrt(5.0 + 1e-6) * scale
+    S = 0.5 * np.outer([2.0, -1.0, 0.5], kn)
+    np.testing.assert_allclose(fin[0, 0], S, rtol=1e-14)
+    np.testing.assert_allclose(out[0, 0], S @ qn, rtol=1e-14)
+
+
+@pytest.mark.parametrize("path", ["prefill", "chunked", "decode"])
+def test_qk_norm_ignores_the_length_of_q_and_k(path):
+    """With qk_norm, rescaling any token's q or k by a positive factor changes nothing (up to the 1e-6
+    floor under the norm, kept negligible here by norms far above it)."""
+    rng = np.random.default_rng(40)
+    T = 9
+    q, k, v, la, b, s0 = rand_case(rng, T, hk=2, hv=4, dk=6, dv=5, unit_k=False)
+    cq = rng.uniform(0.5, 4.0, (T, 2, 1)).astype(np.float32)
+    ck = rng.uniform(0.5, 4.0, (T, 2, 1)).astype(np.float32)
+    def run(qq, kk):
+        if path == "prefill":
+            return oracle.prefill(qq, kk, v, la, b, one_seq(T), s0, qk_norm=True, q_scale=0.3)
+        if path == "chunked":
+            return oracle.prefill_chunked(qq, kk, v, la, b, one_seq(T), s0, chunk=4, qk_norm=True, q_scale=0.3)
+        st0 = np.repeat(s0, T, axis=0)   # T independent states, one token each
+        return oracle.decode_step(st0, qq, kk, v, la, b, qk_norm=True, q_scale=0.3)
+    o1, f1 = run(q, k)
+    o2, f2 = run(q * cq, k * ck)   # the rescaled inputs are rounded to fp32: agreement to ~1e-7 relative
+    np.testing.assert_allclose(o2, o1, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(f2, f1, rtol=1e-5, atol=1e-6)
+
+
+def test_qk_norm_on_unit_vectors_is_the_plain_recurrence():
+    rng = np.random.default_rng(41)
+    T = 7
+    q, k, v, la, b, s0 = rand_case(rng, T, hk=1, hv=2, dk=5, dv=3)
+    q = (q / np.linalg.norm(q, axis=-1, keepdims=True)).astype(np.float32)
+    o1, f1 = oracle.prefill(q, k, v, la, b, one_seq(T), s0)
+    o2, f2 = oracle.prefill(q, k, v, la, b, one_seq(T), s0, qk_norm=True)
+    # 1/sqrt(|x|^2 + 1e-6) differs from 1 by ~5e-7 (plus the fp32 rounding of the unit vectors)
+    np.testing.assert_allclose(o2, o1, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(f2, f1, rtol=1e-5, atol=1e-6)
+
+
+def test_q_scale_scales_outputs_only():
+    """o = S q is linear in q; the state never reads q."""
+    rng = np.random.default_rng(42)
+    T = 6
+    q, k, v, la, b, s0 = rand_case(rng, T, hk=1, hv=2, dk=4, dv=3)
+    o1, f1 = oracle.prefill(q, k, v, la, b, one_seq(T), s0)
+    o2, f2 = oracle.prefill(q, k, v, la, b, one_seq(T), s0, q_scale=0.125)
+    np.testing.assert_array_equal(f2, f1)
+    np.testing.assert_allclose(o2, 0.125 * o1, rtol=1e-13, atol=1e-15)
+
+
+def test_chunked_with_qk_norm_equals_sequential():
+    rng = np.random.default_rng(43)
+    T = 23
+    q, k, v, la, b, s0 = rand_case(rng, T, hk=1, hv=2, dk=5, dv=4, unit_k=False)
+    o1, f1 = oracle.prefill(q, k, v, la, b, one_seq(T), s0, qk_norm=True, q_scale=0.5)
+    o2, f2 = oracle.prefill_chunked(q, k, v, la, b, one_seq(T), s0, chunk=8, qk_norm=True, q_scale=0.5)
+    np.testing.assert_allclose(o2, o1, rtol=1e-9, atol=1e-10)
+    np.testing.assert_allclose(f2, f1, rtol=1e-9, atol=1e-10)
+
+
 # ---------------------------------------------------------------- decode, packing, grouping
 
 def test_decode_chain_equals_prefill():
