@@ -294,6 +294,43 @@ def time_decode_per_layer(dev, stream, steps=64, n_rep=5):
     return s.elapsed_time(e) * 1e3 / steps
 
 
+def time_qk_prep(dev, stream, iters=20):
+    """The 4K layer from raw q/k projections: L2 normalisation and q scaling fused into the kernels
+    (qk_norm), against the same done as a separate PyTorch pass before the plain call."""
+    import torch
+    import torch.nn.functional as F
+    from gated_deltanet_linear_03_gb300 import gdn, synth
+    inp = synth.prefill_inputs([T_TOKENS], hk=HK, hv=HV, dk=D, dv=D, seed=1001, raw_qk=True)
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    la, b, cu = inp.log_alpha.to(dev), inp.beta.to(dev), inp.cu_seqlens.to(dev)
+    cu_host = inp.cu_seqlens.tolist()
+    scale = 1.0 / math.sqrt(D)
+    fused = gdn.PrefillPlan(q, k, v, la, b, cu, cu_seqlens_host=cu_host, qk_norm=True, q_scale=scale)
+    qn, kn = torch.empty_like(q), torch.empty_like(k)
+    plain = gdn.PrefillPlan(qn, kn, v, la, b, cu, cu_seqlens_host=cu_host)
+
+    def separate():
+        qn.copy_((F.normalize(q.float(), dim=-1, eps=1e-3) * scale).to(torch.bfloat16))
+        kn.copy_(F.normalize(k.float(), dim=-1, eps=1e-3).to(torch.bfloat16))
+        plain.run(stream=stream)
+
+    res = {}
+    for name, fn in (("fused_us", lambda: fused.run(stream=stream)), ("separate_pass_us", separate)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(iters):
+                fn()
+            e0.record(stream)
+        torch.cuda.synchronize()
+        res[name] = s0.elapsed_time(e0) * 1e3 / iters
+    res["workload"] = "4K layer from raw q/k projections (L2-normalise q and k, q / sqrt(d))"
+    return res
+
+
 def run_each_kernel_once(args):
     """Two passes of every kernel of the path on the bench workload (chunk preparation, state pass,
     direct scan, 30-layer decode), nothing timed: the target for profiler captures."""
@@ -509,6 +546,7 @@ def run_gb300(args):
         decode_us = time_decode(dev, stream)
         decode_layer_us = time_decode_per_layer(dev, stream)
         scan_ms = time_scan(plan_scan, stream)
+        qk_prep = time_qk_prep(dev, stream)
     clocks = clk.summary()
     e2e_tps, h2d, d2h = time_e2e(host, cu_host, dev, stream, max(3, min(args.steps, 20)))
     err = gdn.device_error(stream)
@@ -551,6 +589,7 @@ def run_gb300(args):
                                                     "CUDA graph"}},
         "scan": {"tok_per_s": T_TOKENS / (scan_ms * 1e-3), "ms": scan_ms,
                  "fp32_tflops": FLOPS_SCAN * T_TOKENS * HV / (scan_ms * 1e-3) / 1e12},
+        "qk_prep": qk_prep,
         "e2e": {"value": e2e_units / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,

@@ -47,6 +47,7 @@ constexpr uint32_t kSW = kLayoutSwizzle128B;
 
 constexpr size_t kPTile = (size_t)D * C * 2;     // P_hi or P_lo of one (chunk, head): 16 KiB
 constexpr size_t kRTile = (size_t)C * C * 2;     // R of one (chunk, head): 8 KiB
+constexpr size_t kNormBytes = 2 * C * 4;         // q/k preparation factors of one (chunk, head): f_k [64], f_q [64]
 
 // ---------------------------------------------------------------- chunk lookup
 struct ChunkLoc {
@@ -149,8 +150,9 @@ constexpr uint32_t PREP_A = 32768;     // fp32 A [64][68]; later (Gamma T)^T hi 
 constexpr int A_LD = 68;
 constexpr uint32_t PREP_AQK = PREP_A + 64 * A_LD * 4;   // 50176: Aqk hi, Aqk lo tiles [64 x 64] bf16
 constexpr uint32_t PREP_Y = PREP_AQK + 16384;           // fp32 scratch [3][16][16]
-constexpr uint32_t PREP_G = PREP_Y + 3 * 256 * 4;       // g [64], beta [64], Gamma = e^{g_L - g} [64]
-constexpr uint32_t PREP_SMEM = PREP_G + 768 + 1024;     // + alignment slack: 3 CTAs per SM
+constexpr uint32_t PREP_G = PREP_Y + 3 * 256 * 4;       // g [64], beta [64], Gamma = e^{g_L - g} [64],
+                                                        // then the q/k preparation factors f_k [64], f_q [64]
+constexpr uint32_t PREP_SMEM = PREP_G + 1280 + 1024;    // + alignment slack: 3 CTAs per SM
 constexpr uint32_t PREP_TMEM_COLS = 128;
 
 // Row ii of T (fp32, 64 columns): rows 0-31 over the Q half of k-block 0, rows 32-63 over that of k-block 1.
@@ -252,7 +254,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
                   const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
                   const float *__restrict__ log_alpha, const float *__restrict__ beta,
-                  const int32_t *__restrict__ cu, int n_seqs, int total, int hk, int hv, unsigned int *err) {
+                  const int32_t *__restrict__ cu, int n_seqs, int total, int hk, int hv, float *__restrict__ norms,
+                  int qk_norm, float q_scale, unsigned int *err) {
     extern __shared__ uint8_t prep_raw[];
     uint8_t *sm = align1024(prep_raw);
     __shared__ uint64_t bar_tma, bar_mma;
@@ -286,6 +289,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     float *g_s = reinterpret_cast<float *>(sm + PREP_G);  // [64]
     float *b_s = g_s + 64;                                // [64]
     float *gam_s = g_s + 128;                             // [64], 0 past the chunk's end
+    float *kf_s = g_s + 192, *qf_s = g_s + 256;           // [64] each: f_k = 1/|k| (or 1), f_q = q_scale/|q| (or q_scale)
     // warp 1 loads this chunk's gates now; their cumulative sum is formed while the TMA and MMA run
     float la0 = 0.f, la1 = 0.f, bt0 = 0.f, bt1 = 0.f;
     if (warp == 1) {
@@ -325,6 +329,34 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         }
         mma_commit(&bar_mma);
     }
+    {   // Query/key preparation factors of the 64 k rows (threads 0-63) and 64 q rows (64-127), from the staged
+        // tiles (which the MMA above only reads).  The products use raw q and k; the factors scale rows and
+        // columns of [K;Q]K^T and the rows of P = K^T diag(f_k) Gamma T.  The state pass reads them from the
+        // workspace.
+        const int r = tid & 63;
+        const bool isq = tid >= 64;
+        float f = isq ? q_scale : 1.f;
+        if (qk_norm) {
+            float ss = 0.f;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+                for (int c = 0; c < 64; c += 8) {
+                    const uint4 x =
+                        *reinterpret_cast<const uint4 *>(sm + PREP_KQ + kb * 16384 + (isq ? 8192 : 0) + sw128_offset(r, c));
+                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        ss = fmaf(bf16_lo(w[e]), bf16_lo(w[e]), ss);
+                        ss = fmaf(bf16_hi(w[e]), bf16_hi(w[e]), ss);
+                    }
+                }
+            }
+            f *= qk_inv_norm(ss, 1);
+        }
+        (isq ? qf_s : kf_s)[r] = f;
+        if (ok && qk_norm) norms[((size_t)gc * hv + h) * 128 + tid] = f;   // read by the pass only with qk_norm
+    }
     if (warp == 1) {
         const float2 g2 = cumsum_pairs(la0, la1, L, lane);
         const float gl = g_of(g2, L - 1);
@@ -338,6 +370,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     if (ok) ok = mbar_wait(&bar_mma, 0);
     ok = __syncthreads_and(ok);
     tc_fence_after();
+    if (qk_norm && tid < 64) gam_s[tid] *= kf_s[tid];   // P = K^T diag(f_k Gamma) T (read after the solve's barriers)
     {   // T (over the Q rows, which [K;Q]K^T no longer needs) starts at zero; its upper blocks stay zero
         float4 *t0q = reinterpret_cast<float4 *>(sm + PREP_KQ + 8192);
         float4 *t1q = reinterpret_cast<float4 *>(sm + PREP_KQ + 24576);
@@ -373,10 +406,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 }
             }
         }
+        if (qk_norm) {
+#pragma unroll
+            for (int jj = 0; jj < 64; ++jj)
+                if (jj < 32 || !low_rows) vals[jj] *= kf_s[jj];   // column factor f_k,j
+        }
         const float gi = g_s[i];
         const bool row_ok = ok && i < L;
         if (warp < 2) {
-            const float bi = b_s[i];
+            const float bi = b_s[i] * kf_s[i];                  // row factor f_k,i
             float *arow = reinterpret_cast<float *>(sm + PREP_A) + i * A_LD;
 #pragma unroll
             for (int jj = 0; jj < 64; jj += 4) {
@@ -394,9 +432,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
                 if (jj < 32 || !low_rows) {
                     float x[8];
+                    const float fqi = qf_s[i];                  // row factor f_q,i
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        x[e] = (row_ok && jj + e <= i) ? __expf(gi - g_s[jj + e]) * vals[jj + e] : 0.f;
+                        x[e] = (row_ok && jj + e <= i) ? fqi * __expf(gi - g_s[jj + e]) * vals[jj + e] : 0.f;
                     split8_bf16(x, hi, lo);
                 }
                 const uint32_t off = sw128_offset(i, jj);
@@ -568,14 +607,18 @@ constexpr int DG = DS / 2;          // state rows per thread (the two warp group
 // row piece); loaded one chunk ahead so that their latency is off the state chain.
 struct ChunkInputs {
     float la0, la1;   // log_alpha of tokens 2*lane, 2*lane+1 (raw; 0 past the end)
+    float f;          // q/k preparation factor of this thread's token row (f_k for K rows, f_q for Q rows)
     float b;          // beta of this thread's token row (K-row threads)
     uint4 v[DG / 8];  // 16 bf16 of this thread's v row piece (K-row threads)
 };
 
 __device__ __forceinline__ void load_chunk_inputs(ChunkInputs &in, const float *__restrict__ log_alpha,
                                                   const float *__restrict__ beta, const __nv_bfloat16 *__restrict__ v,
-                                                  int t0, int L, int hv, int h, int rowg, int lane, bool krow, int i) {
+                                                  const float *__restrict__ norms, float q_scale, int gcx, int t0,
+                                                  int L, int hv, int h, int rowg, int lane, bool krow, int i) {
     const int i0 = 2 * lane, i1 = 2 * lane + 1;
+    // norms is null without qk_norm: the factors are then 1 (k) and q_scale (q)
+    in.f = norms ? norms[((size_t)gcx * hv + h) * 128 + (krow ? i : 64 + i)] : (krow ? 1.f : q_scale);
     in.la0 = i0 < L ? log_alpha[(size_t)(t0 + i0) * hv + h] : 0.f;
     in.la1 = i1 < L ? log_alpha[(size_t)(t0 + i1) * hv + h] : 0.f;
     in.b = 0.f;
@@ -624,7 +667,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
                   const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
-                  const __nv_bfloat16 *__restrict__ v,
+                  const __nv_bfloat16 *__restrict__ v, const float *__restrict__ norms, float q_scale,
                   const float *__restrict__ log_alpha, const float *__restrict__ beta,
                   const float *__restrict__ init_state, const int32_t *__restrict__ cu, int n_seqs, int total,
                   int nch, int hk, int hv, void *__restrict__ out, int out_f32, float *__restrict__ final_state,
@@ -686,7 +729,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         pass_issue_loads(sm, &bar_tma[0], &qmap, &kmap, &phmap, &plmap, &rhmap, &rlmap, hq, ta, gc0, hv, h);
     }
     ChunkInputs nxt;
-    if (started) load_chunk_inputs(nxt, log_alpha, beta, v, ta, min(C, tb - ta), hv, h, rowg, lane, krow, i);
+    if (started)
+        load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0, ta, min(C, tb - ta), hv, h, rowg, lane, krow, i);
 
     // state columns: thread (d, grp) holds S[rowg + r][d] for r < 16
     float S[DG];
@@ -760,7 +804,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 ok = false;
         }
         if (c + 1 < nchunks)
-            load_chunk_inputs(nxt, log_alpha, beta, v, t0 + C, min(C, tb - t0 - C), hv, h, rowg, lane, krow, i);
+            load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc + 1, t0 + C, min(C, tb - t0 - C), hv, h,
+                              rowg, lane, krow, i);
 
         const float2 g2 = cumsum_pairs(cur.la0, cur.la1, L, lane);
         const float gL = g_of(g2, L - 1);
@@ -775,7 +820,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             tc_fence_after();
             float a[16], b[16];   // x S_hi^T and x S_lo^T, this group's 16 rows
             tmem_ld16x2(tmem + tlane + TM_D1 + grp * 16, tmem + tlane + TM_D1 + 32 + grp * 16, a, b);
-            const float bi = cur.b, be = cur.b * eg;
+            const float bi = cur.b, be = cur.b * eg * cur.f;
 #pragma unroll
             for (int q4 = 0; q4 < DG / 8; ++q4) {
                 const uint4 x = cur.v[q4];
@@ -824,7 +869,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 float a[16], b[16];
                 tmem_ld16x2(tmem + tlane + TM_D1 + grp * 16, tmem + tlane + TM_D1 + 32 + grp * 16, a, b);
 #pragma unroll
-                for (int r = 0; r < DG; ++r) qcur[r] = eg * (a[r] + b[r]);
+                for (int r = 0; r < DG; ++r) qcur[r] = (eg * cur.f) * (a[r] + b[r]);
             }
             if (c > 0) {
                 if (!mbar_wait(&bar_rx[par ^ 1], rx_parity(c - 1))) ok = false;
@@ -921,18 +966,20 @@ long total_chunks(int n_seqs, const int32_t *cu_host) {
 size_t chunked_workspace_bytes(int n_seqs, const int32_t *cu_host, int hv, int d) {
     if (d != D) return 0;
     const long nch = total_chunks(n_seqs, cu_host);
-    return (size_t)nch * hv * (2 * kPTile + 2 * kRTile);
+    return (size_t)nch * hv * (2 * kPTile + 2 * kRTile + kNormBytes);
 }
 
 cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
     if (p.d != D) return cudaErrorNotSupported;
     const long nch = total_chunks(p.n_seqs, p.cu_seqlens_host);
     if (nch > 0x7fffffffL / (p.hv * D)) return cudaErrorInvalidValue;
-    // workspace: P_hi | P_lo  [nch][hv][D][C]  then R_hi | R_lo  [nch][hv][C][C]  (bf16)
+    // workspace: P_hi | P_lo  [nch][hv][D][C]  then R_hi | R_lo  [nch][hv][C][C]  (bf16), then the q/k
+    // preparation factors [nch][hv][2 C] (fp32: f_k of the chunk's 64 k rows, then f_q of its q rows)
     __nv_bfloat16 *phi = static_cast<__nv_bfloat16 *>(p.workspace);
     __nv_bfloat16 *plo = phi + (size_t)nch * p.hv * D * C;
     __nv_bfloat16 *rhi = plo + (size_t)nch * p.hv * D * C;
     __nv_bfloat16 *rlo = rhi + (size_t)nch * p.hv * C * C;
+    float *norms = reinterpret_cast<float *>(rlo + (size_t)nch * p.hv * C * C);
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -960,13 +1007,15 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
         dim3 grid((unsigned)nch, (unsigned)p.hv);
         chunk_prep_kernel<<<grid, kThreads, PREP_SMEM, p.stream>>>(qmap, kmap, phmap, plmap, rhmap, rlmap,
                                                                    p.log_alpha, p.beta, p.cu_seqlens, p.n_seqs,
-                                                                   p.total_tokens, p.hk, p.hv, p.err);
+                                                                   p.total_tokens, p.hk, p.hv, norms, p.qk_norm,
+                                                                   p.q_scale, p.err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
         const unsigned grid2 = (unsigned)(p.n_seqs * p.hv * (D / DS));
         state_pass_kernel<<<grid2, kPassThreads, PASS_SMEM, p.stream>>>(
-            qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.n_seqs,
+            qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, p.qk_norm ? norms : nullptr, p.q_scale, p.log_alpha, p.beta,
+            p.init_state, p.cu_seqlens, p.n_seqs,
             p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state, p.err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

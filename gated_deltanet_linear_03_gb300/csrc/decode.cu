@@ -12,6 +12,9 @@
 //     u  = beta (v_i - alpha sk)                 (delta)
 //     s' = alpha s + u k                         (new row)
 //     o_i = s'.q = alpha sq + u (k.q)            (output after the update)
+// With query/key preparation (qk_norm, q_scale) k and q stand for f_k k and f_q q, where f_k = 1/|k| and
+// f_q = q_scale/|q| (or 1 and q_scale); the factors are applied to the reduced dot products and to the
+// update coefficient (s' = alpha s + (u f_k) k), never element by element.
 // The section "Reduce intermediate and state traffic" asks for exactly this
 // fusion: the temporaries never leave registers.
 #include "gdn_internal.cuh"
@@ -54,7 +57,8 @@ __global__ void __launch_bounds__(kThreads)
 decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
                    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                    const __nv_bfloat16 *__restrict__ v, const float *__restrict__ log_alpha,
-                   const float *__restrict__ beta, void *__restrict__ out, int out_f32) {
+                   const float *__restrict__ beta, void *__restrict__ out, int out_f32, int qk_norm,
+                   float q_scale) {
     constexpr int LPR = D / 4;                  // lanes per row
     constexpr int GROUPS = 32 / LPR;            // lane groups per warp
     constexpr int WARP_ROWS = GROUPS * kRowsPerGroup;
@@ -83,10 +87,25 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
 #pragma unroll
     for (int i = 0; i < kRowsPerGroup; ++i) s[i] = __ldcs(srow + (size_t)i * (D / 4));
 
-    // k.q over the head (same for every row of the group)
+    // k.q over the head (same for every row of the group), and the preparation factors of k and q
     float kq = kv[0] * qv[0] + kv[1] * qv[1] + kv[2] * qv[2] + kv[3] * qv[3];
+    float fk = 1.f, fq = q_scale;
+    if (qk_norm) {
+        float kk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+        float qq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
 #pragma unroll
-    for (int off = LPR / 2; off >= 1; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        for (int off = LPR / 2; off >= 1; off >>= 1) {
+            kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            kk += __shfl_xor_sync(0xffffffffu, kk, off);
+            qq += __shfl_xor_sync(0xffffffffu, qq, off);
+        }
+        fk = qk_inv_norm(kk, 1);
+        fq = q_scale * qk_inv_norm(qq, 1);
+    } else {
+#pragma unroll
+        for (int off = LPR / 2; off >= 1; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+    }
+    kq *= fk * fq;
 
     const float la = clamp_log_alpha(log_alpha[head]);
     const float alpha = __expf(la);
@@ -113,18 +132,19 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
 #pragma unroll
         for (int j = 0; j < PER; ++j)
             if (my_base + j == i) mine = part[j];
-        const float sk = __shfl_sync(0xffffffffu, mine, src_k);
+        const float sk = fk * __shfl_sync(0xffffffffu, mine, src_k);
         u[i] = b * (__bfloat162float(vrow[i]) - alpha * sk);
     }
 
     // write the updated rows
 #pragma unroll
     for (int i = 0; i < kRowsPerGroup; ++i) {
+        const float uk = u[i] * fk;
         float4 o;
-        o.x = alpha * s[i].x + u[i] * kv[0];
-        o.y = alpha * s[i].y + u[i] * kv[1];
-        o.z = alpha * s[i].z + u[i] * kv[2];
-        o.w = alpha * s[i].w + u[i] * kv[3];
+        o.x = alpha * s[i].x + uk * kv[0];
+        o.y = alpha * s[i].y + uk * kv[1];
+        o.z = alpha * s[i].z + uk * kv[2];
+        o.w = alpha * s[i].w + uk * kv[3];
         __stcs(srow + (size_t)i * (D / 4), o);
     }
 
@@ -136,7 +156,7 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
         const int idx = my_base + j;
         if (idx >= 8 && idx < 16) {
             const int i = idx - 8;
-            const float o = alpha * part[j] + u[i] * kq;
+            const float o = alpha * fq * part[j] + u[i] * kq;
             const size_t oi = (size_t)head * D + row_in_head + i;
             if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
             else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(o);
@@ -163,7 +183,9 @@ struct __align__(16) ShortSmem {
     __nv_bfloat16 v[kShortMaxTokens][short_rows<D>()];
     float alpha[kShortMaxTokens];
     float beta[kShortMaxTokens];
-    float kq[kShortMaxTokens];
+    float kq[kShortMaxTokens];   // prepared k.q
+    float fk[kShortMaxTokens];   // preparation factors of k and q
+    float fq[kShortMaxTokens];
 };
 
 template <int D>
@@ -172,7 +194,8 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
                      const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
                      const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
-                     void *__restrict__ out, int out_f32, float *__restrict__ final_state) {
+                     void *__restrict__ out, int out_f32, float *__restrict__ final_state, int qk_norm,
+                     float q_scale) {
     constexpr int LPR = D / 4, GROUPS = 32 / LPR, ROWS = short_rows<D>(), SLICES = D / ROWS;
     constexpr int NT = short_warps<D>() * 32;
     constexpr int PER = (16 / LPR) > 0 ? (16 / LPR) : 1;
@@ -220,19 +243,34 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
         for (int i = 0; i < kRowsPerGroup; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
-    // k.q of every token, one lane group per token (all warps run the same number of rounds)
+    // k.q and |k|^2, |q|^2 of every token, one lane group per token (all warps run the same number of rounds)
     for (int t0 = 0; t0 < L; t0 += short_warps<D>() * GROUPS) {
         const int t = t0 + warp * GROUPS + group;
-        float x = 0.f;
+        float x = 0.f, kk = 0.f, qq = 0.f;
         if (t < L) {
             const uint2 kr = *reinterpret_cast<const uint2 *>(&sm.k[t][gl * 4]);
             const uint2 qr = *reinterpret_cast<const uint2 *>(&sm.q[t][gl * 4]);
-            x = bf16_lo(kr.x) * bf16_lo(qr.x) + bf16_hi(kr.x) * bf16_hi(qr.x) + bf16_lo(kr.y) * bf16_lo(qr.y) +
-                bf16_hi(kr.y) * bf16_hi(qr.y);
+            const float k4[4] = {bf16_lo(kr.x), bf16_hi(kr.x), bf16_lo(kr.y), bf16_hi(kr.y)};
+            const float q4[4] = {bf16_lo(qr.x), bf16_hi(qr.x), bf16_lo(qr.y), bf16_hi(qr.y)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x = fmaf(k4[e], q4[e], x);
+                kk = fmaf(k4[e], k4[e], kk);
+                qq = fmaf(q4[e], q4[e], qq);
+            }
         }
 #pragma unroll
-        for (int off = LPR / 2; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-        if (gl == 0 && t < L) sm.kq[t] = x;
+        for (int off = LPR / 2; off >= 1; off >>= 1) {
+            x += __shfl_xor_sync(0xffffffffu, x, off);
+            kk += __shfl_xor_sync(0xffffffffu, kk, off);
+            qq += __shfl_xor_sync(0xffffffffu, qq, off);
+        }
+        if (gl == 0 && t < L) {
+            const float fk = qk_inv_norm(kk, qk_norm), fq = q_scale * qk_inv_norm(qq, qk_norm);
+            sm.fk[t] = fk;
+            sm.fq[t] = fq;
+            sm.kq[t] = x * fk * fq;
+        }
     }
     __syncthreads();
 
@@ -244,7 +282,7 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
         const uint2 qr = *reinterpret_cast<const uint2 *>(&sm.q[t][gl * 4]);
         const float kv[4] = {bf16_lo(kr.x), bf16_hi(kr.x), bf16_lo(kr.y), bf16_hi(kr.y)};
         const float qv[4] = {bf16_lo(qr.x), bf16_hi(qr.x), bf16_lo(qr.y), bf16_hi(qr.y)};
-        const float alpha = sm.alpha[t], b = sm.beta[t], kq = sm.kq[t];
+        const float alpha = sm.alpha[t], b = sm.beta[t], kq = sm.kq[t], fk = sm.fk[t], fq = sm.fq[t];
         float part[16];
 #pragma unroll
         for (int i = 0; i < kRowsPerGroup; ++i) {
@@ -260,15 +298,16 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
 #pragma unroll
             for (int j = 0; j < PER; ++j)
                 if (my_base + j == i) mine = part[j];
-            const float sk = __shfl_sync(0xffffffffu, mine, src_k);
+            const float sk = fk * __shfl_sync(0xffffffffu, mine, src_k);
             u[i] = b * (__bfloat162float(sm.v[t][vrow0 + i]) - alpha * sk);
         }
 #pragma unroll
         for (int i = 0; i < kRowsPerGroup; ++i) {
-            s[i].x = alpha * s[i].x + u[i] * kv[0];
-            s[i].y = alpha * s[i].y + u[i] * kv[1];
-            s[i].z = alpha * s[i].z + u[i] * kv[2];
-            s[i].w = alpha * s[i].w + u[i] * kv[3];
+            const float uk = u[i] * fk;
+            s[i].x = alpha * s[i].x + uk * kv[0];
+            s[i].y = alpha * s[i].y + uk * kv[1];
+            s[i].z = alpha * s[i].z + uk * kv[2];
+            s[i].w = alpha * s[i].w + uk * kv[3];
         }
         // the holder lane of sq_i writes o_i (with 32 lanes per row two lanes hold each sum: the even one)
         if (LPR != 32 || (lane & 1) == 0) {
@@ -277,7 +316,7 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
                 const int idx = my_base + j;
                 if (idx >= 8 && idx < 16) {
                     const int i = idx - 8;
-                    const float o = alpha * part[j] + u[i] * kq;
+                    const float o = alpha * fq * part[j] + u[i] * kq;
                     const size_t oi = ((size_t)(tbeg + t) * hv + h) * D + row_in_head + i;
                     if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
                     else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(o);
@@ -296,7 +335,7 @@ cudaError_t launch_short_d(const PrefillProblem &p) {
     const unsigned grid = (unsigned)(p.n_seqs * p.hv * (D / short_rows<D>()));
     short_prefill_kernel<D><<<grid, short_warps<D>() * 32, 0, p.stream>>>(
         p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.out,
-        p.out_f32, p.final_state);
+        p.out_f32, p.final_state, p.qk_norm, p.q_scale);
     return cudaGetLastError();
 }
 
@@ -327,15 +366,15 @@ cudaError_t launch_decode(const DecodeProblem &p) {
     switch (p.d) {
         case 32:
             decode_step_kernel<32><<<grid, kThreads, 0, p.stream>>>((int)total_rows, p.hk, p.hv, p.state, p.q, p.k, p.v,
-                                                                   p.log_alpha, p.beta, p.out, p.out_f32);
+                                                                   p.log_alpha, p.beta, p.out, p.out_f32, p.qk_norm, p.q_scale);
             break;
         case 64:
             decode_step_kernel<64><<<grid, kThreads, 0, p.stream>>>((int)total_rows, p.hk, p.hv, p.state, p.q, p.k, p.v,
-                                                                   p.log_alpha, p.beta, p.out, p.out_f32);
+                                                                   p.log_alpha, p.beta, p.out, p.out_f32, p.qk_norm, p.q_scale);
             break;
         default:
             decode_step_kernel<128><<<grid, kThreads, 0, p.stream>>>((int)total_rows, p.hk, p.hv, p.state, p.q, p.k,
-                                                                    p.v, p.log_alpha, p.beta, p.out, p.out_f32);
+                                                                    p.v, p.log_alpha, p.beta, p.out, p.out_f32, p.qk_norm, p.q_scale);
     }
     return cudaGetLastError();
 }

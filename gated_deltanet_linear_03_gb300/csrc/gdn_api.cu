@@ -2,6 +2,7 @@
 // launch of the matching kernel on the caller's stream.  Validation never
 // touches the CUDA runtime, so argument errors are reported without side
 // effects (and work on machines without a GPU).
+#include <math.h>
 #include <string.h>
 
 #include "gdn_internal.cuh"
@@ -76,7 +77,7 @@ unsigned int *device_error_ptr() {
 
 extern "C" {
 
-int gdn_version(void) { return 100; }
+int gdn_version(void) { return 101; }
 
 const char *gdn_status_string(gdn_status s) {
     switch (s) {
@@ -116,10 +117,11 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
                        const float *log_alpha, const float *beta,
                        const float *init_state,
                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
-                       void *out, int out_dtype, float *final_state,
+                       void *out, int out_dtype, float *final_state, int qk_norm, float q_scale,
                        int algo, void *workspace, size_t workspace_bytes, void *stream, int phases) {
     gdn_status st = check_heads(hk, hv, dk, dv);
     if (st != GDN_OK) return st;
+    if ((qk_norm != 0 && qk_norm != 1) || !isfinite(q_scale)) return GDN_ERR_INVALID_ARG;
     if ((st = check_cu(n_seqs, total_tokens, cu_seqlens_host)) != GDN_OK) return st;
     if (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
     if (algo == GDN_ALGO_AUTO) algo = resolve_auto(n_seqs, hv, dk, cu_seqlens_host);
@@ -169,6 +171,7 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
     p.log_alpha = log_alpha; p.beta = beta; p.init_state = init_state;
     p.cu_seqlens = cu_seqlens; p.cu_seqlens_host = cu_seqlens_host;
     p.out = out; p.out_f32 = out_dtype == GDN_DTYPE_F32; p.final_state = final_state;
+    p.qk_norm = qk_norm; p.q_scale = q_scale;
     p.workspace = workspace; p.workspace_bytes = workspace_bytes;
     p.err = device_error_ptr();
     p.stream = static_cast<cudaStream_t>(stream);
@@ -198,10 +201,11 @@ gdn_status gdn_prefill(int n_seqs, int total_tokens, int hk, int hv, int dk, int
                        const float *log_alpha, const float *beta,
                        const float *init_state,
                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
-                       void *out, int out_dtype, float *final_state,
+                       void *out, int out_dtype, float *final_state, int qk_norm, float q_scale,
                        int algo, void *workspace, size_t workspace_bytes, void *stream) {
     return prefill_impl(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
-                        cu_seqlens_host, out, out_dtype, final_state, algo, workspace, workspace_bytes, stream, 3);
+                        cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, algo, workspace,
+                        workspace_bytes, stream, 3);
 }
 
 gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
@@ -209,21 +213,22 @@ gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_tokens, in
                                      const float *log_alpha, const float *beta,
                                      const float *init_state,
                                      const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
-                                     void *out, int out_dtype, float *final_state,
+                                     void *out, int out_dtype, float *final_state, int qk_norm, float q_scale,
                                      void *workspace, size_t workspace_bytes, void *stream) {
     if (phase != GDN_PHASE_PREP && phase != GDN_PHASE_PASS) return GDN_ERR_INVALID_ARG;
     return prefill_impl(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
-                        cu_seqlens_host, out, out_dtype, final_state, GDN_ALGO_CHUNKED, workspace, workspace_bytes,
-                        stream, phase == GDN_PHASE_PREP ? 1 : 2);
+                        cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, GDN_ALGO_CHUNKED, workspace,
+                        workspace_bytes, stream, phase == GDN_PHASE_PREP ? 1 : 2);
 }
 
 gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
                            const void *q, const void *k, const void *v,
                            const float *log_alpha, const float *beta,
-                           void *out, int out_dtype, void *stream) {
+                           void *out, int out_dtype, int qk_norm, float q_scale, void *stream) {
     gdn_status st = check_heads(hk, hv, dk, dv);
     if (st != GDN_OK) return st;
     if (n < 0) return GDN_ERR_INVALID_ARG;
+    if ((qk_norm != 0 && qk_norm != 1) || !isfinite(q_scale)) return GDN_ERR_INVALID_ARG;
     if (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
     if (n == 0) return GDN_OK;
     if (!state || !q || !k || !v || !log_alpha || !beta || !out) return GDN_ERR_INVALID_ARG;
@@ -247,6 +252,7 @@ gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
     p.k = static_cast<const __nv_bfloat16 *>(k);
     p.v = static_cast<const __nv_bfloat16 *>(v);
     p.log_alpha = log_alpha; p.beta = beta; p.out = out; p.out_f32 = out_dtype == GDN_DTYPE_F32;
+    p.qk_norm = qk_norm; p.q_scale = q_scale;
     p.err = nullptr;
     p.stream = static_cast<cudaStream_t>(stream);
     return gdn::launch_decode(p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

@@ -18,6 +18,12 @@ constexpr int kChunkedHeadDim = 128;
 
 __device__ __forceinline__ float clamp_log_alpha(float la) { return fmaxf(la, kLogAlphaFloor); }
 
+// Query/key preparation: with qk_norm a head vector x is used as x / sqrt(|x|^2 + kQkNormEps).
+constexpr float kQkNormEps = 1e-6f;
+__device__ __forceinline__ float qk_inv_norm(float sum_sq, int qk_norm) {
+    return qk_norm ? rsqrtf(sum_sq + kQkNormEps) : 1.f;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xffff0000u); }
 
@@ -38,6 +44,8 @@ struct PrefillProblem {
     void *out;
     int out_f32;
     float *final_state;
+    int qk_norm;        // L2-normalise q and k head vectors (x / sqrt(|x|^2 + kQkNormEps))
+    float q_scale;      // then multiply q by this
     void *workspace;
     size_t workspace_bytes;
     unsigned int *err;
@@ -51,6 +59,8 @@ struct DecodeProblem {
     const float *log_alpha, *beta;
     void *out;
     int out_f32;
+    int qk_norm;
+    float q_scale;
     unsigned int *err;
     cudaStream_t stream;
 };

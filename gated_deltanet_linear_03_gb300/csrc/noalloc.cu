@@ -28,9 +28,9 @@
 
 namespace {
 
-// 96 MiB = 2048 (chunk, value head) pairs of 48 KiB: one 4096-token prompt at
+// 97 MiB = 2048 (chunk, value head) pairs of 48.5 KiB: one 4096-token prompt at
 // 32 value heads, or 8192 tokens at 16.
-constexpr size_t kNoAllocScratchBytes = size_t(96) << 20;
+constexpr size_t kNoAllocScratchBytes = size_t(97) << 20;
 static_assert(kNoAllocScratchBytes == (size_t)GDN_NOALLOC_SCRATCH_BYTES, "header and library disagree");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -56,7 +56,8 @@ extern "C" gdn_status gdn_prefill_noalloc(int n_seqs, int total_tokens, int hk, 
                                           const float *log_alpha, const float *beta,
                                           const float *init_state,
                                           const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
-                                          void *out, int out_dtype, float *final_state, void *stream) {
+                                          void *out, int out_dtype, float *final_state, int qk_norm,
+                                          float q_scale, void *stream) {
     gdn_status st = GDN_OK;
     const size_t need = gdn_prefill_workspace_size(n_seqs, total_tokens, hk, hv, dk, dv, cu_seqlens_host,
                                                    GDN_ALGO_CHUNKED, &st);
@@ -65,6 +66,6 @@ extern "C" gdn_status gdn_prefill_noalloc(int n_seqs, int total_tokens, int hk, 
     void *scratch = scratch_device_address();
     if (scratch == nullptr) return GDN_ERR_CUDA;
     return gdn_prefill(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
-                       cu_seqlens_host, out, out_dtype, final_state, GDN_ALGO_CHUNKED, scratch,
+                       cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, GDN_ALGO_CHUNKED, scratch,
                        kNoAllocScratchBytes, stream);
 }

@@ -29,14 +29,18 @@ constexpr int kRows = 16;   // value rows per CTA
 constexpr int kTPR = kThreads / kRows;   // threads per row
 constexpr int kTB = 64;     // tokens per staged block
 
-template <int D>
+// PREP adds the per-token query/key preparation factors (kept out of the plain layout: it is sized to fit
+// three CTAs per SM).
+template <int D, bool PREP>
 struct ScanSmem {
     __nv_bfloat16 k[2][kTB][D];
     __nv_bfloat16 q[2][kTB][D];
     __nv_bfloat16 v[2][kTB][kRows];
     float la[2][kTB];
     float b[2][kTB];
-    float kq[kTB];
+    float kq[kTB];              // prepared k.q of each token of the block
+    float fk[PREP ? kTB : 1];   // query/key preparation factors (1/|k| or 1, q_scale/|q| or q_scale)
+    float fq[PREP ? kTB : 1];
     float o[kTB][kRows];
 };
 
@@ -52,8 +56,8 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
-template <int D>
-__device__ __forceinline__ void stage_block(ScanSmem<D> &sm, int buf, long t0, int nt, int hk, int hv,
+template <int D, bool PREP>
+__device__ __forceinline__ void stage_block(ScanSmem<D, PREP> &sm, int buf, long t0, int nt, int hk, int hv,
                                             int hq, int h, int row0, const __nv_bfloat16 *__restrict__ q,
                                             const __nv_bfloat16 *__restrict__ k,
                                             const __nv_bfloat16 *__restrict__ v,
@@ -77,17 +81,19 @@ __device__ __forceinline__ void stage_block(ScanSmem<D> &sm, int buf, long t0, i
     }
 }
 
-template <int D>
+// PREP: query/key preparation enabled (qk_norm, or q_scale != 1); without it the token loop is the plain one.
+template <int D, bool PREP>
 __global__ void __launch_bounds__(kThreads)
 scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__restrict__ q,
                     const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
                     const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
-                    void *__restrict__ out, int out_f32, float *__restrict__ final_state) {
+                    void *__restrict__ out, int out_f32, float *__restrict__ final_state, int qk_norm,
+                    float q_scale) {
     constexpr int COLS = D / kTPR;        // state columns per thread
     constexpr int SLICES = D / kRows;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    ScanSmem<D> &sm = *reinterpret_cast<ScanSmem<D> *>(smem_raw);
+    ScanSmem<D, PREP> &sm = *reinterpret_cast<ScanSmem<D, PREP> *>(smem_raw);
 
     const int slice = blockIdx.x % SLICES;
     const int h = (blockIdx.x / SLICES) % hv;
@@ -116,7 +122,7 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
     const long ntok = tend - tbeg;
     const int nblk = (int)((ntok + kTB - 1) / kTB);
     if (nblk > 0) {
-        stage_block<D>(sm, 0, tbeg, (int)min((long)kTB, ntok), hk, hv, hq, h, row0, q, k, v, log_alpha, beta);
+        stage_block<D, PREP>(sm, 0, tbeg, (int)min((long)kTB, ntok), hk, hv, hq, h, row0, q, k, v, log_alpha, beta);
         cp_async_commit();
     }
     for (int blk = 0; blk < nblk; ++blk) {
@@ -125,26 +131,44 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
         const int nt = (int)min((long)kTB, tend - t0);
         if (blk + 1 < nblk) {
             const long t1 = t0 + kTB;
-            stage_block<D>(sm, buf ^ 1, t1, (int)min((long)kTB, tend - t1), hk, hv, hq, h, row0, q, k, v,
+            stage_block<D, PREP>(sm, buf ^ 1, t1, (int)min((long)kTB, tend - t1), hk, hv, hq, h, row0, q, k, v,
                            log_alpha, beta);
         }
         cp_async_commit();
         cp_async_wait_prev();
         __syncthreads();
-        // k.q of every token of the block, once: 16 lanes per token, 8 tokens per round.  Every warp runs
-        // the same number of rounds (the shuffles need all 32 lanes); tokens past nt compute nothing.
+        // k.q (and |k|^2, |q|^2) of every token of the block, once: 16 lanes per token, 8 tokens per round.
+        // Every warp runs the same number of rounds (the shuffles need all 32 lanes); tokens past nt compute
+        // nothing.
         for (int t0k = 0; t0k < nt; t0k += kThreads / 16) {
             const int t = t0k + (threadIdx.x >> 4), l = threadIdx.x & 15;
-            float acc = 0.f;
+            float acc = 0.f, kk = 0.f, qq = 0.f;
             if (t < nt) {
 #pragma unroll
-                for (int j = 0; j < D / 16; ++j)
-                    acc = fmaf(__bfloat162float(sm.k[buf][t][l + 16 * j]), __bfloat162float(sm.q[buf][t][l + 16 * j]),
-                               acc);
+                for (int j = 0; j < D / 16; ++j) {
+                    const float kx = __bfloat162float(sm.k[buf][t][l + 16 * j]);
+                    const float qx = __bfloat162float(sm.q[buf][t][l + 16 * j]);
+                    acc = fmaf(kx, qx, acc);
+                    kk = fmaf(kx, kx, kk);
+                    qq = fmaf(qx, qx, qq);
+                }
             }
 #pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (l == 0 && t < nt) sm.kq[t] = acc;
+            for (int off = 8; off >= 1; off >>= 1) {
+                acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                kk += __shfl_xor_sync(0xffffffffu, kk, off);
+                qq += __shfl_xor_sync(0xffffffffu, qq, off);
+            }
+            if (l == 0 && t < nt) {
+                if (PREP) {
+                    const float fk = qk_inv_norm(kk, qk_norm), fq = q_scale * qk_inv_norm(qq, qk_norm);
+                    sm.fk[t] = fk;
+                    sm.fq[t] = fq;
+                    sm.kq[t] = acc * fk * fq;
+                } else {
+                    sm.kq[t] = acc;
+                }
+            }
         }
         __syncthreads();
 
@@ -174,13 +198,15 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
                 a0 += __shfl_xor_sync(0xffffffffu, a0, off);
                 a1 += __shfl_xor_sync(0xffffffffu, a1, off);
             }
-            const float a2 = sm.kq[t];
+            // prepared k and q are fk k and fq q: scale the reduced dots and the update coefficient
+            const float a2 = sm.kq[t], fk = PREP ? sm.fk[t] : 1.f, fq = PREP ? sm.fq[t] : 1.f;
             const float alpha = expf(clamp_log_alpha(sm.la[buf][t]));
             const float bt = sm.b[buf][t];
-            const float u = bt * (__bfloat162float(sm.v[buf][t][r]) - alpha * a0);
+            const float u = bt * (__bfloat162float(sm.v[buf][t][r]) - alpha * (fk * a0));
+            const float uk = u * fk;
 #pragma unroll
-            for (int j = 0; j < COLS; ++j) S[j] = fmaf(alpha, S[j], u * kk[j]);
-            if (c == 0) sm.o[t][r] = fmaf(alpha, a1, u * a2);
+            for (int j = 0; j < COLS; ++j) S[j] = fmaf(alpha, S[j], uk * kk[j]);
+            if (c == 0) sm.o[t][r] = fmaf(alpha, fq * a1, u * a2);
         }
         __syncthreads();
         // write this block's outputs: row-contiguous 32-value pieces
@@ -201,23 +227,29 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
     }
 }
 
-template <int D>
-cudaError_t launch_scan_d(const PrefillProblem &p) {
-    const size_t smem = sizeof(ScanSmem<D>);
+template <int D, bool PREP>
+cudaError_t launch_scan_dp(const PrefillProblem &p) {
+    const size_t smem = sizeof(ScanSmem<D, PREP>);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static bool attr_set[128] = {};
     if (dev < 128 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(scan_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(scan_prefill_kernel<D, PREP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     const unsigned grid = (unsigned)(p.n_seqs * p.hv * (D / kRows));
-    scan_prefill_kernel<D><<<grid, kThreads, smem, p.stream>>>(
+    scan_prefill_kernel<D, PREP><<<grid, kThreads, smem, p.stream>>>(
         p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.out,
-        p.out_f32, p.final_state);
+        p.out_f32, p.final_state, p.qk_norm, p.q_scale);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_scan_d(const PrefillProblem &p) {
+    return (p.qk_norm || p.q_scale != 1.f) ? launch_scan_dp<D, true>(p) : launch_scan_dp<D, false>(p);
 }
 
 }  // namespace

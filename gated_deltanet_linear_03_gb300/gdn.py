@@ -24,7 +24,7 @@ DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 # every symbol include/gdn.h declares
 EXPORTS = ("gdn_prefill", "gdn_prefill_chunked_phase", "gdn_prefill_workspace_size", "gdn_decode_step",
            "gdn_device_error", "gdn_status_string", "gdn_version", "gdn_prefill_noalloc", "gdn_prefill_algo")
-NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024
+NOALLOC_SCRATCH_BYTES = 97 * 1024 * 1024
 PHASE = {"prep": 1, "pass": 2}
 
 
@@ -47,17 +47,18 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                            "`python -c 'import __graft_entry__ as g; g.build()'`")
     lib = ctypes.CDLL(path)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-    lib.gdn_prefill.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, P, Z, P]
+    F = ctypes.c_float
+    lib.gdn_prefill.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, I, P, Z, P]
     lib.gdn_prefill.restype = I
-    lib.gdn_prefill_chunked_phase.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, P, Z, P]
+    lib.gdn_prefill_chunked_phase.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, Z, P]
     lib.gdn_prefill_chunked_phase.restype = I
-    lib.gdn_prefill_noalloc.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, P]
+    lib.gdn_prefill_noalloc.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P]
     lib.gdn_prefill_noalloc.restype = I
     lib.gdn_prefill_workspace_size.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
     lib.gdn_prefill_workspace_size.restype = Z
     lib.gdn_prefill_algo.argtypes = [I, I, I, I, I, I, P]
     lib.gdn_prefill_algo.restype = I
-    lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, P]
+    lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, I, ctypes.c_float, P]
     lib.gdn_decode_step.restype = I
     lib.gdn_device_error.argtypes = [P]
     lib.gdn_device_error.restype = I
@@ -128,8 +129,12 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
             beta: torch.Tensor, cu_seqlens: torch.Tensor, *, init_state: Optional[torch.Tensor] = None,
             out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
             final_state=True, algo: str = "chunked", workspace: Optional[torch.Tensor] = None,
-            cu_seqlens_host: Optional[Sequence[int]] = None, stream=None):
+            cu_seqlens_host: Optional[Sequence[int]] = None, stream=None, qk_norm: bool = False,
+            q_scale: float = 1.0):
     """Run ``gdn_prefill``.  Returns ``(out, final_state)``.
+
+    ``qk_norm`` / ``q_scale``: the in-kernel query/key preparation (every q and k head vector
+    L2-normalised, then q multiplied by ``q_scale``); the defaults use q and k as given.
 
     ``final_state`` may be ``True`` (allocate), ``False``/``None`` (do not emit)
     or a tensor to write into (it may be ``init_state`` for an in-place update).
@@ -163,7 +168,8 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib.gdn_prefill(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                          _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out), DTYPE[out.dtype],
-                         _ptr(final_state), ALGO[algo], _ptr(workspace), ws_bytes, _stream_ptr(stream))
+                         _ptr(final_state), int(bool(qk_norm)), float(q_scale), ALGO[algo], _ptr(workspace),
+                         ws_bytes, _stream_ptr(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill")
     return out, final_state
@@ -172,7 +178,8 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
 def prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor,
                     beta: torch.Tensor, cu_seqlens: torch.Tensor, *, init_state: Optional[torch.Tensor] = None,
                     out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16, final_state=True,
-                    cu_seqlens_host: Optional[Sequence[int]] = None, stream=None):
+                    cu_seqlens_host: Optional[Sequence[int]] = None, stream=None, qk_norm: bool = False,
+                    q_scale: float = 1.0):
     """Run ``gdn_prefill_noalloc``: the chunked prefill using the library's fixed
     scratch instead of a workspace (for callers that cannot allocate device
     memory; see include/gdn.h for its size limit and sharing rules).
@@ -199,7 +206,7 @@ def prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha
     cu_arr, _ = _host_cu(cu_seqlens, cu_seqlens_host)
     st = lib.gdn_prefill_noalloc(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                                  _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out), DTYPE[out.dtype],
-                                 _ptr(final_state), _stream_ptr(stream))
+                                 _ptr(final_state), int(bool(qk_norm)), float(q_scale), _stream_ptr(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill_noalloc")
     return out, final_state
@@ -212,7 +219,7 @@ class PrefillPlan:
 
     def __init__(self, q, k, v, log_alpha, beta, cu_seqlens, *, init_state=None, out=None,
                  out_dtype=torch.bfloat16, final_state=True, algo="chunked", workspace=None,
-                 cu_seqlens_host=None):
+                 cu_seqlens_host=None, qk_norm=False, q_scale=1.0):
         self.lib = load_library()
         _need(q, "q", torch.bfloat16, 3)
         _need(k, "k", torch.bfloat16, 3)
@@ -241,22 +248,24 @@ class PrefillPlan:
         self.ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
                      self.cu_arr, _ptr(out), DTYPE[out.dtype], _ptr(final_state))
         self.ws = (_ptr(workspace), ws_bytes)
+        self.qk = (int(bool(qk_norm)), float(q_scale))
 
     def run(self, stream=None):
-        st = self.lib.gdn_prefill(*self.head, *self.ptrs, self.algo, *self.ws, _stream_ptr(stream))
+        st = self.lib.gdn_prefill(*self.head, *self.ptrs, *self.qk, self.algo, *self.ws, _stream_ptr(stream))
         if st != GDN_OK:
             raise GdnError(st, "gdn_prefill")
         return self.out, self.final_state
 
     def run_phase(self, phase: str, stream=None):
-        st = self.lib.gdn_prefill_chunked_phase(PHASE[phase], *self.head, *self.ptrs, *self.ws, _stream_ptr(stream))
+        st = self.lib.gdn_prefill_chunked_phase(PHASE[phase], *self.head, *self.ptrs, *self.qk, *self.ws,
+                                                _stream_ptr(stream))
         if st != GDN_OK:
             raise GdnError(st, "gdn_prefill_chunked_phase")
 
 
 def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                 log_alpha: torch.Tensor, beta: torch.Tensor, *, out: Optional[torch.Tensor] = None,
-                out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+                out_dtype=torch.bfloat16, stream=None, qk_norm: bool = False, q_scale: float = 1.0) -> torch.Tensor:
     """Run ``gdn_decode_step`` (state updated in place).  Returns ``out``."""
     lib = load_library()
     _need(state, "state", torch.float32, 4)
@@ -270,7 +279,8 @@ def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.
     if out is None:
         out = torch.empty(n, hv, dv, device=q.device, dtype=out_dtype)
     st = lib.gdn_decode_step(n, hk, hv, dk, dv, _ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
-                             _ptr(beta), _ptr(out), DTYPE[out.dtype], _stream_ptr(stream))
+                             _ptr(beta), _ptr(out), DTYPE[out.dtype], int(bool(qk_norm)), float(q_scale),
+                             _stream_ptr(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_decode_step")
     return out

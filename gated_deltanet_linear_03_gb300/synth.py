@@ -72,22 +72,30 @@ def _gates(shape, gen, kind: str):
     raise ValueError(kind)
 
 
-def qkv(T: int, hk: int, hv: int, dk: int, dv: int, gen, *, scale_q: bool = True):
-    q = _unit(torch.randn(T, hk, dk, generator=gen))
+def qkv(T: int, hk: int, hv: int, dk: int, dv: int, gen, *, scale_q: bool = True, raw_qk: bool = False):
+    """q, k unit vectors (q scaled by 1/sqrt(dk) when ``scale_q``), v ~ N(0, 1).  With ``raw_qk`` q and k are
+    raw projections instead: N(0, 1) entries times a per-vector length drawn from [0.25, 4], for the
+    in-kernel query/key preparation to normalise."""
+    q = torch.randn(T, hk, dk, generator=gen)
+    k = torch.randn(T, hk, dk, generator=gen)
+    v = torch.randn(T, hv, dv, generator=gen)
+    if raw_qk:
+        q = q * (0.25 + 3.75 * torch.rand(T, hk, 1, generator=gen))
+        k = k * (0.25 + 3.75 * torch.rand(T, hk, 1, generator=gen))
+        return q, k, v
+    q, k = _unit(q), _unit(k)
     if scale_q:
         q = q / math.sqrt(dk)
-    k = _unit(torch.randn(T, hk, dk, generator=gen))
-    v = torch.randn(T, hv, dv, generator=gen)
     return q, k, v
 
 
 def prefill_inputs(lengths: Sequence[int], *, hk=16, hv=32, dk=128, dv=128, seed=1001,
                    gates="model", init_std: float = 0.0, scale_q: bool = True,
-                   qkv_dtype=torch.bfloat16) -> PrefillInputs:
+                   qkv_dtype=torch.bfloat16, raw_qk: bool = False) -> PrefillInputs:
     """Packed prefill inputs for sequences of the given lengths."""
     gen = torch.Generator().manual_seed(seed)
     T = int(sum(lengths))
-    q, k, v = qkv(T, hk, hv, dk, dv, gen, scale_q=scale_q)
+    q, k, v = qkv(T, hk, hv, dk, dv, gen, scale_q=scale_q, raw_qk=raw_qk)
     la, b = _gates((T, hv), gen, gates)
     cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(list(lengths), dtype=torch.int64), 0).to(torch.int32)
@@ -106,11 +114,11 @@ def log_uniform_lengths(n: int, lo: int, hi: int, seed: int) -> list:
 
 
 def decode_inputs(n: int, steps: int, *, hk=16, hv=32, dk=128, dv=128, seed=1002,
-                  state_std: float = 0.02, gates="model") -> DecodeInputs:
+                  state_std: float = 0.02, gates="model", raw_qk: bool = False) -> DecodeInputs:
     """``n`` independent states (one per layer) and ``steps`` tokens of fresh inputs."""
     gen = torch.Generator().manual_seed(seed)
     state = torch.randn(n, hv, dv, dk, generator=gen) * state_std
-    q, k, v = qkv(steps * n, hk, hv, dk, dv, gen)
+    q, k, v = qkv(steps * n, hk, hv, dk, dv, gen, raw_qk=raw_qk)
     la, b = _gates((steps * n, hv), gen, gates)
     bf = torch.bfloat16
     return DecodeInputs(state.contiguous(),

@@ -102,6 +102,14 @@ typedef enum {
  *   final_state      fp32 [n_seqs, hv, dv, dk] or NULL.  It may be the same
  *                    buffer as init_state (updated in place); any other overlap
  *                    with an input is an error.
+ *   qk_norm, q_scale query/key preparation inside the kernels ("Optimizing
+ *                    on-device inference for Apple Silicon", section "Reduce
+ *                    intermediate and state traffic": the decode path fuses
+ *                    query and key preparation).  With qk_norm = 1 every q and
+ *                    k head vector x is used as x / sqrt(|x|^2 + 1e-6); in all
+ *                    cases q is then multiplied by q_scale (a finite float;
+ *                    1/sqrt(dk) for raw projections).  qk_norm = 0, q_scale = 1
+ *                    uses q and k exactly as given.
  *   algo             GDN_ALGO_CHUNKED, GDN_ALGO_SCAN or GDN_ALGO_AUTO
  *   workspace        device scratch of at least gdn_prefill_workspace_size()
  *                    bytes (may be NULL when that size is 0), 256-byte aligned.
@@ -114,6 +122,7 @@ GDN_API gdn_status gdn_prefill(int n_seqs, int total_tokens, int hk, int hv, int
                        const float *init_state,
                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                        void *out, int out_dtype, float *final_state,
+                       int qk_norm, float q_scale,
                        int algo, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -139,6 +148,7 @@ GDN_API gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_to
                                              const float *init_state,
                                              const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                                              void *out, int out_dtype, float *final_state,
+                                             int qk_norm, float q_scale,
                                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -178,11 +188,12 @@ GDN_API int gdn_prefill_algo(int n_seqs, int total_tokens, int hk, int hv, int d
  *   v                bf16 [n, hv, dv]
  *   log_alpha, beta  fp32 [n, hv]
  *   out              [n, hv, dv], dtype out_dtype; must not overlap state
+ *   qk_norm, q_scale as for gdn_prefill
  */
 GDN_API gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
                            const void *q, const void *k, const void *v,
                            const float *log_alpha, const float *beta,
-                           void *out, int out_dtype, void *stream);
+                           void *out, int out_dtype, int qk_norm, float q_scale, void *stream);
 
 /*
  * Synchronise `stream` and return (and clear) the device-side error word the
@@ -201,7 +212,7 @@ GDN_API gdn_status gdn_device_error(void *stream);
  *
  * Arguments, layouts and errors as for gdn_prefill, without algo and
  * workspace.  The scratch is one library-owned device array of
- * GDN_NOALLOC_SCRATCH_BYTES (96 MiB), held on every GPU that loads the library
+ * GDN_NOALLOC_SCRATCH_BYTES (97 MiB), held on every GPU that loads the library
  * until the process exits:
  *   - problems that need more scratch than that (gdn_prefill_workspace_size
  *     with GDN_ALGO_CHUNKED above GDN_NOALLOC_SCRATCH_BYTES; e.g. more than
@@ -214,14 +225,15 @@ GDN_API gdn_status gdn_device_error(void *stream);
  *     threads) race on it and must be serialised by the caller;
  *   - it calls no cudaMalloc, cudaFree or other allocating routine.
  */
-#define GDN_NOALLOC_SCRATCH_BYTES (96ull * 1024ull * 1024ull)
+#define GDN_NOALLOC_SCRATCH_BYTES (97ull * 1024ull * 1024ull)
 
 GDN_API gdn_status gdn_prefill_noalloc(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
                                        const void *q, const void *k, const void *v,
                                        const float *log_alpha, const float *beta,
                                        const float *init_state,
                                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
-                                       void *out, int out_dtype, float *final_state, void *stream);
+                                       void *out, int out_dtype, float *final_state,
+                                       int qk_norm, float q_scale, void *stream);
 
 /* Static, human-readable name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status status);

@@ -49,12 +49,12 @@ FAKE = 0x10000  # an aligned address that is never dereferenced: validation fail
 def prefill(lib, **kw):
     a = dict(n_seqs=1, T=64, hk=1, hv=2, dk=128, dv=128, q=FAKE, k=FAKE * 2, v=FAKE * 3, la=FAKE * 4,
              b=FAKE * 5, s0=None, cu=FAKE * 6, cu_host=_cu([0, 64]), out=FAKE * 7, odt=0, fin=None,
-             algo=1, ws=None, wsb=0)
+             algo=1, ws=None, wsb=0, qkn=0, qs=1.0)
     a.update(kw)
     P = ctypes.c_void_p
     return lib.gdn_prefill(a["n_seqs"], a["T"], a["hk"], a["hv"], a["dk"], a["dv"], P(a["q"]), P(a["k"]),
                            P(a["v"]), P(a["la"]), P(a["b"]), P(a["s0"]), P(a["cu"]), a["cu_host"], P(a["out"]),
-                           a["odt"], P(a["fin"]), a["algo"], P(a["ws"]), a["wsb"], None)
+                           a["odt"], P(a["fin"]), a["qkn"], a["qs"], a["algo"], P(a["ws"]), a["wsb"], None)
 
 
 def test_prefill_rejects_bad_heads(lib):
@@ -76,6 +76,9 @@ def test_prefill_rejects_bad_cu_seqlens(lib):
 
 def test_prefill_rejects_bad_dtype_algo_pointers(lib):
     assert prefill(lib, odt=7) == 2
+    assert prefill(lib, qkn=2) == 1                 # qk_norm is 0 or 1
+    assert prefill(lib, qkn=1, qs=float("inf")) == 1
+    assert prefill(lib, qs=float("nan")) == 1
     assert prefill(lib, algo=5) == 2
     assert prefill(lib, q=None) == 1
     assert prefill(lib, q=FAKE + 4) == 3          # misaligned
@@ -109,8 +112,9 @@ def test_decode_rejects_bad_args(lib):
     P = ctypes.c_void_p
 
     def dec(n=1, hk=1, hv=2, d=128, state=FAKE, q=FAKE * 2, k=FAKE * 3, v=FAKE * 4, la=FAKE * 5, b=FAKE * 6,
-            out=FAKE * 7, odt=0):
-        return lib.gdn_decode_step(n, hk, hv, d, d, P(state), P(q), P(k), P(v), P(la), P(b), P(out), odt, None)
+            out=FAKE * 7, odt=0, qkn=0, qs=1.0):
+        return lib.gdn_decode_step(n, hk, hv, d, d, P(state), P(q), P(k), P(v), P(la), P(b), P(out), odt, qkn, qs,
+                                   None)
 
     assert dec(hk=3, hv=4) == 1
     assert dec(d=96) == 2
@@ -120,6 +124,8 @@ def test_decode_rejects_bad_args(lib):
     assert dec(q=FAKE + 8) == 3
     assert dec(odt=3) == 2
     assert dec(out=FAKE) == 1                # out overlaps state
+    assert dec(qkn=-1) == 1
+    assert dec(qs=float("inf")) == 1
 
 
 def test_auto_algo_rule(lib):

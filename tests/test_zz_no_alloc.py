@@ -49,7 +49,7 @@ def test_noalloc_matches_workspace_entry_point_twice(gdn):
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(gdn):
-    """Needs more than 96 MiB of scratch: refused on the host before any GPU work."""
+    """Needs more than 97 MiB of scratch: refused on the host before any GPU work."""
     lib = gdn.load_library()
     T = 4096 + 64
     cu = (ctypes.c_int32 * 2)(0, T)
@@ -58,5 +58,5 @@ def test_noalloc_rejects_problems_beyond_the_scratch(gdn):
     assert st.value == 0 and need > gdn.NOALLOC_SCRATCH_BYTES
     fake = ctypes.c_void_p(0x10000)
     r = lib.gdn_prefill_noalloc(1, T, 16, 32, 128, 128, fake, fake, fake, fake, fake, None, fake, cu, fake, 0,
-                                None, None)
+                                None, 0, 1.0, None)
     assert r == 7   # GDN_ERR_WORKSPACE
