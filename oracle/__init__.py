@@ -87,12 +87,23 @@ def _shapes(q, k, v):
     return T, hk, dk, hv, dv
 
 
+def rms_norm(out, weight, eps):
+    """Output normalisation (fp64): every head's output vector o (the last axis) becomes
+    o / sqrt(mean(o^2) + eps) * weight.  The pages' decode path fuses "the recurrent update with its
+    normalisation" ("Optimizing on-device inference for Apple Silicon", section "Reduce intermediate and
+    state traffic"); they give neither the norm nor its weights, and this root-mean-square norm over the
+    value dimension with a per-channel weight is our reading."""
+    o = np.asarray(out, dtype=np.float64)
+    w = np.asarray(weight, dtype=np.float64)
+    return o / np.sqrt((o * o).mean(axis=-1, keepdims=True) + float(eps)) * w
+
+
 def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, n_threads=None,
-            want_out=True, qk_norm=False, q_scale=1.0):
+            want_out=True, qk_norm=False, q_scale=1.0, norm_weight=None, norm_eps=1e-6):
     """Sequential fp64 scan.  Returns (out [T,hv,dv] fp64 or None, final_state [N,hv,dv,dk] fp64).
 
     ``qk_norm``: L2-normalise every q and k head vector first (x / sqrt(|x|^2 + 1e-6)); q is then
-    multiplied by ``q_scale``."""
+    multiplied by ``q_scale``.  ``norm_weight`` ([dv]): apply :func:`rms_norm` to the outputs."""
     q, k, v = _f32(q), _f32(k), _f32(v)
     la, b = _f32(log_alpha), _f32(beta)
     T, hk, dk, hv, dv = _shapes(q, k, v)
@@ -108,6 +119,8 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, n_threads=
                                     int(bool(qk_norm)), float(q_scale), int(n_threads or max_threads()))
     if rc:
         raise RuntimeError(f"gdn_oracle_prefill failed: {rc}")
+    if norm_weight is not None and out is not None:
+        out = rms_norm(out, norm_weight, norm_eps)
     return out, fin
 
 
@@ -131,7 +144,8 @@ def prefill_chunked(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, ch
     return out, fin
 
 
-def decode_step(state, q, k, v, log_alpha, beta, *, n_threads=None, qk_norm=False, q_scale=1.0):
+def decode_step(state, q, k, v, log_alpha, beta, *, n_threads=None, qk_norm=False, q_scale=1.0,
+                norm_weight=None, norm_eps=1e-6):
     """One token per state.  state [n,hv,dv,dk]; q,k [n,hk,dk]; v [n,hv,dv]; gates [n,hv].
 
     Returns (out [n,hv,dv] fp64, new_state fp64); the input array is not modified.
@@ -148,6 +162,8 @@ def decode_step(state, q, k, v, log_alpha, beta, *, n_threads=None, qk_norm=Fals
                                         int(n_threads or max_threads()))
     if rc:
         raise RuntimeError(f"gdn_oracle_decode_step failed: {rc}")
+    if norm_weight is not None:
+        out = rms_norm(out, norm_weight, norm_eps)
     return out, st
 
 

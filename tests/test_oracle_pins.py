@@ -322,6 +322,45 @@ def test_chunked_with_qk_norm_equals_sequential():
     np.testing.assert_allclose(f2, f1, rtol=1e-9, atol=1e-10)
 
 
+# ---------------------------------------------------------------- output normalisation
+
+def test_output_norm_by_hand():
+    """o = (3, 4): mean of squares 12.5; with eps 0.5 the divisor is sqrt(13) = 3.6055..."""
+    o = np.array([[3.0, 4.0]])
+    got = oracle.rms_norm(o, np.array([2.0, -1.0]), 0.5)
+    np.testing.assert_allclose(got, [[6.0 / math.sqrt(13.0), -4.0 / math.sqrt(13.0)]], rtol=1e-15)
+
+
+def test_output_norm_properties():
+    """With unit weight the normalised output has mean square ms/(ms + eps); scaling v (so o) by c > 0
+    leaves it unchanged up to eps; the state never depends on the norm."""
+    rng = np.random.default_rng(44)
+    T = 6
+    q, k, v, la, b, s0 = rand_case(rng, T, hk=1, hv=2, dk=4, dv=5)
+    s0 = None
+    raw, f0 = oracle.prefill(q, k, v, la, b, one_seq(T), s0)
+    o1, f1 = oracle.prefill(q, k, v, la, b, one_seq(T), s0, norm_weight=np.ones(5), norm_eps=1e-9)
+    ms = (raw ** 2).mean(axis=-1)
+    np.testing.assert_allclose((o1 ** 2).mean(axis=-1), ms / (ms + 1e-9), rtol=1e-12)
+    np.testing.assert_array_equal(f1, f0)
+    o2, _ = oracle.prefill(q, k, (v * 3.0).astype(np.float32), la, b, one_seq(T), s0, norm_weight=np.ones(5),
+                           norm_eps=1e-9)
+    np.testing.assert_allclose(o2, o1, rtol=1e-6, atol=1e-7)
+    w = rng.uniform(0.5, 2.0, 5)
+    o3, _ = oracle.prefill(q, k, v, la, b, one_seq(T), s0, norm_weight=w, norm_eps=1e-9)
+    np.testing.assert_allclose(o3, o1 * w, rtol=1e-13)
+
+
+def test_output_norm_decode_matches_prefill():
+    rng = np.random.default_rng(45)
+    q, k, v, la, b, s0 = rand_case(rng, 1, hk=1, hv=2, dk=4, dv=4)
+    w = rng.uniform(0.5, 2.0, 4)
+    o_p, f_p = oracle.prefill(q, k, v, la, b, one_seq(1), s0, norm_weight=w)
+    o_d, f_d = oracle.decode_step(s0, q, k, v, la, b, norm_weight=w)
+    np.testing.assert_allclose(o_d, o_p, rtol=1e-14)
+    np.testing.assert_array_equal(f_d, f_p)
+
+
 # ---------------------------------------------------------------- decode, packing, grouping
 
 def test_decode_chain_equals_prefill():
