@@ -226,7 +226,7 @@ def soak(fn, seconds: float):
         torch.cuda.synchronize()
 
 
-def time_decode(dev, stream, steps=256, n_rep=5):
+def time_decode(dev, stream, steps=256, n_rep=5, norm=False):
     """30-layer decode steps (one batched launch per step over the 30 layer states), rotating n_rep
     state replicas so that no step finds its 60 MiB of state in L2.  The `steps` launches are captured
     in one CUDA graph, as a model's decode step would be, so host launch overhead is not measured."""
@@ -237,9 +237,10 @@ def time_decode(dev, stream, steps=256, n_rep=5):
     q, k, v = di.q.to(dev), di.k.to(dev), di.v.to(dev)
     la, b = di.log_alpha.to(dev), di.beta.to(dev)
     out = torch.empty(DECODE_LAYERS, HV, D, dtype=torch.bfloat16, device=dev)
+    w = torch.linspace(0.5, 2.0, D, device=dev) if norm else None
 
     def step(i):
-        gdn.decode_step(states[i % n_rep], q[i], k[i], v[i], la[i], b[i], out=out, stream=stream)
+        gdn.decode_step(states[i % n_rep], q[i], k[i], v[i], la[i], b[i], out=out, stream=stream, norm_weight=w)
     with torch.cuda.stream(stream):
         for i in range(5):
             step(i)
@@ -544,6 +545,7 @@ def run_gb300(args):
             soak(lambda: plans[0].run(stream=stream), 1.5)
         total_ms, prep_ms, pass_ms = time_prefill_steps(plans, args.steps, args.warmup, stream)
         decode_us = time_decode(dev, stream)
+        decode_norm_us = time_decode(dev, stream, norm=True)
         decode_layer_us = time_decode_per_layer(dev, stream)
         scan_ms = time_scan(plan_scan, stream)
         qk_prep = time_qk_prep(dev, stream)
@@ -583,6 +585,9 @@ def run_gb300(args):
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                 "frac": dec_gbs / peaks["hbm_gbs"], "traffic": load_traffic("decode_step_kernel")},
                    "l2": "5 rotating state replicas (300 MiB)", "launch": "256 steps replayed as one CUDA graph",
+                   "with_output_norm": {"us_per_step": decode_norm_us,
+                                        "hbm_gbs": DECODE_STATE_BYTES / (decode_norm_us * 1e-6) / 1e9,
+                                        "fused": "root-mean-square output norm with per-channel weight"},
                    "per_layer_launches": {"us_per_step": decode_layer_us,
                                           "hbm_gbs": DECODE_STATE_BYTES / (decode_layer_us * 1e-6) / 1e9,
                                           "launch": "30 single-layer launches per step, 64 steps in one "

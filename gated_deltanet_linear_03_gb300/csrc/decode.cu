@@ -18,9 +18,13 @@
 // The section "Reduce intermediate and state traffic" asks for exactly this
 // fusion: the temporaries never leave registers.
 #include "gdn_internal.cuh"
+#include "sm100.cuh"
 
 namespace gdn {
 namespace {
+
+using sm100::cluster_sync;
+using sm100::ld_dsmem_f32;
 
 constexpr int kRowsPerGroup = 8;   // rows each lane group carries at once
 constexpr int kThreads = 128;
@@ -52,13 +56,16 @@ __device__ __forceinline__ void reduce16(float (&v)[16], int lane) {
     }
 }
 
-template <int D>
+// NORM: fuse the output normalisation o <- o / sqrt(mean_head(o^2) + eps) * w.  Each warp's rows belong to
+// one head; a head is one warp (d = 32), one CTA (d = 64) or a cluster of four CTAs (d = 128), whose partial
+// sums of squares are exchanged through distributed shared memory.
+template <int D, bool NORM>
 __global__ void __launch_bounds__(kThreads)
 decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
                    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                    const __nv_bfloat16 *__restrict__ v, const float *__restrict__ log_alpha,
                    const float *__restrict__ beta, void *__restrict__ out, int out_f32, int qk_norm,
-                   float q_scale) {
+                   float q_scale, const float *__restrict__ norm_w, float norm_eps) {
     constexpr int LPR = D / 4;                  // lanes per row
     constexpr int GROUPS = 32 / LPR;            // lane groups per warp
     constexpr int WARP_ROWS = GROUPS * kRowsPerGroup;
@@ -67,7 +74,9 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int group = lane / LPR, gl = lane % LPR;
     const long row0 = ((long)blockIdx.x * (kThreads / 32) + warp) * WARP_ROWS + group * kRowsPerGroup;
-    if (row0 >= total_rows) return;  // whole group out of range (8 | D keeps groups in one head)
+    // whole group out of range (8 | D keeps groups in one head).  With NORM and d >= 64 the grid covers the
+    // rows exactly (the host checks), so no thread of a CTA that meets a barrier below leaves early.
+    if (row0 >= total_rows) return;
 
     const long head = row0 / D;                 // flat (n, h)
     const int h = (int)(head % hv);
@@ -150,13 +159,46 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
 
     // outputs: the holder lane of sq_i writes o_i (with 32 lanes per row two
     // lanes hold each sum; the even one writes)
-    if (LPR == 32 && (lane & 1)) return;
+    const bool writer = LPR != 32 || (lane & 1) == 0;
+    float ov[PER];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int idx = my_base + j;
+        ov[j] = 0.f;
+        if (idx >= 8 && idx < 16) {
+            ov[j] = alpha * fq * part[j] + u[idx - 8] * kq;
+            if (writer) ss = fmaf(ov[j], ov[j], ss);
+        }
+    }
+    float scale = 1.f;
+    if (NORM) {
+        __shared__ float warp_ss[kThreads / 32];
+        __shared__ float cta_ss;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        float head_ss = ss;   // d = 32: the warp is the head
+        if (D >= 64) {
+            if (lane == 0) warp_ss[warp] = ss;
+            __syncthreads();
+            head_ss = (warp_ss[0] + warp_ss[1]) + (warp_ss[2] + warp_ss[3]);
+            if (D == 128) {   // the head spans the four CTAs of this cluster
+                if (threadIdx.x == 0) cta_ss = head_ss;
+                cluster_sync();
+                head_ss = (ld_dsmem_f32(&cta_ss, 0) + ld_dsmem_f32(&cta_ss, 1)) +
+                          (ld_dsmem_f32(&cta_ss, 2) + ld_dsmem_f32(&cta_ss, 3));
+                cluster_sync();   // no CTA leaves while its partial may still be read
+            }
+        }
+        scale = rsqrtf(head_ss * (1.f / D) + norm_eps);
+    }
+    if (!writer) return;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
         const int idx = my_base + j;
         if (idx >= 8 && idx < 16) {
             const int i = idx - 8;
-            const float o = alpha * fq * part[j] + u[i] * kq;
+            const float o = NORM ? ov[j] * scale * norm_w[row_in_head + i] : ov[j];
             const size_t oi = (size_t)head * D + row_in_head + i;
             if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
             else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(o);
@@ -351,6 +393,34 @@ cudaError_t launch_short_prefill(const PrefillProblem &p) {
     }
 }
 
+namespace {
+
+template <int D, bool NORM>
+cudaError_t launch_decode_d(const DecodeProblem &p, unsigned grid) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (NORM && D == 128) ? 4 : 1;   // four 32-row CTAs make a 128-row head
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = p.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = (NORM && D == 128) ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_step_kernel<D, NORM>, (int)((long)p.n * p.hv * p.d), p.hk,
+                                             p.hv, p.state, p.q, p.k, p.v, p.log_alpha, p.beta, p.out, p.out_f32,
+                                             p.qk_norm, p.q_scale, p.norm_w, p.norm_eps);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_decode_norm(const DecodeProblem &p, unsigned grid) {
+    return p.norm_w ? launch_decode_d<D, true>(p, grid) : launch_decode_d<D, false>(p, grid);
+}
+
+}  // namespace
+
 cudaError_t launch_decode(const DecodeProblem &p) {
     const long total_rows = (long)p.n * p.hv * p.d;
     if (total_rows == 0) return cudaSuccess;
@@ -362,21 +432,13 @@ cudaError_t launch_decode(const DecodeProblem &p) {
         default: return cudaErrorInvalidValue;
     }
     const long rows_per_block = (long)warp_rows * (kThreads / 32);
+    if (p.norm_w && p.d >= 64 && total_rows % rows_per_block) return cudaErrorInvalidValue;   // see the kernel
     const unsigned grid = (unsigned)((total_rows + rows_per_block - 1) / rows_per_block);
     switch (p.d) {
-        case 32:
-            decode_step_kernel<32><<<grid, kThreads, 0, p.stream>>>((int)total_rows, p.hk, p.hv, p.state, p.q, p.k, p.v,
-                                                                   p.log_alpha, p.beta, p.out, p.out_f32, p.qk_norm, p.q_scale);
-            break;
-        case 64:
-            decode_step_kernel<64><<<grid, kThreads, 0, p.stream>>>((int)total_rows, p.hk, p.hv, p.state, p.q, p.k, p.v,
-                                                                   p.log_alpha, p.beta, p.out, p.out_f32, p.qk_norm, p.q_scale);
-            break;
-        default:
-            decode_step_kernel<128><<<grid, kThreads, 0, p.stream>>>((int)total_rows, p.hk, p.hv, p.state, p.q, p.k,
-                                                                    p.v, p.log_alpha, p.beta, p.out, p.out_f32, p.qk_norm, p.q_scale);
+        case 32: return launch_decode_norm<32>(p, grid);
+        case 64: return launch_decode_norm<64>(p, grid);
+        default: return launch_decode_norm<128>(p, grid);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace gdn

@@ -224,11 +224,14 @@ gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_tokens, in
 gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
                            const void *q, const void *k, const void *v,
                            const float *log_alpha, const float *beta,
-                           void *out, int out_dtype, int qk_norm, float q_scale, void *stream) {
+                           void *out, int out_dtype, int qk_norm, float q_scale,
+                           const float *norm_weight, float norm_eps, void *stream) {
     gdn_status st = check_heads(hk, hv, dk, dv);
     if (st != GDN_OK) return st;
     if (n < 0) return GDN_ERR_INVALID_ARG;
     if ((qk_norm != 0 && qk_norm != 1) || !isfinite(q_scale)) return GDN_ERR_INVALID_ARG;
+    if (norm_weight && (!isfinite(norm_eps) || norm_eps < 0.f)) return GDN_ERR_INVALID_ARG;
+    if (norm_weight && !aligned16(norm_weight)) return GDN_ERR_ALIGNMENT;
     if (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
     if (n == 0) return GDN_OK;
     if (!state || !q || !k || !v || !log_alpha || !beta || !out) return GDN_ERR_INVALID_ARG;
@@ -253,6 +256,7 @@ gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
     p.v = static_cast<const __nv_bfloat16 *>(v);
     p.log_alpha = log_alpha; p.beta = beta; p.out = out; p.out_f32 = out_dtype == GDN_DTYPE_F32;
     p.qk_norm = qk_norm; p.q_scale = q_scale;
+    p.norm_w = norm_weight; p.norm_eps = norm_eps;
     p.err = nullptr;
     p.stream = static_cast<cudaStream_t>(stream);
     return gdn::launch_decode(p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

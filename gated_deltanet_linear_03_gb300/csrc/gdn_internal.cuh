@@ -61,6 +61,8 @@ struct DecodeProblem {
     int out_f32;
     int qk_norm;
     float q_scale;
+    const float *norm_w;   // fused output normalisation weight [d], or null
+    float norm_eps;
     unsigned int *err;
     cudaStream_t stream;
 };

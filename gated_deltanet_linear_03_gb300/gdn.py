@@ -58,7 +58,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdn_prefill_workspace_size.restype = Z
     lib.gdn_prefill_algo.argtypes = [I, I, I, I, I, I, P]
     lib.gdn_prefill_algo.restype = I
-    lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, I, ctypes.c_float, P]
+    lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, I, ctypes.c_float, P, ctypes.c_float, P]
     lib.gdn_decode_step.restype = I
     lib.gdn_device_error.argtypes = [P]
     lib.gdn_device_error.restype = I
@@ -265,8 +265,11 @@ class PrefillPlan:
 
 def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                 log_alpha: torch.Tensor, beta: torch.Tensor, *, out: Optional[torch.Tensor] = None,
-                out_dtype=torch.bfloat16, stream=None, qk_norm: bool = False, q_scale: float = 1.0) -> torch.Tensor:
-    """Run ``gdn_decode_step`` (state updated in place).  Returns ``out``."""
+                out_dtype=torch.bfloat16, stream=None, qk_norm: bool = False, q_scale: float = 1.0,
+                norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6) -> torch.Tensor:
+    """Run ``gdn_decode_step`` (state updated in place).  Returns ``out``.
+
+    ``norm_weight`` (fp32 [dv]): fuse the output normalisation o / sqrt(mean(o^2) + norm_eps) * weight."""
     lib = load_library()
     _need(state, "state", torch.float32, 4)
     _need(q, "q", torch.bfloat16, 3)
@@ -280,7 +283,7 @@ def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.
         out = torch.empty(n, hv, dv, device=q.device, dtype=out_dtype)
     st = lib.gdn_decode_step(n, hk, hv, dk, dv, _ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
                              _ptr(beta), _ptr(out), DTYPE[out.dtype], int(bool(qk_norm)), float(q_scale),
-                             _stream_ptr(stream))
+                             _ptr(norm_weight), float(norm_eps), _stream_ptr(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_decode_step")
     return out

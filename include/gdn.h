@@ -189,11 +189,20 @@ GDN_API int gdn_prefill_algo(int n_seqs, int total_tokens, int hk, int hv, int d
  *   log_alpha, beta  fp32 [n, hv]
  *   out              [n, hv, dv], dtype out_dtype; must not overlap state
  *   qk_norm, q_scale as for gdn_prefill
+ *   norm_weight      fp32 [dv] device array, or NULL.  When given, the output
+ *                    normalisation is fused into the step: each head's output
+ *                    vector o becomes o / sqrt(mean(o^2) + norm_eps) * norm_weight
+ *                    ("Optimizing on-device inference for Apple Silicon",
+ *                    section "Reduce intermediate and state traffic": the
+ *                    decode path fuses the recurrent update with its
+ *                    normalisation; the form of the norm is our reading).
+ *   norm_eps         finite, >= 0; used only with norm_weight
  */
 GDN_API gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
                            const void *q, const void *k, const void *v,
                            const float *log_alpha, const float *beta,
-                           void *out, int out_dtype, int qk_norm, float q_scale, void *stream);
+                           void *out, int out_dtype, int qk_norm, float q_scale,
+                           const float *norm_weight, float norm_eps, void *stream);
 
 /*
  * Synchronise `stream` and return (and clear) the device-side error word the

@@ -112,9 +112,9 @@ def test_decode_rejects_bad_args(lib):
     P = ctypes.c_void_p
 
     def dec(n=1, hk=1, hv=2, d=128, state=FAKE, q=FAKE * 2, k=FAKE * 3, v=FAKE * 4, la=FAKE * 5, b=FAKE * 6,
-            out=FAKE * 7, odt=0, qkn=0, qs=1.0):
+            out=FAKE * 7, odt=0, qkn=0, qs=1.0, nw=None, ne=1e-6):
         return lib.gdn_decode_step(n, hk, hv, d, d, P(state), P(q), P(k), P(v), P(la), P(b), P(out), odt, qkn, qs,
-                                   None)
+                                   P(nw), ne, None)
 
     assert dec(hk=3, hv=4) == 1
     assert dec(d=96) == 2
@@ -126,6 +126,8 @@ def test_decode_rejects_bad_args(lib):
     assert dec(out=FAKE) == 1                # out overlaps state
     assert dec(qkn=-1) == 1
     assert dec(qs=float("inf")) == 1
+    assert dec(nw=FAKE * 9, ne=-1.0) == 1    # negative eps
+    assert dec(nw=FAKE * 9 + 4) == 3         # misaligned weight
 
 
 def test_auto_algo_rule(lib):

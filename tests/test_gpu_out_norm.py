@@ -1,0 +1,63 @@
+"""GPU parity of the fused output normalisation (o / sqrt(mean(o^2) + eps) * w per head) against the fp64
+oracle.  Normalised outputs are O(1), so they are compared in fp32 against the 2e-3 bound, and in bf16
+against the bf16 rounding of the reference (relative 2^-8)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_linear_03_gb300 import synth
+from helpers import OUT_ATOL, STATE_RTOL, max_abs_err, np32, state_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    from gated_deltanet_linear_03_gb300 import gdn as g
+    g.load_library()
+    return g
+
+
+def weight(d, seed):
+    gen = torch.Generator().manual_seed(seed)
+    return 0.5 + 1.5 * torch.rand(d, generator=gen)
+
+
+def bf16_ok(out, ref):
+    ref = np.asarray(ref, np.float64)
+    return np.all(np.abs(np32(out).astype(np.float64) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-3)
+
+
+# d = 128: four CTAs of 32 rows per head (a cluster); d = 64: one CTA per head; d = 32: one warp per head,
+# including a batch whose rows leave the last CTA partly empty (n * hv * 32 not a multiple of 128)
+@pytest.mark.parametrize("d,hk,hv,n", [(128, 16, 32, 30), (128, 2, 4, 1), (64, 2, 4, 3), (32, 2, 2, 5), (32, 1, 1, 3)])
+@pytest.mark.parametrize("qk_norm", [False, True])
+def test_decode_with_output_norm(gdn, d, hk, hv, n, qk_norm):
+    steps = 3
+    di = synth.decode_inputs(n, steps, hk=hk, hv=hv, dk=d, dv=d, seed=60 + d, raw_qk=qk_norm)
+    w = weight(d, 61)
+    scale = 1.0 / np.sqrt(d) if qk_norm else 1.0
+    st_gpu = di.state.cuda()
+    st_ref = di.state.double().numpy()
+    for s in range(steps):
+        args = [x[s] for x in (di.q, di.k, di.v, di.log_alpha, di.beta)]
+        dev = [a.cuda() for a in args]
+        out = gdn.decode_step(st_gpu, *dev, out_dtype=torch.float32, qk_norm=qk_norm, q_scale=scale,
+                              norm_weight=w.cuda(), norm_eps=1e-6)
+        o_ref, st_ref = oracle.decode_step(st_ref, *[np32(a) for a in args], qk_norm=qk_norm, q_scale=scale,
+                                           norm_weight=w.numpy(), norm_eps=1e-6)
+        torch.cuda.synchronize()
+        assert max_abs_err(out, o_ref) <= OUT_ATOL
+        assert state_rel_err(st_gpu, st_ref) <= STATE_RTOL
+
+
+def test_decode_output_norm_bf16(gdn):
+    di = synth.decode_inputs(30, 1, seed=62)
+    w = weight(128, 63)
+    st = di.state.cuda()
+    args = [x[0] for x in (di.q, di.k, di.v, di.log_alpha, di.beta)]
+    out = gdn.decode_step(st, *[a.cuda() for a in args], norm_weight=w.cuda())
+    o_ref, _ = oracle.decode_step(di.state.double().numpy(), *[np32(a) for a in args], norm_weight=w.numpy())
+    torch.cuda.synchronize()
+    assert bf16_ok(out, o_ref)
