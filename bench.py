@@ -315,8 +315,11 @@ def time_qk_prep(dev, stream, iters=20):
         kn.copy_(F.normalize(k.float(), dim=-1, eps=1e-3).to(torch.bfloat16))
         plain.run(stream=stream)
 
+    w = torch.linspace(0.5, 2.0, D, device=dev)
+    normed = gdn.PrefillPlan(q, k, v, la, b, cu, cu_seqlens_host=cu_host, qk_norm=True, q_scale=scale, norm_weight=w)
     res = {}
-    for name, fn in (("fused_us", lambda: fused.run(stream=stream)), ("separate_pass_us", separate)):
+    for name, fn in (("fused_us", lambda: fused.run(stream=stream)), ("separate_pass_us", separate),
+                     ("fused_with_output_norm_us", lambda: normed.run(stream=stream))):
         with torch.cuda.stream(stream):
             for _ in range(3):
                 fn()
@@ -328,7 +331,8 @@ def time_qk_prep(dev, stream, iters=20):
             e0.record(stream)
         torch.cuda.synchronize()
         res[name] = s0.elapsed_time(e0) * 1e3 / iters
-    res["workload"] = "4K layer from raw q/k projections (L2-normalise q and k, q / sqrt(d))"
+    res["workload"] = ("4K layer from raw q/k projections (L2-normalise q and k, q / sqrt(d)); the last key also "
+                       "fuses the output normalisation")
     return res
 
 

@@ -635,13 +635,45 @@ __device__ __forceinline__ void load_chunk_inputs(ChunkInputs &in, const float *
 
 // Outputs of one chunk for this thread's token and 16 value rows (Q-row threads):
 // O_i = e^{g_i} (Q S^T)_i (in qs) + (R X)_i ((R_hi + R_lo) X_hi, and (R_hi + R_lo) X_lo).
-__device__ __forceinline__ void store_outputs(float (&qs)[DG], uint32_t tmem_rx, int grp, int i, int L, int t0,
-                                              int hv, int h, int rowg, void *__restrict__ out, int out_f32) {
-    float a[16], b[16];
-    tmem_ld16x2(tmem_rx + grp * 16, tmem_rx + 32 + grp * 16, a, b);
-    if (i < L) {
+// outputs_begin adds R X into qs; outputs_end writes them.  NORM: the output normalisation over the head's
+// 128 rows, which this cluster's four CTAs hold 32 of each: begin publishes the token's sum of squares over
+// this thread's rows and arrives on the cluster barrier, end waits for it, adds the head's sums through
+// distributed shared memory and scales.  Every thread of the cluster takes part in each round (K-row threads
+// arrive early and wait later); `valid` false keeps the round but skips TMEM and global memory.
+template <bool NORM>
+__device__ __forceinline__ void outputs_begin(float (&qs)[DG], uint32_t tmem_rx, int grp, int i, int L, bool valid,
+                                              float (*ps)[64]) {
+    if (valid) {
+        float a[16], b[16];
+        tmem_ld16x2(tmem_rx + grp * 16, tmem_rx + 32 + grp * 16, a, b);
 #pragma unroll
         for (int e = 0; e < DG; ++e) qs[e] += a[e] + b[e];
+    }
+    if (NORM) {
+        float ss = 0.f;
+        if (valid && i < L) {
+#pragma unroll
+            for (int e = 0; e < DG; ++e) ss = fmaf(qs[e], qs[e], ss);
+        }
+        ps[grp][i] = ss;
+        cluster_arrive();
+    }
+}
+
+template <bool NORM>
+__device__ __forceinline__ void outputs_end(float (&qs)[DG], int grp, int i, int L, int t0, int hv, int h, int rowg,
+                                            void *__restrict__ out, int out_f32, bool valid, float (*ps)[64],
+                                            const float *__restrict__ norm_w, float norm_eps) {
+    if (NORM) {
+        cluster_wait();
+        float tot = 0.f;
+#pragma unroll
+        for (int rk = 0; rk < D / DS; ++rk) tot += ld_dsmem_f32(&ps[0][i], rk) + ld_dsmem_f32(&ps[1][i], rk);
+        const float sc = rsqrtf(tot * (1.f / D) + norm_eps);
+#pragma unroll
+        for (int e = 0; e < DG; ++e) qs[e] *= sc * norm_w[rowg + e];
+    }
+    if (valid && i < L) {
         const size_t o = ((size_t)(t0 + i) * hv + h) * D + rowg;
         if (out_f32) {
             float4 *op = reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + o);
@@ -663,6 +695,7 @@ __device__ __forceinline__ void store_outputs(float (&qs)[DG], uint32_t tmem_rx,
 // Thread 0 issues the [Q;K] S^T MMAs and thread 32 the TMA loads (both Q-row threads, which have nothing
 // to do before the X barrier); threads kPxIssuer and kRxIssuer (K-row threads, which have nothing to do
 // between the X barrier and the state update) issue P X and R X.
+template <bool NORM>
 __global__ void __launch_bounds__(kPassThreads, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
@@ -671,10 +704,11 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                   const float *__restrict__ log_alpha, const float *__restrict__ beta,
                   const float *__restrict__ init_state, const int32_t *__restrict__ cu, int n_seqs, int total,
                   int nch, int hk, int hv, void *__restrict__ out, int out_f32, float *__restrict__ final_state,
-                  unsigned int *err) {
+                  const float *__restrict__ norm_w, float norm_eps, unsigned int *err) {
     extern __shared__ uint8_t pass_raw[];
     uint8_t *sm = align1024(pass_raw);
     __shared__ uint64_t bar_tma[2], bar_d1, bar_px, bar_rx[2];
+    __shared__ float ps_norm[2][2][64];   // NORM: per-token sums of squares of each group's rows, by chunk parity
     __shared__ uint32_t tmem_slot;
 
     constexpr int SLICES = D / DS;
@@ -774,8 +808,18 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     auto rx_parity = [](int cc) { return (uint32_t)((cc >> 1) & 1); };
 
     float qs[DG];
-    int c = 0, prev_t0 = 0, prev_L = 0;
-    for (; ok && c < nchunks; ++c) {
+    float qcur_n[DG];   // NORM: this chunk's e^g Q S^T, kept until the previous chunk's outputs have left
+    int c = 0, prev_t0 = 0, prev_L = 0, c_stop = nchunks;
+    // With NORM every chunk keeps its cluster barrier round even after an error (the cluster barrier has no
+    // time limit, so no CTA may leave the sequence of rounds its peers still run): work stops, rounds do not.
+    for (; (NORM || ok) && c < nchunks; ++c) {
+        if (NORM && !ok) {
+            if (c > 0) {
+                cluster_arrive();
+                cluster_wait();
+            }
+            continue;
+        }
         const int s = c & 1;
         const uint32_t par = c & 1;
         const int t0 = ta + c * C, L = min(C, tb - t0);
@@ -858,6 +902,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 mma_bf16(rx, dRL0 + so + 2 * kk, dXOP + 128 * kk, idb, 1);
             mma_commit(&bar_rx[par]);
         }
+        if (NORM && krow && c > 0) cluster_arrive();   // K-row threads' share of this chunk's output round
         if (!krow) {
             // Q-row threads, off the state chain while P X runs: e^{g_i} (Q S^T)_i of this chunk (D1 is
             // rewritten only after the end-of-chunk barrier), then the previous chunk's outputs, whose R X
@@ -871,14 +916,25 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 #pragma unroll
                 for (int r = 0; r < DG; ++r) qcur[r] = (eg * cur.f) * (a[r] + b[r]);
             }
+            if (NORM) {
+#pragma unroll
+                for (int r = 0; r < DG; ++r) qcur_n[r] = qcur[r];
+            }
             if (c > 0) {
                 if (!mbar_wait(&bar_rx[par ^ 1], rx_parity(c - 1))) ok = false;
                 tc_fence_after();
-                store_outputs(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, prev_t0, hv, h, rowg, out,
-                              out_f32);
+                outputs_begin<NORM>(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, true,
+                                    ps_norm[(c - 1) & 1]);
+                // without the norm the outputs leave now; with it, after the state update (the cluster round
+                // then overlaps the update instead of delaying it)
+                if (!NORM)
+                    outputs_end<false>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, true, nullptr, norm_w,
+                                       norm_eps);
             }
+            if (!NORM) {
 #pragma unroll
-            for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
+                for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
+            }
         }
 
         // state: S[r][d] <- e^{g_L} S[r][d] + (P X)[d][r] + (P X)[d][32 + r]   (this group's 16 rows)
@@ -892,29 +948,51 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             for (int e = 0; e < DG; ++e) S[e] = fmaf(eL, S[e], a[e] + b[e]);
         }
         write_sop();
+        if (NORM) {
+            if (krow) {
+                if (c > 0) cluster_wait();
+            } else {
+                if (c > 0)
+                    outputs_end<true>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, true,
+                                      ps_norm[(c - 1) & 1], norm_w, norm_eps);
+#pragma unroll
+                for (int r = 0; r < DG; ++r) qs[r] = qcur_n[r];
+            }
+        }
         prev_t0 = t0;
         prev_L = L;
         fence_proxy_async_smem();
         tc_fence_before();
         ok = __syncthreads_and(ok);
         tc_fence_after();
+        if (!ok && c_stop == nchunks) c_stop = c + 1;
     }
+    if (!NORM) c_stop = c;
 
     if (!ok) {
-        // the loop stopped after chunk c - 1; its prefetch of chunk c may still be in flight
+        // the loop's work stopped after chunk c_stop - 1; its prefetch of chunk c_stop may still be in flight
         if (tid == 0 && started) {
             raise_error(err, kErrTimeout);
-            if (c < nchunks) mbar_wait(&bar_tma[c & 1], (c >> 1) & 1);
+            if (c_stop < nchunks) mbar_wait(&bar_tma[c_stop & 1], (c_stop >> 1) & 1);
+        }
+        if (NORM && nchunks > 0) {   // the last chunk's output round, kept
+            cluster_arrive();
+            cluster_wait();
         }
     } else {
-        if (nchunks > 0 && !krow) {
+        if (nchunks > 0) {
             const uint32_t lp = (nchunks - 1) & 1;
-            const bool done = mbar_wait(&bar_rx[lp], rx_parity(nchunks - 1));
-            tc_fence_after();
-            if (done)
-                store_outputs(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32);
-            else
-                raise_error(err, kErrTimeout);
+            if (!krow) {
+                const bool done = mbar_wait(&bar_rx[lp], rx_parity(nchunks - 1));
+                tc_fence_after();
+                if (!done) raise_error(err, kErrTimeout);
+                outputs_begin<NORM>(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, done, ps_norm[lp]);
+                outputs_end<NORM>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, done, ps_norm[lp], norm_w,
+                                  norm_eps);
+            } else if (NORM) {
+                cluster_arrive();
+                cluster_wait();
+            }
         }
         if (final_state) {
 #pragma unroll
@@ -922,7 +1000,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         }
     }
     tc_fence_before();
-    __syncthreads();
+    if (NORM) cluster_sync();   // no CTA leaves while a peer may still read its sums
+    else __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, PASS_TMEM_COLS);
 }
@@ -988,7 +1067,9 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
     if (dev < 128 && !attrs_set[dev]) {
         e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
+            e = cudaFuncSetAttribute(state_pass_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(state_pass_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
         if (e != cudaSuccess) return e;
         attrs_set[dev] = true;
     }
@@ -1012,12 +1093,30 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
+        // with the output normalisation the D / DS slices of a (sequence, head) form one cluster
         const unsigned grid2 = (unsigned)(p.n_seqs * p.hv * (D / DS));
-        state_pass_kernel<<<grid2, kPassThreads, PASS_SMEM, p.stream>>>(
-            qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, p.qk_norm ? norms : nullptr, p.q_scale, p.log_alpha, p.beta,
-            p.init_state, p.cu_seqlens, p.n_seqs,
-            p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state, p.err);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = D / DS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid2);
+        cfg.blockDim = dim3(kPassThreads);
+        cfg.dynamicSmemBytes = PASS_SMEM;
+        cfg.stream = p.stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = p.norm_w ? 1 : 0;
+        const float *nrm = p.qk_norm ? norms : nullptr;
+        e = p.norm_w ? cudaLaunchKernelEx(&cfg, state_pass_kernel<true>, qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm,
+                                          p.q_scale, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.n_seqs,
+                                          p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state,
+                                          p.norm_w, p.norm_eps, p.err)
+                     : cudaLaunchKernelEx(&cfg, state_pass_kernel<false>, qmap, kmap, phmap, plmap, rhmap, rlmap, p.v,
+                                          nrm, p.q_scale, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.n_seqs,
+                                          p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state,
+                                          p.norm_w, p.norm_eps, p.err);
+        if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

@@ -59,7 +59,8 @@ __device__ __forceinline__ void reduce16(float (&v)[16], int lane) {
 // NORM: fuse the output normalisation o <- o / sqrt(mean_head(o^2) + eps) * w.  Each warp's rows belong to
 // one head; a head is one warp (d = 32), one CTA (d = 64) or a cluster of four CTAs (d = 128), whose partial
 // sums of squares are exchanged through distributed shared memory.
-template <int D, bool NORM>
+// PREP: query/key preparation (qk_norm, or q_scale != 1); the plain instantiation has none of its arithmetic.
+template <int D, bool PREP, bool NORM>
 __global__ void __launch_bounds__(kThreads)
 decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
                    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
@@ -98,8 +99,8 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
 
     // k.q over the head (same for every row of the group), and the preparation factors of k and q
     float kq = kv[0] * qv[0] + kv[1] * qv[1] + kv[2] * qv[2] + kv[3] * qv[3];
-    float fk = 1.f, fq = q_scale;
-    if (qk_norm) {
+    float fk = 1.f, fq = PREP ? q_scale : 1.f;
+    if (PREP && qk_norm) {
         float kk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
         float qq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
 #pragma unroll
@@ -114,7 +115,7 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
 #pragma unroll
         for (int off = LPR / 2; off >= 1; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
     }
-    kq *= fk * fq;
+    if (PREP) kq *= fk * fq;
 
     const float la = clamp_log_alpha(log_alpha[head]);
     const float alpha = __expf(la);
@@ -141,14 +142,14 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
 #pragma unroll
         for (int j = 0; j < PER; ++j)
             if (my_base + j == i) mine = part[j];
-        const float sk = fk * __shfl_sync(0xffffffffu, mine, src_k);
+        const float sk = (PREP ? fk : 1.f) * __shfl_sync(0xffffffffu, mine, src_k);
         u[i] = b * (__bfloat162float(vrow[i]) - alpha * sk);
     }
 
     // write the updated rows
 #pragma unroll
     for (int i = 0; i < kRowsPerGroup; ++i) {
-        const float uk = u[i] * fk;
+        const float uk = PREP ? u[i] * fk : u[i];
         float4 o;
         o.x = alpha * s[i].x + uk * kv[0];
         o.y = alpha * s[i].y + uk * kv[1];
@@ -167,7 +168,7 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
         const int idx = my_base + j;
         ov[j] = 0.f;
         if (idx >= 8 && idx < 16) {
-            ov[j] = alpha * fq * part[j] + u[idx - 8] * kq;
+            ov[j] = (PREP ? alpha * fq : alpha) * part[j] + u[idx - 8] * kq;
             if (writer) ss = fmaf(ov[j], ov[j], ss);
         }
     }
@@ -218,7 +219,7 @@ __host__ __device__ constexpr int short_warps() { return D == 32 ? 1 : 4; }
 template <int D>
 __host__ __device__ constexpr int short_rows() { return short_warps<D>() * (32 / (D / 4)) * kRowsPerGroup; }   // 32, 64, 32
 
-template <int D>
+template <int D, bool NORM>
 struct __align__(16) ShortSmem {
     __nv_bfloat16 k[kShortMaxTokens][D];
     __nv_bfloat16 q[kShortMaxTokens][D];
@@ -228,20 +229,22 @@ struct __align__(16) ShortSmem {
     float kq[kShortMaxTokens];   // prepared k.q
     float fk[kShortMaxTokens];   // preparation factors of k and q
     float fq[kShortMaxTokens];
+    float o[NORM ? kShortMaxTokens : 1][short_rows<D>()];   // outputs, held back for the output normalisation
+    float ps[NORM ? kShortMaxTokens : 1];   // per-token sum of squares of this CTA's outputs, then the scale
 };
 
-template <int D>
+template <int D, bool NORM>
 __global__ void __launch_bounds__(short_warps<D>() * 32)
 short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__restrict__ q,
                      const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
                      const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
                      void *__restrict__ out, int out_f32, float *__restrict__ final_state, int qk_norm,
-                     float q_scale) {
+                     float q_scale, const float *__restrict__ norm_w, float norm_eps) {
     constexpr int LPR = D / 4, GROUPS = 32 / LPR, ROWS = short_rows<D>(), SLICES = D / ROWS;
     constexpr int NT = short_warps<D>() * 32;
     constexpr int PER = (16 / LPR) > 0 ? (16 / LPR) : 1;
-    __shared__ ShortSmem<D> sm;
+    __shared__ ShortSmem<D, NORM> sm;
 
     const int slice = blockIdx.x % SLICES;
     const int h = (blockIdx.x / SLICES) % hv;
@@ -360,7 +363,8 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
                     const int i = idx - 8;
                     const float o = alpha * fq * part[j] + u[i] * kq;
                     const size_t oi = ((size_t)(tbeg + t) * hv + h) * D + row_in_head + i;
-                    if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
+                    if (NORM) sm.o[t][vrow0 + i] = o;
+                    else if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
                     else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(o);
                 }
             }
@@ -370,15 +374,76 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
 #pragma unroll
         for (int i = 0; i < kRowsPerGroup; ++i) srow[(size_t)i * (D / 4)] = s[i];
     }
+    if (NORM) {
+        // Output normalisation over the head's d rows: per token, the sum of squares of this CTA's rows; with
+        // d = 128 the head's four CTAs form a cluster and add theirs through distributed shared memory.
+        __syncthreads();
+        for (int t = tid; t < L; t += NT) {
+            float x = 0.f;
+            for (int j = 0; j < ROWS; ++j) x = fmaf(sm.o[t][j], sm.o[t][j], x);
+            sm.ps[t] = x;
+        }
+        float scale_t[(kShortMaxTokens + NT - 1) / NT];
+        if (SLICES > 1) {
+            cluster_sync();
+#pragma unroll
+            for (int m = 0; m < (kShortMaxTokens + NT - 1) / NT; ++m) {
+                const int t = tid + m * NT;
+                float x = 0.f;
+                if (t < L)
+                    for (int rk = 0; rk < SLICES; ++rk) x += ld_dsmem_f32(&sm.ps[t], rk);
+                scale_t[m] = x;
+            }
+            cluster_sync();   // every peer has read this CTA's sums
+        } else {
+            __syncthreads();
+#pragma unroll
+            for (int m = 0; m < (kShortMaxTokens + NT - 1) / NT; ++m) {
+                const int t = tid + m * NT;
+                scale_t[m] = t < L ? sm.ps[t] : 0.f;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < (kShortMaxTokens + NT - 1) / NT; ++m) {
+            const int t = tid + m * NT;
+            if (t < L) sm.ps[t] = rsqrtf(scale_t[m] * (1.f / D) + norm_eps);
+        }
+        __syncthreads();
+        for (int i = tid; i < L * ROWS; i += NT) {
+            const int t = i / ROWS, j = i % ROWS;
+            const float o = sm.o[t][j] * sm.ps[t] * norm_w[slice * ROWS + j];
+            const size_t oi = ((size_t)(tbeg + t) * hv + h) * D + slice * ROWS + j;
+            if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
+            else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(o);
+        }
+    }
+}
+
+template <int D, bool NORM>
+cudaError_t launch_short_dn(const PrefillProblem &p) {
+    constexpr int SLICES = D / short_rows<D>();   // CTAs per head; a cluster when the output is normalised
+    const unsigned grid = (unsigned)(p.n_seqs * p.hv * SLICES);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = SLICES;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(short_warps<D>() * 32);
+    cfg.stream = p.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = (NORM && SLICES > 1) ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, short_prefill_kernel<D, NORM>, p.total_tokens, p.hk, p.hv, p.q, p.k, p.v,
+                                             p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.out, p.out_f32,
+                                             p.final_state, p.qk_norm, p.q_scale, p.norm_w, p.norm_eps);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_short_d(const PrefillProblem &p) {
-    const unsigned grid = (unsigned)(p.n_seqs * p.hv * (D / short_rows<D>()));
-    short_prefill_kernel<D><<<grid, short_warps<D>() * 32, 0, p.stream>>>(
-        p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.out,
-        p.out_f32, p.final_state, p.qk_norm, p.q_scale);
-    return cudaGetLastError();
+    return p.norm_w ? launch_short_dn<D, true>(p) : launch_short_dn<D, false>(p);
 }
 
 }  // namespace
@@ -395,7 +460,7 @@ cudaError_t launch_short_prefill(const PrefillProblem &p) {
 
 namespace {
 
-template <int D, bool NORM>
+template <int D, bool PREP, bool NORM>
 cudaError_t launch_decode_d(const DecodeProblem &p, unsigned grid) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -408,15 +473,20 @@ cudaError_t launch_decode_d(const DecodeProblem &p, unsigned grid) {
     cfg.stream = p.stream;
     cfg.attrs = attr;
     cfg.numAttrs = (NORM && D == 128) ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_step_kernel<D, NORM>, (int)((long)p.n * p.hv * p.d), p.hk,
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_step_kernel<D, PREP, NORM>, (int)((long)p.n * p.hv * p.d), p.hk,
                                              p.hv, p.state, p.q, p.k, p.v, p.log_alpha, p.beta, p.out, p.out_f32,
                                              p.qk_norm, p.q_scale, p.norm_w, p.norm_eps);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+template <int D, bool PREP>
+cudaError_t launch_decode_prep(const DecodeProblem &p, unsigned grid) {
+    return p.norm_w ? launch_decode_d<D, PREP, true>(p, grid) : launch_decode_d<D, PREP, false>(p, grid);
+}
+
 template <int D>
 cudaError_t launch_decode_norm(const DecodeProblem &p, unsigned grid) {
-    return p.norm_w ? launch_decode_d<D, true>(p, grid) : launch_decode_d<D, false>(p, grid);
+    return (p.qk_norm || p.q_scale != 1.f) ? launch_decode_prep<D, true>(p, grid) : launch_decode_prep<D, false>(p, grid);
 }
 
 }  // namespace

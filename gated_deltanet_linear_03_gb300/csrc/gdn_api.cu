@@ -77,7 +77,7 @@ unsigned int *device_error_ptr() {
 
 extern "C" {
 
-int gdn_version(void) { return 101; }
+int gdn_version(void) { return 102; }
 
 const char *gdn_status_string(gdn_status s) {
     switch (s) {
@@ -118,10 +118,13 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
                        const float *init_state,
                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                        void *out, int out_dtype, float *final_state, int qk_norm, float q_scale,
+                       const float *norm_weight, float norm_eps,
                        int algo, void *workspace, size_t workspace_bytes, void *stream, int phases) {
     gdn_status st = check_heads(hk, hv, dk, dv);
     if (st != GDN_OK) return st;
     if ((qk_norm != 0 && qk_norm != 1) || !isfinite(q_scale)) return GDN_ERR_INVALID_ARG;
+    if (norm_weight && (!isfinite(norm_eps) || norm_eps < 0.f)) return GDN_ERR_INVALID_ARG;
+    if (norm_weight && !aligned16(norm_weight)) return GDN_ERR_ALIGNMENT;
     if ((st = check_cu(n_seqs, total_tokens, cu_seqlens_host)) != GDN_OK) return st;
     if (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
     if (algo == GDN_ALGO_AUTO) algo = resolve_auto(n_seqs, hv, dk, cu_seqlens_host);
@@ -172,6 +175,7 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
     p.cu_seqlens = cu_seqlens; p.cu_seqlens_host = cu_seqlens_host;
     p.out = out; p.out_f32 = out_dtype == GDN_DTYPE_F32; p.final_state = final_state;
     p.qk_norm = qk_norm; p.q_scale = q_scale;
+    p.norm_w = norm_weight; p.norm_eps = norm_eps;
     p.workspace = workspace; p.workspace_bytes = workspace_bytes;
     p.err = device_error_ptr();
     p.stream = static_cast<cudaStream_t>(stream);
@@ -202,10 +206,11 @@ gdn_status gdn_prefill(int n_seqs, int total_tokens, int hk, int hv, int dk, int
                        const float *init_state,
                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                        void *out, int out_dtype, float *final_state, int qk_norm, float q_scale,
+                       const float *norm_weight, float norm_eps,
                        int algo, void *workspace, size_t workspace_bytes, void *stream) {
     return prefill_impl(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
-                        cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, algo, workspace,
-                        workspace_bytes, stream, 3);
+                        cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, norm_weight, norm_eps, algo,
+                        workspace, workspace_bytes, stream, 3);
 }
 
 gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
@@ -214,11 +219,12 @@ gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_tokens, in
                                      const float *init_state,
                                      const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                                      void *out, int out_dtype, float *final_state, int qk_norm, float q_scale,
+                                     const float *norm_weight, float norm_eps,
                                      void *workspace, size_t workspace_bytes, void *stream) {
     if (phase != GDN_PHASE_PREP && phase != GDN_PHASE_PASS) return GDN_ERR_INVALID_ARG;
     return prefill_impl(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
-                        cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, GDN_ALGO_CHUNKED, workspace,
-                        workspace_bytes, stream, phase == GDN_PHASE_PREP ? 1 : 2);
+                        cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, norm_weight, norm_eps,
+                        GDN_ALGO_CHUNKED, workspace, workspace_bytes, stream, phase == GDN_PHASE_PREP ? 1 : 2);
 }
 
 gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,

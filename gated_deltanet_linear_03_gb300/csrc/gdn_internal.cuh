@@ -46,6 +46,8 @@ struct PrefillProblem {
     float *final_state;
     int qk_norm;        // L2-normalise q and k head vectors (x / sqrt(|x|^2 + kQkNormEps))
     float q_scale;      // then multiply q by this
+    const float *norm_w;   // fused output normalisation weight [d], or null
+    float norm_eps;
     void *workspace;
     size_t workspace_bytes;
     unsigned int *err;

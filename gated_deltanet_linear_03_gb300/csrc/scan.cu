@@ -20,9 +20,13 @@
 // 64 are scanned (k.q of each token is formed once while staging); outputs are
 // staged and written back as coalesced rows.
 #include "gdn_internal.cuh"
+#include "sm100.cuh"
 
 namespace gdn {
 namespace {
+
+using sm100::cluster_sync;
+using sm100::ld_dsmem_f32;
 
 constexpr int kThreads = 128;
 constexpr int kRows = 16;   // value rows per CTA
@@ -82,14 +86,16 @@ __device__ __forceinline__ void stage_block(ScanSmem<D, PREP> &sm, int buf, long
 }
 
 // PREP: query/key preparation enabled (qk_norm, or q_scale != 1); without it the token loop is the plain one.
-template <int D, bool PREP>
+// NORM: fused output normalisation (launched as a cluster of the head's slices); the plain instantiation
+// carries no cluster code (its presence alone slowed the plain scan by 17%).
+template <int D, bool PREP, bool NORM>
 __global__ void __launch_bounds__(kThreads)
 scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__restrict__ q,
                     const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
                     const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
                     void *__restrict__ out, int out_f32, float *__restrict__ final_state, int qk_norm,
-                    float q_scale) {
+                    float q_scale, const float *__restrict__ norm_w, float norm_eps) {
     constexpr int COLS = D / kTPR;        // state columns per thread
     constexpr int SLICES = D / kRows;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -209,6 +215,32 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
             if (c == 0) sm.o[t][r] = fmaf(alpha, fq * a1, u * a2);
         }
         __syncthreads();
+        if (NORM) {
+            // Output normalisation over the head's d rows, which the SLICES CTAs of this cluster share: each CTA
+            // sums the squares of its 16 rows per token (in kq's space, free until the next block), the totals
+            // meet through distributed shared memory (into this block's la, also free), and the outputs are
+            // scaled in place.
+            float *ps = sm.kq, *tot = sm.la[buf];
+            for (int t = threadIdx.x; t < nt; t += kThreads) {
+                float x = 0.f;
+#pragma unroll
+                for (int j = 0; j < kRows; ++j) x = fmaf(sm.o[t][j], sm.o[t][j], x);
+                ps[t] = x;
+            }
+            cluster_sync();
+            for (int t = threadIdx.x; t < nt; t += kThreads) {
+                float x = 0.f;
+#pragma unroll
+                for (int rk = 0; rk < SLICES; ++rk) x += ld_dsmem_f32(&ps[t], rk);
+                tot[t] = rsqrtf(x * (1.f / D) + norm_eps);
+            }
+            cluster_sync();   // every peer has read ps before the next block rewrites it; tot is complete
+            for (int i = threadIdx.x; i < nt * kRows; i += kThreads) {
+                const int t = i / kRows, j = i % kRows;
+                sm.o[t][j] *= tot[t] * norm_w[row0 + j];
+            }
+            __syncthreads();
+        }
         // write this block's outputs: row-contiguous 32-value pieces
         for (int i = threadIdx.x; i < nt * kRows; i += kThreads) {
             const int t = i / kRows, j = i % kRows;
@@ -227,7 +259,7 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
     }
 }
 
-template <int D, bool PREP>
+template <int D, bool PREP, bool NORM>
 cudaError_t launch_scan_dp(const PrefillProblem &p) {
     const size_t smem = sizeof(ScanSmem<D, PREP>);
     int dev = 0;
@@ -235,21 +267,40 @@ cudaError_t launch_scan_dp(const PrefillProblem &p) {
     if (e != cudaSuccess) return e;
     static bool attr_set[128] = {};
     if (dev < 128 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(scan_prefill_kernel<D, PREP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(scan_prefill_kernel<D, PREP, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
+    // with the output normalisation the D / kRows slices of a head form one cluster
     const unsigned grid = (unsigned)(p.n_seqs * p.hv * (D / kRows));
-    scan_prefill_kernel<D, PREP><<<grid, kThreads, smem, p.stream>>>(
-        p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.out,
-        p.out_f32, p.final_state, p.qk_norm, p.q_scale);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = D / kRows;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = p.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = NORM ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, scan_prefill_kernel<D, PREP, NORM>, p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha,
+                           p.beta, p.init_state, p.cu_seqlens, p.out, p.out_f32, p.final_state, p.qk_norm, p.q_scale,
+                           p.norm_w, p.norm_eps);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int D, bool NORM>
+cudaError_t launch_scan_dn(const PrefillProblem &p) {
+    return (p.qk_norm || p.q_scale != 1.f) ? launch_scan_dp<D, true, NORM>(p) : launch_scan_dp<D, false, NORM>(p);
 }
 
 template <int D>
 cudaError_t launch_scan_d(const PrefillProblem &p) {
-    return (p.qk_norm || p.q_scale != 1.f) ? launch_scan_dp<D, true>(p) : launch_scan_dp<D, false>(p);
+    return p.norm_w ? launch_scan_dn<D, true>(p) : launch_scan_dn<D, false>(p);
 }
 
 }  // namespace

@@ -48,11 +48,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     F = ctypes.c_float
-    lib.gdn_prefill.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, I, P, Z, P]
+    lib.gdn_prefill.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, F, I, P, Z, P]
     lib.gdn_prefill.restype = I
-    lib.gdn_prefill_chunked_phase.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, Z, P]
+    lib.gdn_prefill_chunked_phase.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, F, P, Z, P]
     lib.gdn_prefill_chunked_phase.restype = I
-    lib.gdn_prefill_noalloc.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P]
+    lib.gdn_prefill_noalloc.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, F, P]
     lib.gdn_prefill_noalloc.restype = I
     lib.gdn_prefill_workspace_size.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
     lib.gdn_prefill_workspace_size.restype = Z
@@ -130,11 +130,12 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
             out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
             final_state=True, algo: str = "chunked", workspace: Optional[torch.Tensor] = None,
             cu_seqlens_host: Optional[Sequence[int]] = None, stream=None, qk_norm: bool = False,
-            q_scale: float = 1.0):
+            q_scale: float = 1.0, norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6):
     """Run ``gdn_prefill``.  Returns ``(out, final_state)``.
 
     ``qk_norm`` / ``q_scale``: the in-kernel query/key preparation (every q and k head vector
     L2-normalised, then q multiplied by ``q_scale``); the defaults use q and k as given.
+    ``norm_weight`` (fp32 [dv]): fuse the output normalisation o / sqrt(mean(o^2) + norm_eps) * weight.
 
     ``final_state`` may be ``True`` (allocate), ``False``/``None`` (do not emit)
     or a tensor to write into (it may be ``init_state`` for an in-place update).
@@ -168,8 +169,8 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib.gdn_prefill(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                          _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out), DTYPE[out.dtype],
-                         _ptr(final_state), int(bool(qk_norm)), float(q_scale), ALGO[algo], _ptr(workspace),
-                         ws_bytes, _stream_ptr(stream))
+                         _ptr(final_state), int(bool(qk_norm)), float(q_scale), _ptr(norm_weight),
+                         float(norm_eps), ALGO[algo], _ptr(workspace), ws_bytes, _stream_ptr(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill")
     return out, final_state
@@ -179,7 +180,7 @@ def prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha
                     beta: torch.Tensor, cu_seqlens: torch.Tensor, *, init_state: Optional[torch.Tensor] = None,
                     out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16, final_state=True,
                     cu_seqlens_host: Optional[Sequence[int]] = None, stream=None, qk_norm: bool = False,
-                    q_scale: float = 1.0):
+                    q_scale: float = 1.0, norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6):
     """Run ``gdn_prefill_noalloc``: the chunked prefill using the library's fixed
     scratch instead of a workspace (for callers that cannot allocate device
     memory; see include/gdn.h for its size limit and sharing rules).
@@ -206,7 +207,8 @@ def prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha
     cu_arr, _ = _host_cu(cu_seqlens, cu_seqlens_host)
     st = lib.gdn_prefill_noalloc(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                                  _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out), DTYPE[out.dtype],
-                                 _ptr(final_state), int(bool(qk_norm)), float(q_scale), _stream_ptr(stream))
+                                 _ptr(final_state), int(bool(qk_norm)), float(q_scale), _ptr(norm_weight),
+                                 float(norm_eps), _stream_ptr(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill_noalloc")
     return out, final_state
@@ -219,7 +221,7 @@ class PrefillPlan:
 
     def __init__(self, q, k, v, log_alpha, beta, cu_seqlens, *, init_state=None, out=None,
                  out_dtype=torch.bfloat16, final_state=True, algo="chunked", workspace=None,
-                 cu_seqlens_host=None, qk_norm=False, q_scale=1.0):
+                 cu_seqlens_host=None, qk_norm=False, q_scale=1.0, norm_weight=None, norm_eps=1e-6):
         self.lib = load_library()
         _need(q, "q", torch.bfloat16, 3)
         _need(k, "k", torch.bfloat16, 3)
@@ -248,7 +250,8 @@ class PrefillPlan:
         self.ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
                      self.cu_arr, _ptr(out), DTYPE[out.dtype], _ptr(final_state))
         self.ws = (_ptr(workspace), ws_bytes)
-        self.qk = (int(bool(qk_norm)), float(q_scale))
+        self.qk = (int(bool(qk_norm)), float(q_scale), _ptr(norm_weight), float(norm_eps))
+        self.norm_weight = norm_weight
 
     def run(self, stream=None):
         st = self.lib.gdn_prefill(*self.head, *self.ptrs, *self.qk, self.algo, *self.ws, _stream_ptr(stream))

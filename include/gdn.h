@@ -110,6 +110,11 @@ typedef enum {
  *                    cases q is then multiplied by q_scale (a finite float;
  *                    1/sqrt(dk) for raw projections).  qk_norm = 0, q_scale = 1
  *                    uses q and k exactly as given.
+ *   norm_weight,     fused output normalisation, as for gdn_decode_step: with
+ *   norm_eps         norm_weight (fp32 [dv] device array) each head's output
+ *                    vector o of every token becomes
+ *                    o / sqrt(mean(o^2) + norm_eps) * norm_weight; NULL
+ *                    leaves the outputs as computed.
  *   algo             GDN_ALGO_CHUNKED, GDN_ALGO_SCAN or GDN_ALGO_AUTO
  *   workspace        device scratch of at least gdn_prefill_workspace_size()
  *                    bytes (may be NULL when that size is 0), 256-byte aligned.
@@ -122,7 +127,7 @@ GDN_API gdn_status gdn_prefill(int n_seqs, int total_tokens, int hk, int hv, int
                        const float *init_state,
                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                        void *out, int out_dtype, float *final_state,
-                       int qk_norm, float q_scale,
+                       int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
                        int algo, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -148,7 +153,7 @@ GDN_API gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_to
                                              const float *init_state,
                                              const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                                              void *out, int out_dtype, float *final_state,
-                                             int qk_norm, float q_scale,
+                                             int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
                                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -242,7 +247,8 @@ GDN_API gdn_status gdn_prefill_noalloc(int n_seqs, int total_tokens, int hk, int
                                        const float *init_state,
                                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                                        void *out, int out_dtype, float *final_state,
-                                       int qk_norm, float q_scale, void *stream);
+                                       int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
+                                       void *stream);
 
 /* Static, human-readable name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status status);

@@ -49,12 +49,13 @@ FAKE = 0x10000  # an aligned address that is never dereferenced: validation fail
 def prefill(lib, **kw):
     a = dict(n_seqs=1, T=64, hk=1, hv=2, dk=128, dv=128, q=FAKE, k=FAKE * 2, v=FAKE * 3, la=FAKE * 4,
              b=FAKE * 5, s0=None, cu=FAKE * 6, cu_host=_cu([0, 64]), out=FAKE * 7, odt=0, fin=None,
-             algo=1, ws=None, wsb=0, qkn=0, qs=1.0)
+             algo=1, ws=None, wsb=0, qkn=0, qs=1.0, nw=None, ne=1e-6)
     a.update(kw)
     P = ctypes.c_void_p
     return lib.gdn_prefill(a["n_seqs"], a["T"], a["hk"], a["hv"], a["dk"], a["dv"], P(a["q"]), P(a["k"]),
                            P(a["v"]), P(a["la"]), P(a["b"]), P(a["s0"]), P(a["cu"]), a["cu_host"], P(a["out"]),
-                           a["odt"], P(a["fin"]), a["qkn"], a["qs"], a["algo"], P(a["ws"]), a["wsb"], None)
+                           a["odt"], P(a["fin"]), a["qkn"], a["qs"], P(a["nw"]), a["ne"], a["algo"], P(a["ws"]),
+                           a["wsb"], None)
 
 
 def test_prefill_rejects_bad_heads(lib):
@@ -79,6 +80,8 @@ def test_prefill_rejects_bad_dtype_algo_pointers(lib):
     assert prefill(lib, qkn=2) == 1                 # qk_norm is 0 or 1
     assert prefill(lib, qkn=1, qs=float("inf")) == 1
     assert prefill(lib, qs=float("nan")) == 1
+    assert prefill(lib, nw=FAKE * 50, ne=float("nan")) == 1
+    assert prefill(lib, nw=FAKE * 50 + 8) == 3
     assert prefill(lib, algo=5) == 2
     assert prefill(lib, q=None) == 1
     assert prefill(lib, q=FAKE + 4) == 3          # misaligned

@@ -61,3 +61,57 @@ def test_decode_output_norm_bf16(gdn):
     o_ref, _ = oracle.decode_step(di.state.double().numpy(), *[np32(a) for a in args], norm_weight=w.numpy())
     torch.cuda.synchronize()
     assert bf16_ok(out, o_ref)
+
+
+PREFILL_CASES = {
+    # lengths, algo, d: the chunked pass (cluster of 4 slices, per-chunk exchange, partial last chunks and a
+    # 1-token sequence), the register scan (cluster of d/16 slices, per 64-token block), the streaming scan
+    # (a batch of short sequences: cluster of 4 for d = 128, one CTA per head below)
+    "chunked_ragged": ([200, 1, 64, 130], "chunked", 128),
+    "chunked_T64": ([64], "chunked", 128),
+    "scan_long": ([150, 70], "scan", 128),
+    "scan_single_short": ([8], "scan", 128),
+    "scan_short_batch": ([5, 32, 1, 17, 9, 0, 3, 12], "scan", 128),
+    "scan_long_d64": ([100, 37], "scan", 64),
+    "scan_short_batch_d64": ([5, 2, 17, 9], "scan", 64),
+    "scan_long_d32": ([90, 3], "scan", 32),
+    "scan_short_batch_d32": ([8, 3, 1, 5, 2, 7, 4, 6], "scan", 32),
+}
+
+
+@pytest.mark.parametrize("case", list(PREFILL_CASES))
+@pytest.mark.parametrize("qk_norm", [False, True])
+def test_prefill_with_output_norm(gdn, case, qk_norm):
+    lengths, algo, d = PREFILL_CASES[case]
+    hk, hv = (16, 32) if d == 128 else (8, 32)
+    inp = synth.prefill_inputs(lengths, hk=hk, hv=hv, dk=d, dv=d, seed=64, init_std=0.02, raw_qk=qk_norm)
+    w = weight(d, 65)
+    scale = 1.0 / np.sqrt(d) if qk_norm else 1.0
+    kw = dict(qk_norm=qk_norm, q_scale=scale, norm_weight=w.numpy(), norm_eps=1e-6)
+    from helpers import oracle_args, to_device, check_prefill
+    ref_out, ref_fin = oracle.prefill(*oracle_args(inp), **kw)
+    dv_ = to_device(inp)
+    kw["norm_weight"] = w.cuda()
+    out, fin = gdn.prefill(dv_.q, dv_.k, dv_.v, dv_.log_alpha, dv_.beta, dv_.cu_seqlens, init_state=dv_.init_state,
+                           out_dtype=torch.float32, algo=algo, cu_seqlens_host=inp.cu_seqlens.tolist(), **kw)
+    torch.cuda.synchronize()
+    check_prefill(out, fin, ref_out, ref_fin, what=f"{case} qk_norm={qk_norm}")
+
+
+def test_prefill_output_norm_noalloc_and_phases(gdn):
+    from helpers import oracle_args, to_device, check_prefill
+    inp = synth.prefill_inputs([300, 5], seed=66, init_std=0.02)
+    w = weight(128, 67)
+    ref_out, ref_fin = oracle.prefill(*oracle_args(inp), norm_weight=w.numpy())
+    d = to_device(inp)
+    cu = inp.cu_seqlens.tolist()
+    out, fin = gdn.prefill_noalloc(d.q, d.k, d.v, d.log_alpha, d.beta, d.cu_seqlens, init_state=d.init_state,
+                                   out_dtype=torch.float32, cu_seqlens_host=cu, norm_weight=w.cuda())
+    torch.cuda.synchronize()
+    check_prefill(out, fin, ref_out, ref_fin, what="noalloc norm")
+    plan = gdn.PrefillPlan(d.q, d.k, d.v, d.log_alpha, d.beta, d.cu_seqlens, init_state=d.init_state,
+                           out_dtype=torch.float32, cu_seqlens_host=cu, norm_weight=w.cuda())
+    plan.run_phase("prep")
+    plan.run_phase("pass")
+    torch.cuda.synchronize()
+    check_prefill(plan.out, plan.final_state, ref_out, ref_fin, what="phases norm")
