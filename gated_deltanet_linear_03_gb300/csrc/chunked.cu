@@ -249,6 +249,8 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
     }
 }
 
+// PREP: query/key preparation (qk_norm, or q_scale != 1); the plain instantiation has none of its arithmetic.
+template <bool PREP>
 __global__ void __launch_bounds__(kThreads)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
@@ -329,7 +331,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         }
         mma_commit(&bar_mma);
     }
-    {   // Query/key preparation factors of the 64 k rows (threads 0-63) and 64 q rows (64-127), from the staged
+    if (PREP) {   // Query/key preparation factors of the 64 k rows (threads 0-63) and 64 q rows (64-127), from the staged
         // tiles (which the MMA above only reads).  The products use raw q and k; the factors scale rows and
         // columns of [K;Q]K^T and the rows of P = K^T diag(f_k) Gamma T.  The state pass reads them from the
         // workspace.
@@ -370,7 +372,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     if (ok) ok = mbar_wait(&bar_mma, 0);
     ok = __syncthreads_and(ok);
     tc_fence_after();
-    if (qk_norm && tid < 64) gam_s[tid] *= kf_s[tid];   // P = K^T diag(f_k Gamma) T (read after the solve's barriers)
+    if (PREP && qk_norm && tid < 64) gam_s[tid] *= kf_s[tid];   // P = K^T diag(f_k Gamma) T (read after the solve's barriers)
     {   // T (over the Q rows, which [K;Q]K^T no longer needs) starts at zero; its upper blocks stay zero
         float4 *t0q = reinterpret_cast<float4 *>(sm + PREP_KQ + 8192);
         float4 *t1q = reinterpret_cast<float4 *>(sm + PREP_KQ + 24576);
@@ -406,7 +408,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 }
             }
         }
-        if (qk_norm) {
+        if (PREP && qk_norm) {
 #pragma unroll
             for (int jj = 0; jj < 64; ++jj)
                 if (jj < 32 || !low_rows) vals[jj] *= kf_s[jj];   // column factor f_k,j
@@ -414,7 +416,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         const float gi = g_s[i];
         const bool row_ok = ok && i < L;
         if (warp < 2) {
-            const float bi = b_s[i] * kf_s[i];                  // row factor f_k,i
+            const float bi = PREP ? b_s[i] * kf_s[i] : b_s[i];  // row factor f_k,i
             float *arow = reinterpret_cast<float *>(sm + PREP_A) + i * A_LD;
 #pragma unroll
             for (int jj = 0; jj < 64; jj += 4) {
@@ -432,7 +434,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
                 if (jj < 32 || !low_rows) {
                     float x[8];
-                    const float fqi = qf_s[i];                  // row factor f_q,i
+                    const float fqi = PREP ? qf_s[i] : 1.f;     // row factor f_q,i
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         x[e] = (row_ok && jj + e <= i) ? fqi * __expf(gi - g_s[jj + e]) * vals[jj + e] : 0.f;
@@ -1065,7 +1067,9 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
     if (e != cudaSuccess) return e;
     static bool attrs_set[128] = {};
     if (dev < 128 && !attrs_set[dev]) {
-        e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+        e = cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(state_pass_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
         if (e == cudaSuccess)
@@ -1086,10 +1090,14 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
 
     if ((phases & 1) && nch > 0) {
         dim3 grid((unsigned)nch, (unsigned)p.hv);
-        chunk_prep_kernel<<<grid, kThreads, PREP_SMEM, p.stream>>>(qmap, kmap, phmap, plmap, rhmap, rlmap,
-                                                                   p.log_alpha, p.beta, p.cu_seqlens, p.n_seqs,
-                                                                   p.total_tokens, p.hk, p.hv, norms, p.qk_norm,
-                                                                   p.q_scale, p.err);
+        if (p.qk_norm || p.q_scale != 1.f)
+            chunk_prep_kernel<true><<<grid, kThreads, PREP_SMEM, p.stream>>>(
+                qmap, kmap, phmap, plmap, rhmap, rlmap, p.log_alpha, p.beta, p.cu_seqlens, p.n_seqs, p.total_tokens,
+                p.hk, p.hv, norms, p.qk_norm, p.q_scale, p.err);
+        else
+            chunk_prep_kernel<false><<<grid, kThreads, PREP_SMEM, p.stream>>>(
+                qmap, kmap, phmap, plmap, rhmap, rlmap, p.log_alpha, p.beta, p.cu_seqlens, p.n_seqs, p.total_tokens,
+                p.hk, p.hv, norms, p.qk_norm, p.q_scale, p.err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
