@@ -431,6 +431,90 @@ def time_scan(plan_scan, stream, iters=5):
     return s.elapsed_time(e) / iters
 
 
+def time_plan(plan, stream, iters):
+    """Device time (ms) of one call of a prefill plan: one untimed call, then the mean of `iters`."""
+    import torch
+    with torch.cuda.stream(stream):
+        plan.run(stream=stream)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(iters):
+            plan.run(stream=stream)
+        e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def time_long_context(dev, stream, decode_steps=64):
+    """The 128K-token single-layer prefill (model shape and gates), by the chunked path and by the direct
+    scan on the same inputs, each emitting the final state; then `decode_steps` batch-1 decode steps that
+    continue from the chunked path's final state (one layer, captured in one CUDA graph).  The inputs are
+    drawn on the device (same recipe, its own seed stream): drawing 3 GiB on the host takes minutes."""
+    import torch
+    from gated_deltanet_linear_03_gb300 import gdn, synth
+    T = 131072
+    inp = synth.prefill_inputs([T], seed=1003, device=dev)
+    args = (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.cu_seqlens.to(dev))
+    res = {"workload": "1 sequence x 131072 tokens, 16 q/k heads, 32 v heads, d=128, bf16 q/k/v, "
+                       "final state emitted"}
+    state = None
+    for algo, iters in (("chunked", 5), ("scan", 2)):
+        plan = gdn.PrefillPlan(*args, algo=algo, cu_seqlens_host=[0, T])
+        ms = time_plan(plan, stream, iters)
+        res[algo] = {"ms": ms, "tok_per_s": T / (ms * 1e-3)}
+        if algo == "chunked":
+            state = plan.final_state.clone()
+        del plan
+    res["chunked_over_scan_speedup"] = res["scan"]["ms"] / res["chunked"]["ms"]
+    di = synth.decode_inputs(1, decode_steps, seed=1006, device=dev)
+    out = torch.empty(1, HV, D, dtype=torch.bfloat16, device=dev)
+
+    def step(i):
+        gdn.decode_step(state, di.q[i], di.k[i], di.v[i], di.log_alpha[i], di.beta[i], out=out, stream=stream)
+    work = state.clone()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+    torch.cuda.synchronize()
+    state.copy_(work)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(decode_steps):
+            step(i)
+    with torch.cuda.stream(stream):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        graph.replay()
+        e.record(stream)
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) * 1e3 / decode_steps
+    res["decode_after_prefill"] = {"steps": decode_steps, "us_per_step": us, "tok_per_s": 1e6 / us,
+                                   "launch": f"{decode_steps} single-layer steps in one CUDA graph, "
+                                             "continuing in place from the 128K final state (2 MiB, L2-resident)"}
+    return res
+
+
+def time_ragged(dev, stream, iters=5):
+    """Eight packed sequences, lengths log-uniform in [256, 32768] (seed 1004), nonzero initial states,
+    by the chunked path and by the direct scan (inputs drawn on the device, as for the 128K case)."""
+    from gated_deltanet_linear_03_gb300 import gdn, synth
+    lengths = synth.log_uniform_lengths(8, 256, 32768, 1004)
+    inp = synth.prefill_inputs(lengths, seed=1004, init_std=0.02, device=dev)
+    cu_host = inp.cu_seqlens.tolist()
+    args = (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.cu_seqlens.to(dev))
+    T = cu_host[-1]
+    res = {"workload": f"8 packed sequences {lengths} ({T} tokens), 16 q/k heads, 32 v heads, d=128, "
+                       "initial states ~N(0, 0.02^2)",
+           "auto_picks": gdn.resolve_algo(len(lengths), T, HK, HV, D, D, cu_host)}
+    for algo in ("chunked", "scan"):
+        plan = gdn.PrefillPlan(*args, init_state=inp.init_state, algo=algo, cu_seqlens_host=cu_host)
+        ms = time_plan(plan, stream, iters)
+        res[algo] = {"ms": ms, "tok_per_s": T / (ms * 1e-3)}
+        del plan
+    return res
+
+
 def time_e2e(host, cu_host, dev, stream, steps):
     """Public call with host buffers: H2D inputs, gdn.prefill, D2H outputs + final state, every step."""
     import torch
@@ -553,6 +637,8 @@ def run_gb300(args):
         decode_layer_us = time_decode_per_layer(dev, stream)
         scan_ms = time_scan(plan_scan, stream)
         qk_prep = time_qk_prep(dev, stream)
+        long_ctx = time_long_context(dev, stream)
+        ragged = time_ragged(dev, stream)
     clocks = clk.summary()
     e2e_tps, h2d, d2h = time_e2e(host, cu_host, dev, stream, max(3, min(args.steps, 20)))
     err = gdn.device_error(stream)
@@ -599,6 +685,8 @@ def run_gb300(args):
         "scan": {"tok_per_s": T_TOKENS / (scan_ms * 1e-3), "ms": scan_ms,
                  "fp32_tflops": FLOPS_SCAN * T_TOKENS * HV / (scan_ms * 1e-3) / 1e12},
         "qk_prep": qk_prep,
+        "long_context": long_ctx,
+        "ragged": ragged,
         "e2e": {"value": e2e_units / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,

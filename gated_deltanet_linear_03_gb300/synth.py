@@ -61,8 +61,8 @@ def _unit(x: torch.Tensor) -> torch.Tensor:
 
 
 def _gates(shape, gen, kind: str):
-    z1 = torch.randn(shape, generator=gen)
-    z2 = torch.randn(shape, generator=gen)
+    z1 = torch.randn(shape, generator=gen, device=gen.device)
+    z2 = torch.randn(shape, generator=gen, device=gen.device)
     if kind == "model":
         return -0.5 * F.softplus(z1 + 2.0), torch.sigmoid(z2)
     if kind == "tiny":
@@ -76,12 +76,13 @@ def qkv(T: int, hk: int, hv: int, dk: int, dv: int, gen, *, scale_q: bool = True
     """q, k unit vectors (q scaled by 1/sqrt(dk) when ``scale_q``), v ~ N(0, 1).  With ``raw_qk`` q and k are
     raw projections instead: N(0, 1) entries times a per-vector length drawn from [0.25, 4], for the
     in-kernel query/key preparation to normalise."""
-    q = torch.randn(T, hk, dk, generator=gen)
-    k = torch.randn(T, hk, dk, generator=gen)
-    v = torch.randn(T, hv, dv, generator=gen)
+    dev = gen.device
+    q = torch.randn(T, hk, dk, generator=gen, device=dev)
+    k = torch.randn(T, hk, dk, generator=gen, device=dev)
+    v = torch.randn(T, hv, dv, generator=gen, device=dev)
     if raw_qk:
-        q = q * (0.25 + 3.75 * torch.rand(T, hk, 1, generator=gen))
-        k = k * (0.25 + 3.75 * torch.rand(T, hk, 1, generator=gen))
+        q = q * (0.25 + 3.75 * torch.rand(T, hk, 1, generator=gen, device=dev))
+        k = k * (0.25 + 3.75 * torch.rand(T, hk, 1, generator=gen, device=dev))
         return q, k, v
     q, k = _unit(q), _unit(k)
     if scale_q:
@@ -91,9 +92,11 @@ def qkv(T: int, hk: int, hv: int, dk: int, dv: int, gen, *, scale_q: bool = True
 
 def prefill_inputs(lengths: Sequence[int], *, hk=16, hv=32, dk=128, dv=128, seed=1001,
                    gates="model", init_std: float = 0.0, scale_q: bool = True,
-                   qkv_dtype=torch.bfloat16, raw_qk: bool = False) -> PrefillInputs:
-    """Packed prefill inputs for sequences of the given lengths."""
-    gen = torch.Generator().manual_seed(seed)
+                   qkv_dtype=torch.bfloat16, raw_qk: bool = False, device=None) -> PrefillInputs:
+    """Packed prefill inputs for sequences of the given lengths.  With a CUDA ``device`` the draws come from
+    that device's generator (same recipe and seed, different numbers): for timing large workloads only,
+    never for comparison with the oracle."""
+    gen = torch.Generator(device=device or "cpu").manual_seed(seed)
     T = int(sum(lengths))
     q, k, v = qkv(T, hk, hv, dk, dv, gen, scale_q=scale_q, raw_qk=raw_qk)
     la, b = _gates((T, hv), gen, gates)
@@ -101,7 +104,7 @@ def prefill_inputs(lengths: Sequence[int], *, hk=16, hv=32, dk=128, dv=128, seed
     cu[1:] = torch.cumsum(torch.tensor(list(lengths), dtype=torch.int64), 0).to(torch.int32)
     s0 = None
     if init_std > 0:
-        s0 = torch.randn(len(lengths), hv, dv, dk, generator=gen) * init_std
+        s0 = torch.randn(len(lengths), hv, dv, dk, generator=gen, device=gen.device) * init_std
     return PrefillInputs(q.to(qkv_dtype), k.to(qkv_dtype), v.to(qkv_dtype),
                          la.float().contiguous(), b.float().contiguous(), s0, cu)
 
@@ -114,10 +117,11 @@ def log_uniform_lengths(n: int, lo: int, hi: int, seed: int) -> list:
 
 
 def decode_inputs(n: int, steps: int, *, hk=16, hv=32, dk=128, dv=128, seed=1002,
-                  state_std: float = 0.02, gates="model", raw_qk: bool = False) -> DecodeInputs:
-    """``n`` independent states (one per layer) and ``steps`` tokens of fresh inputs."""
-    gen = torch.Generator().manual_seed(seed)
-    state = torch.randn(n, hv, dv, dk, generator=gen) * state_std
+                  state_std: float = 0.02, gates="model", raw_qk: bool = False, device=None) -> DecodeInputs:
+    """``n`` independent states (one per layer) and ``steps`` tokens of fresh inputs (``device`` as in
+    ``prefill_inputs``)."""
+    gen = torch.Generator(device=device or "cpu").manual_seed(seed)
+    state = torch.randn(n, hv, dv, dk, generator=gen, device=gen.device) * state_std
     q, k, v = qkv(steps * n, hk, hv, dk, dv, gen, raw_qk=raw_qk)
     la, b = _gates((steps * n, hv), gen, gates)
     bf = torch.bfloat16

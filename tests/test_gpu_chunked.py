@@ -13,7 +13,8 @@ import torch
 import oracle
 from gated_deltanet_linear_03_gb300 import synth
 from gated_deltanet_linear_03_gb300.synth import PrefillInputs
-from helpers import as_bf16_inputs, check_prefill, max_abs_err, oracle_args, state_rel_err, to_device
+from helpers import (OUT_ATOL, STATE_RTOL, as_bf16_inputs, check_prefill, max_abs_err, oracle_args,
+                     state_rel_err, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -149,12 +150,51 @@ def sampled_heads(inp: PrefillInputs, heads):
             None if s0 is None else s0.double().numpy())
 
 
-@pytest.mark.parametrize("which", ["long_128k", "ragged_8"])
-def test_full_size_sampled_heads(gdn, which):
-    inp = getattr(synth, which)()
+@pytest.fixture(scope="module")
+def full_size():
+    """The two full-size workloads with the oracle's outputs and final states on three value heads."""
     heads = [0, 17, 31]
-    q, k, v, la, b, cu, s0 = sampled_heads(inp, heads)
-    # each sampled v head with its own q/k head: hk = hv = len(heads)
-    ref_out, ref_fin = oracle.prefill(q, k, v, la, b, cu, s0)
-    out, fin = run(gdn, inp, "chunked")
-    check_prefill(out[:, heads].contiguous(), fin[:, heads].contiguous(), ref_out, ref_fin, what=which)
+    cases = {}
+    for which in ("long_128k", "ragged_8"):
+        inp = getattr(synth, which)()
+        q, k, v, la, b, cu, s0 = sampled_heads(inp, heads)
+        # each sampled v head with its own q/k head: hk = hv = len(heads)
+        cases[which] = (inp, oracle.prefill(q, k, v, la, b, cu, s0))
+    return heads, cases
+
+
+@pytest.mark.parametrize("algo", ["chunked", "scan"])
+@pytest.mark.parametrize("which", ["long_128k", "ragged_8"])
+def test_full_size_sampled_heads(gdn, full_size, which, algo):
+    heads, cases = full_size
+    inp, (ref_out, ref_fin) = cases[which]
+    out, fin = run(gdn, inp, algo)
+    check_prefill(out[:, heads].contiguous(), fin[:, heads].contiguous(), ref_out, ref_fin,
+                  what=f"{which} {algo}")
+
+
+def test_long_128k_then_decode(gdn, full_size):
+    """The long-context case end to end: the 128K-token prefill emits its final state, and 64 batch-1
+    decode steps continue from it in place.  Sampled heads follow the oracle's own continuation from the
+    oracle's final state; both paths' final states agree with each other as well."""
+    heads, cases = full_size
+    inp, (_, ref_fin) = cases["long_128k"]
+    out_c, fin_c = run(gdn, inp, "chunked")
+    _, fin_s = run(gdn, inp, "scan")
+    assert state_rel_err(fin_c[:, heads], ref_fin) <= STATE_RTOL
+    diff = (fin_c - fin_s).flatten(2).norm(dim=-1) / fin_s.flatten(2).norm(dim=-1)
+    assert diff.max().item() <= 2 * STATE_RTOL
+    steps = 64
+    di = synth.decode_inputs(1, steps, seed=1006)
+    qh = [h // (inp.v.shape[1] // inp.q.shape[1]) for h in heads]
+    state = fin_c.clone()
+    ref = np.asarray(ref_fin, np.float64)
+    for t in range(steps):
+        args = (di.q[t], di.k[t], di.v[t], di.log_alpha[t], di.beta[t])
+        o = gdn.decode_step(state, *[x.cuda() for x in args], out_dtype=torch.float32)
+        o_ref, ref = oracle.decode_step(ref, di.q[t][:, qh].float().numpy(), di.k[t][:, qh].float().numpy(),
+                                        di.v[t][:, heads].float().numpy(), di.log_alpha[t][:, heads].numpy(),
+                                        di.beta[t][:, heads].numpy())
+        torch.cuda.synchronize()
+        assert max_abs_err(o[:, heads].contiguous(), o_ref) <= OUT_ATOL, t
+    assert state_rel_err(state[:, heads].contiguous(), ref) <= STATE_RTOL
