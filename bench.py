@@ -20,9 +20,11 @@ Also measured and reported on the same line:
     launch per step and as 30 single-layer launches per step;
   * the direct-scan prefill on the same 4K workload (the scan vs. blocks
     comparison);
-  * e2e: the same prefill metric through the public call with host buffers
-    (pinned host -> device copies of the inputs and device -> host copies of
-    the outputs and final state inside the timed region);
+  * e2e: the same prefill metric through the library's host-buffer call
+    gdn_prefill_host (pinned host -> device copies of the inputs and device ->
+    host copies of the outputs and final state inside the timed region, every
+    step), two calls in flight on two streams so that copies and kernels of
+    consecutive steps overlap; the serial figure (one stream) is reported too;
   * cpu_baseline: the fp64 CPU oracle timed on this host's cores;
   * SM clocks sampled with nvidia-smi while the GPU is under load.
 
@@ -516,38 +518,35 @@ def time_ragged(dev, stream, iters=5):
 
 
 def time_e2e(host, cu_host, dev, stream, steps):
-    """Public call with host buffers: H2D inputs, gdn.prefill, D2H outputs + final state, every step."""
+    """End to end through the library's host-buffer call (gdn_prefill_host): every step copies its inputs
+    from pinned host memory, runs the prefill and copies the outputs and the final state back to pinned host
+    memory.  Pipelined: two plans, each with its own device staging and host outputs, alternate on two
+    streams, so one step's copies run under the other step's kernels (H2D and D2H use separate copy
+    engines).  Also timed serially: one plan on one stream, nothing overlapped."""
     import torch
     from gated_deltanet_linear_03_gb300 import gdn
-    pinned = {k: v.pin_memory() for k, v in host.items()}
-    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    out_h = torch.empty(T_TOKENS, HV, D, dtype=torch.bfloat16).pin_memory()
-    fin_h = torch.empty(1, HV, D, D, dtype=torch.float32).pin_memory()
-    ws = torch.empty(gdn.workspace_size(1, T_TOKENS, HK, HV, D, D, cu_host), dtype=torch.uint8, device=dev)
-    out_d = torch.empty(T_TOKENS, HV, D, dtype=torch.bfloat16, device=dev)
-    fin_d = torch.empty(1, HV, D, D, dtype=torch.float32, device=dev)
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+    ins = [host[k].pin_memory() for k in ("q", "k", "v", "la", "b")]
+    plans = [gdn.HostPrefillPlan(*ins, cu_host, device=dev) for _ in range(2)]
+    streams = [stream, torch.cuda.Stream(dev)]
 
-    def step():
-        for key in dbuf:
-            dbuf[key].copy_(pinned[key], non_blocking=True)
-        gdn.prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["la"], dbuf["b"], dbuf["cu"], out=out_d,
-                    final_state=fin_d, workspace=ws, cu_seqlens_host=cu_host, stream=stream)
-        out_h.copy_(out_d, non_blocking=True)
-        fin_h.copy_(fin_d, non_blocking=True)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
+    def timed(n_streams):
+        for i in range(3):
+            plans[i % n_streams].run(streams[i % n_streams])
         torch.cuda.synchronize()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        for _ in range(steps):
-            step()
-        e.record(stream)
-    torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
-    return T_TOKENS / (ms * 1e-3), h2d, d2h
+        start = torch.cuda.Event(enable_timing=True)
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_streams)]
+        start.record(streams[0])
+        for s in streams[1:n_streams]:
+            s.wait_event(start)
+        for i in range(steps):
+            plans[i % n_streams].run(streams[i % n_streams])
+        for e, s in zip(ends, streams):
+            e.record(s)
+        torch.cuda.synchronize()
+        return max(start.elapsed_time(e) for e in ends) / steps
+    ms_pipe = timed(2)
+    ms_serial = timed(1)
+    return T_TOKENS / (ms_pipe * 1e-3), T_TOKENS / (ms_serial * 1e-3), plans[0].h2d_bytes, plans[0].d2h_bytes
 
 
 def cpu_baseline(budget_s: float = 20.0):
@@ -640,7 +639,7 @@ def run_gb300(args):
         long_ctx = time_long_context(dev, stream)
         ragged = time_ragged(dev, stream)
     clocks = clk.summary()
-    e2e_tps, h2d, d2h = time_e2e(host, cu_host, dev, stream, max(3, min(args.steps, 20)))
+    e2e_tps, e2e_serial_tps, h2d, d2h = time_e2e(host, cu_host, dev, stream, max(4, min(args.steps, 20)))
     err = gdn.device_error(stream)
 
     seconds, units = aggregate(total_ms * 1e-3, float(T_TOKENS * args.steps))
@@ -687,7 +686,9 @@ def run_gb300(args):
         "qk_prep": qk_prep,
         "long_context": long_ctx,
         "ragged": ragged,
-        "e2e": {"value": e2e_units / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_units / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "gdn_prefill_host (pinned host inputs and outputs), two plans alternated on two streams",
+                "serial_value": e2e_serial_tps},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "device_error": err,

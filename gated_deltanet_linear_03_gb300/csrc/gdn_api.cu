@@ -77,7 +77,7 @@ unsigned int *device_error_ptr() {
 
 extern "C" {
 
-int gdn_version(void) { return 102; }
+int gdn_version(void) { return 103; }
 
 const char *gdn_status_string(gdn_status s) {
     switch (s) {
@@ -225,6 +225,114 @@ gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_tokens, in
     return prefill_impl(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
                         cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, norm_weight, norm_eps,
                         GDN_ALGO_CHUNKED, workspace, workspace_bytes, stream, phase == GDN_PHASE_PREP ? 1 : 2);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Device staging area of gdn_prefill_host: every piece starts on a 256-byte boundary, the workspace last.
+struct HostStaging {
+    size_t q, k, v, la, b, init, cu, out, fin, ws, total;
+    size_t q_n, v_n, g_n, state_n, cu_n, out_n, ws_n;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+HostStaging host_staging(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv, const int32_t *cu_host,
+                         int out_dtype, bool with_init, bool with_final, int algo) {
+    HostStaging s{};
+    const size_t T = (size_t)total_tokens;
+    s.q_n = T * hk * dk * 2;
+    s.v_n = T * hv * dv * 2;
+    s.g_n = T * hv * 4;
+    s.state_n = (size_t)n_seqs * hv * dv * dk * 4;
+    s.cu_n = (size_t)(n_seqs + 1) * 4;
+    s.out_n = T * hv * dv * (out_dtype == GDN_DTYPE_F32 ? 4 : 2);
+    s.ws_n = algo == GDN_ALGO_CHUNKED ? gdn::chunked_workspace_bytes(n_seqs, cu_host, hv, dk) : 0;
+    size_t at = 0;
+    s.q = at; at += round256(s.q_n);
+    s.k = at; at += round256(s.q_n);
+    s.v = at; at += round256(s.v_n);
+    s.la = at; at += round256(s.g_n);
+    s.b = at; at += round256(s.g_n);
+    s.init = at; at += with_init ? round256(s.state_n) : 0;
+    s.cu = at; at += round256(s.cu_n);
+    s.out = at; at += round256(s.out_n);
+    s.fin = at; at += with_final ? round256(s.state_n) : 0;
+    s.ws = at; at += round256(s.ws_n);
+    s.total = at;
+    return s;
+}
+
+// Shape, option and algorithm checks shared by the two host-buffer calls; resolves GDN_ALGO_AUTO.
+gdn_status check_host_problem(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv, const int32_t *cu_host,
+                              int out_dtype, int &algo) {
+    gdn_status st = check_heads(hk, hv, dk, dv);
+    if (st == GDN_OK) st = check_cu(n_seqs, total_tokens, cu_host);
+    if (st != GDN_OK) return st;
+    if (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
+    if (algo == GDN_ALGO_AUTO) algo = resolve_auto(n_seqs, hv, dk, cu_host);
+    if (algo != GDN_ALGO_CHUNKED && algo != GDN_ALGO_SCAN) return GDN_ERR_UNSUPPORTED;
+    if (algo == GDN_ALGO_CHUNKED && dk != gdn::kChunkedHeadDim) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_prefill_host_staging_size(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                                     const int32_t *cu_seqlens_host, int out_dtype, int with_init_state,
+                                     int with_final_state, int algo, gdn_status *status) {
+    gdn_status st = check_host_problem(n_seqs, total_tokens, hk, hv, dk, dv, cu_seqlens_host, out_dtype, algo);
+    if (status) *status = st;
+    if (st != GDN_OK) return 0;
+    return host_staging(n_seqs, total_tokens, hk, hv, dk, dv, cu_seqlens_host, out_dtype, with_init_state != 0,
+                        with_final_state != 0, algo)
+        .total;
+}
+
+gdn_status gdn_prefill_host(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                            const void *q_host, const void *k_host, const void *v_host,
+                            const float *log_alpha_host, const float *beta_host, const float *init_state_host,
+                            const int32_t *cu_seqlens_host, void *out_host, int out_dtype, float *final_state_host,
+                            int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
+                            int algo, void *staging, size_t staging_bytes, void *stream) {
+    gdn_status st = check_host_problem(n_seqs, total_tokens, hk, hv, dk, dv, cu_seqlens_host, out_dtype, algo);
+    if (st != GDN_OK) return st;
+    if ((qk_norm != 0 && qk_norm != 1) || !isfinite(q_scale)) return GDN_ERR_INVALID_ARG;
+    if (norm_weight && (!isfinite(norm_eps) || norm_eps < 0.f)) return GDN_ERR_INVALID_ARG;
+    if (norm_weight && !aligned16(norm_weight)) return GDN_ERR_ALIGNMENT;
+    if (total_tokens > 0 && (!q_host || !k_host || !v_host || !log_alpha_host || !beta_host || !out_host))
+        return GDN_ERR_INVALID_ARG;
+    const HostStaging s = host_staging(n_seqs, total_tokens, hk, hv, dk, dv, cu_seqlens_host, out_dtype,
+                                       init_state_host != nullptr, final_state_host != nullptr, algo);
+    if (!staging || staging_bytes < s.total) return GDN_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(staging) & 255u) return GDN_ERR_ALIGNMENT;
+    if (total_tokens == 0 && !final_state_host) return GDN_OK;
+
+    uint8_t *base = static_cast<uint8_t *>(staging);
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const struct { size_t off; const void *src; size_t n; } in[] = {
+        {s.q, q_host, s.q_n}, {s.k, k_host, s.q_n}, {s.v, v_host, s.v_n}, {s.la, log_alpha_host, s.g_n},
+        {s.b, beta_host, s.g_n}, {s.init, init_state_host, s.state_n}, {s.cu, cu_seqlens_host, s.cu_n}};
+    for (const auto &c : in)
+        if (c.src && c.n && cudaMemcpyAsync(base + c.off, c.src, c.n, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+            return GDN_ERR_CUDA;
+    st = prefill_impl(n_seqs, total_tokens, hk, hv, dk, dv, base + s.q, base + s.k, base + s.v,
+                      reinterpret_cast<const float *>(base + s.la), reinterpret_cast<const float *>(base + s.b),
+                      init_state_host ? reinterpret_cast<const float *>(base + s.init) : nullptr,
+                      reinterpret_cast<const int32_t *>(base + s.cu), cu_seqlens_host, base + s.out, out_dtype,
+                      final_state_host ? reinterpret_cast<float *>(base + s.fin) : nullptr, qk_norm, q_scale,
+                      norm_weight, norm_eps, algo, s.ws_n ? base + s.ws : nullptr, s.ws_n, stream, 3);
+    if (st != GDN_OK) return st;
+    if (s.out_n && cudaMemcpyAsync(out_host, base + s.out, s.out_n, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (final_state_host &&
+        cudaMemcpyAsync(final_state_host, base + s.fin, s.state_n, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    return GDN_OK;
 }
 
 gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,

@@ -23,7 +23,8 @@ DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 
 # every symbol include/gdn.h declares
 EXPORTS = ("gdn_prefill", "gdn_prefill_chunked_phase", "gdn_prefill_workspace_size", "gdn_decode_step",
-           "gdn_device_error", "gdn_status_string", "gdn_version", "gdn_prefill_noalloc", "gdn_prefill_algo")
+           "gdn_device_error", "gdn_status_string", "gdn_version", "gdn_prefill_noalloc", "gdn_prefill_algo",
+           "gdn_prefill_host", "gdn_prefill_host_staging_size")
 NOALLOC_SCRATCH_BYTES = 97 * 1024 * 1024
 PHASE = {"prep": 1, "pass": 2}
 
@@ -56,6 +57,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdn_prefill_noalloc.restype = I
     lib.gdn_prefill_workspace_size.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
     lib.gdn_prefill_workspace_size.restype = Z
+    lib.gdn_prefill_host.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, I, P, I, F, P, F, I, P, Z, P]
+    lib.gdn_prefill_host.restype = I
+    lib.gdn_prefill_host_staging_size.argtypes = [I, I, I, I, I, I, P, I, I, I, I, ctypes.POINTER(I)]
+    lib.gdn_prefill_host_staging_size.restype = Z
     lib.gdn_prefill_algo.argtypes = [I, I, I, I, I, I, P]
     lib.gdn_prefill_algo.restype = I
     lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, I, ctypes.c_float, P, ctypes.c_float, P]
@@ -212,6 +217,100 @@ def prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill_noalloc")
     return out, final_state
+
+
+def _need_host(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def host_staging_size(n_seqs: int, total_tokens: int, hk: int, hv: int, dk: int, dv: int,
+                      cu_seqlens_host: Sequence[int], out_dtype=torch.bfloat16, init_state: bool = False,
+                      final_state: bool = True, algo: str = "chunked") -> int:
+    """Bytes of device staging ``gdn_prefill_host`` needs for this problem."""
+    lib = load_library()
+    arr = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+    st = ctypes.c_int(0)
+    n = lib.gdn_prefill_host_staging_size(n_seqs, total_tokens, hk, hv, dk, dv, arr, DTYPE[out_dtype],
+                                          int(bool(init_state)), int(bool(final_state)), ALGO[algo],
+                                          ctypes.byref(st))
+    if st.value != GDN_OK:
+        raise GdnError(st.value, "gdn_prefill_host_staging_size")
+    return int(n)
+
+
+class HostPrefillPlan:
+    """Pre-marshalled arguments of one ``gdn_prefill_host`` problem: inputs and outputs in host memory, the
+    copies and the kernels enqueued by the library on one stream.  ``out`` and ``final_state`` are
+    allocated here in page-locked host memory unless passed in; ``staging`` is allocated on ``device``
+    unless passed in.  ``run`` only enqueues: synchronise the stream before reading the outputs or changing
+    the inputs.  Two plans with their own staging, run alternately on two streams, overlap one call's
+    copies with the other's kernels."""
+
+    def __init__(self, q, k, v, log_alpha, beta, cu_seqlens_host, *, init_state=None, out=None,
+                 out_dtype=torch.bfloat16, final_state=True, algo="chunked", staging=None, device=None,
+                 qk_norm=False, q_scale=1.0, norm_weight=None, norm_eps=1e-6):
+        self.lib = load_library()
+        _need_host(q, "q", torch.bfloat16, 3)
+        _need_host(k, "k", torch.bfloat16, 3)
+        _need_host(v, "v", torch.bfloat16, 3)
+        _need_host(log_alpha, "log_alpha", torch.float32, 2)
+        _need_host(beta, "beta", torch.float32, 2)
+        if init_state is not None:
+            _need_host(init_state, "init_state", torch.float32, 4)
+        if norm_weight is not None:
+            _need(norm_weight, "norm_weight", torch.float32, 1)
+        T, hk, dk = q.shape
+        hv, dv = v.shape[1], v.shape[2]
+        cu_vals = [int(x) for x in (cu_seqlens_host.tolist() if isinstance(cu_seqlens_host, torch.Tensor)
+                                    else cu_seqlens_host)]
+        n_seqs = len(cu_vals) - 1
+        self.cu_arr = (ctypes.c_int32 * len(cu_vals))(*cu_vals)
+        if out is None:
+            out = torch.empty(T, hv, dv, dtype=out_dtype, pin_memory=True)
+        _need_host(out, "out", out.dtype, 3)
+        if final_state is True:
+            final_state = torch.empty(n_seqs, hv, dv, dk, dtype=torch.float32, pin_memory=True)
+        elif final_state is False:
+            final_state = None
+        if final_state is not None:
+            _need_host(final_state, "final_state", torch.float32, 4)
+        need = host_staging_size(n_seqs, T, hk, hv, dk, dv, cu_vals, out.dtype, init_state is not None,
+                                 final_state is not None, algo)
+        if staging is None:
+            staging = torch.empty(need, dtype=torch.uint8, device=device or torch.device("cuda"))
+        self.out, self.final_state, self.staging = out, final_state, staging
+        self.tensors = (q, k, v, log_alpha, beta, init_state, norm_weight)
+        self.head = (n_seqs, T, hk, hv, dk, dv)
+        self.ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state), self.cu_arr,
+                     _ptr(out), DTYPE[out.dtype], _ptr(final_state))
+        self.qk = (int(bool(qk_norm)), float(q_scale), _ptr(norm_weight), float(norm_eps))
+        self.tail = (ALGO[algo], _ptr(staging), staging.numel() * staging.element_size())
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, log_alpha, beta, init_state)
+                             if t is not None) + 4 * len(cu_vals)
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in (out, final_state) if t is not None)
+
+    def run(self, stream=None):
+        st = self.lib.gdn_prefill_host(*self.head, *self.ptrs, *self.qk, *self.tail, _stream_ptr(stream))
+        if st != GDN_OK:
+            raise GdnError(st, "gdn_prefill_host")
+        return self.out, self.final_state
+
+
+def prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.Tensor, beta: torch.Tensor,
+                 cu_seqlens_host, *, stream=None, **kw):
+    """Run ``gdn_prefill_host`` once on host tensors and wait for it: returns ``(out, final_state)`` in host
+    memory.  Keyword arguments as for ``HostPrefillPlan``."""
+    plan = HostPrefillPlan(q, k, v, log_alpha, beta, cu_seqlens_host, **kw)
+    plan.run(stream)
+    (stream or torch.cuda.current_stream()).synchronize()
+    return plan.out, plan.final_state
 
 
 class PrefillPlan:

@@ -250,6 +250,47 @@ GDN_API gdn_status gdn_prefill_noalloc(int n_seqs, int total_tokens, int hk, int
                                        int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
                                        void *stream);
 
+/*
+ * gdn_prefill_host: gdn_prefill on inputs and outputs in HOST memory, for
+ * callers whose prompts arrive in host memory and whose results go back there.
+ * Enqueued on `stream`, in this order:
+ *   1. copies of q_host, k_host, v_host, log_alpha_host, beta_host,
+ *      init_state_host (when not NULL) and cu_seqlens_host into `staging`;
+ *   2. gdn_prefill on those device copies, with its workspace also taken from
+ *      `staging`;
+ *   3. copies of the outputs back into out_host and, when not NULL,
+ *      final_state_host.
+ * Shapes, dtypes, options and errors are those of gdn_prefill; the host arrays
+ * are dense with gdn_prefill's layouts and need no particular alignment.
+ * norm_weight, when given, is a DEVICE array (a model parameter that stays
+ * resident).  init_state_host NULL means zero initial states; final_state_host
+ * NULL skips the final states.
+ *
+ *   staging        device memory of at least gdn_prefill_host_staging_size()
+ *                  bytes for the same problem, 256-byte aligned, owned by the
+ *                  caller and used by the call until its step 3 has finished
+ *                  on the stream.  Its contents on entry do not matter.
+ *
+ * The host arrays must stay valid, and the inputs unchanged, until the stream
+ * has executed the copies that read or write them.  With page-locked (pinned)
+ * host memory the call returns without waiting and the copies run
+ * asynchronously, so calls alternated between two streams, each with its own
+ * staging, overlap one call's copies with the other's kernels.  With pageable
+ * host memory the CUDA runtime may complete the copies synchronously.  All
+ * arguments are validated before anything is enqueued.
+ */
+GDN_API size_t gdn_prefill_host_staging_size(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                                             const int32_t *cu_seqlens_host, int out_dtype, int with_init_state,
+                                             int with_final_state, int algo, gdn_status *status);
+
+GDN_API gdn_status gdn_prefill_host(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                                    const void *q_host, const void *k_host, const void *v_host,
+                                    const float *log_alpha_host, const float *beta_host,
+                                    const float *init_state_host, const int32_t *cu_seqlens_host,
+                                    void *out_host, int out_dtype, float *final_state_host,
+                                    int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
+                                    int algo, void *staging, size_t staging_bytes, void *stream);
+
 /* Static, human-readable name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status status);
 

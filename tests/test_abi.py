@@ -164,3 +164,73 @@ def test_auto_workspace_matches_resolved_algo(lib):
 def test_auto_requires_workspace_only_when_chunked(lib):
     # 200 tokens resolves to the chunked path, which needs a workspace
     assert prefill(lib, T=200, cu_host=_cu([0, 200]), algo=2, ws=None, wsb=0) == 7
+
+
+# gdn_prefill_host: the staging layout and the checks made before anything is enqueued
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def host_size(lib, T=64, n=1, hk=1, hv=2, d=128, odt=0, init=0, fin=1, algo=0, cu=None):
+    st = ctypes.c_int(-1)
+    cu = cu or _cu([0, T])
+    size = lib.gdn_prefill_host_staging_size(n, T, hk, hv, d, d, cu, odt, init, fin, algo, ctypes.byref(st))
+    return size, st.value
+
+
+def test_host_staging_size_is_the_sum_of_its_pieces(lib):
+    T, n, hk, hv, d = 200, 2, 2, 4, 128
+    cu = _cu([0, 150, 200])
+    st = ctypes.c_int(-1)
+    ws = lib.gdn_prefill_workspace_size(n, T, hk, hv, d, d, cu, 0, ctypes.byref(st))
+    assert st.value == 0 and ws > 0
+    state = n * hv * d * d * 4
+    for odt, ob in ((0, 2), (1, 4)):
+        for init in (0, 1):
+            for fin in (0, 1):
+                expect = (2 * _r256(T * hk * d * 2) + _r256(T * hv * d * 2) + 2 * _r256(T * hv * 4)
+                          + init * _r256(state) + _r256((n + 1) * 4) + _r256(T * hv * d * ob)
+                          + fin * _r256(state) + _r256(ws))
+                size, s = host_size(lib, T, n, hk, hv, d, odt, init, fin, 0, cu)
+                assert s == 0 and size == expect, (odt, init, fin)
+    size, s = host_size(lib, T, n, hk, hv, d, 0, 0, 1, 1, cu)   # the scan needs no workspace
+    assert s == 0 and size == (2 * _r256(T * hk * d * 2) + _r256(T * hv * d * 2) + 2 * _r256(T * hv * 4)
+                               + _r256((n + 1) * 4) + _r256(T * hv * d * 2) + _r256(state))
+
+
+def test_host_staging_size_rejects_invalid_problems(lib):
+    assert host_size(lib, hk=3, hv=4) == (0, 1)
+    assert host_size(lib, d=64, algo=0) == (0, 2)          # chunked path implements d = 128 only
+    assert host_size(lib, odt=5) == (0, 2)
+    assert host_size(lib, cu=_cu([0, 63])) == (0, 1)
+    assert host_size(lib, algo=9) == (0, 2)
+
+
+def prefill_host(lib, **kw):
+    a = dict(n_seqs=1, T=64, hk=1, hv=2, dk=128, dv=128, q=FAKE, k=FAKE, v=FAKE, la=FAKE, b=FAKE, s0=None,
+             cu_host=_cu([0, 64]), out=FAKE, odt=0, fin=FAKE, qkn=0, qs=1.0, nw=None, ne=1e-6, algo=0,
+             stg=FAKE * 16, stgb=1 << 40)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.gdn_prefill_host(a["n_seqs"], a["T"], a["hk"], a["hv"], a["dk"], a["dv"], P(a["q"]), P(a["k"]),
+                                P(a["v"]), P(a["la"]), P(a["b"]), P(a["s0"]), a["cu_host"], P(a["out"]), a["odt"],
+                                P(a["fin"]), a["qkn"], a["qs"], P(a["nw"]), a["ne"], a["algo"], P(a["stg"]),
+                                a["stgb"], None)
+
+
+def test_prefill_host_validates_before_enqueueing(lib):
+    need, s = host_size(lib)
+    assert s == 0
+    assert prefill_host(lib, stgb=need - 1) == 7            # staging too small
+    assert prefill_host(lib, stg=None) == 7
+    assert prefill_host(lib, stg=FAKE * 16 + 128) == 3      # staging not 256-byte aligned
+    assert prefill_host(lib, q=None) == 1
+    assert prefill_host(lib, out=None) == 1
+    assert prefill_host(lib, qkn=2) == 1
+    assert prefill_host(lib, qs=float("nan")) == 1
+    assert prefill_host(lib, nw=FAKE + 4) == 3              # norm_weight is a 16-byte aligned device array
+    assert prefill_host(lib, nw=FAKE, ne=-1.0) == 1
+    assert prefill_host(lib, odt=3) == 2
+    assert prefill_host(lib, hk=3, hv=4) == 1
+    assert prefill_host(lib, cu_host=_cu([0, 65])) == 1
+    assert prefill_host(lib, T=0, cu_host=_cu([0, 0]), fin=None) == 0   # nothing to do: returns at once
