@@ -42,7 +42,6 @@ using namespace sm100;
 constexpr int D = 128;          // head size of the chunked path
 constexpr int C = kChunk;       // 64 tokens per chunk
 constexpr int DS = 32;          // value rows per state-passing CTA
-constexpr int kThreads = 128;
 constexpr uint32_t kSW = kLayoutSwizzle128B;
 
 constexpr size_t kPTile = (size_t)D * C * 2;     // P_hi or P_lo of one (chunk, head): 16 KiB
@@ -88,8 +87,11 @@ __device__ int first_chunk_of(const int32_t *cu, int n, int total) {
     return acc;
 }
 
+// The next 1 KiB boundary of a dynamic shared-memory pointer.  Pointer arithmetic (no integer round trip)
+// keeps the shared address space visible to the compiler, so accesses through the result compile to
+// shared-memory instructions instead of generic ones.
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -160,44 +162,68 @@ __device__ __forceinline__ float *t_row(uint8_t *sm, int ii) {
     return reinterpret_cast<float *>(sm + PREP_KQ + (ii < 32 ? 8192 : 24576)) + (ii & 31) * 64;
 }
 
-// T = (I + A)^-1 for the strictly lower fp32 A (row stride A_LD), by 16 x 16 blocks, all 128 threads:
-//   diagonal blocks  T_II = (I + A_II)^-1            forward substitution, one column per thread
-//   below them       T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ   level by level in I (J < I in parallel)
+constexpr int kPrepThreads = 256;   // 8 warps: warps w and w + 4 share TMEM lane quadrant w % 4
+
+// T = (I + A)^-1 for the strictly lower fp32 A (row stride A_LD), by 16 x 16 blocks, kPrepThreads threads:
+//   diagonal blocks  T_II = (I + A_II)^-1      forward substitution by threads 0-127, two per column: the
+//                                              first takes rows 0-7 of its block, the second rows 8-15
+//                                              once those are in shared memory
+//   below them       T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ   level by level in I; threads 0-127 take the
+//                                              blocks of even J, threads 128-255 those of odd J
 // In the block products each thread owns a strip of two adjacent columns of one row: four consecutive
 // elements of the left factor come in one 16-byte load (the same address for the lanes of a row) and each
 // row of the right factor in one 8-byte load, so a pair of FMAs costs about one shared-memory load.
 // T must be zero on entry.  Ends with the block synchronised.
 __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict__ A, uint8_t *sm,
                                                          float *__restrict__ Y, int tid) {
-    if (tid < 64) {
-        const int j = tid, b = j >> 4, jj = j & 15;
+    {
+        const int j = tid & 63, second = (tid >> 6) & 1, b = j >> 4, jj = j & 15;
         const float *Ab = A + (16 * b) * A_LD + 16 * b;
-        float tc[16];
+        float tc[8];
 #pragma unroll
-        for (int ii = 0; ii < 16; ++ii) {
-            float acc[4] = {(ii == jj) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+        for (int r = 0; r < 8; ++r) tc[r] = (8 * second + r == jj) ? 1.f : 0.f;
+        if (tid < 64) {   // rows 0-7: right-looking, row k final before rows below subtract A[r][k] T[k]
 #pragma unroll
-            for (int k4 = 0; k4 < ii; k4 += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(Ab + ii * A_LD + k4);
-                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+            for (int k = 0; k < 7; ++k)
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (k4 + e < ii) acc[e] = fmaf(-av[e], tc[k4 + e], acc[e]);
-            }
-            tc[ii] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                for (int r = k + 1; r < 8; ++r) tc[r] = fmaf(-Ab[r * A_LD + k], tc[k], tc[r]);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) t_row(sm, 16 * b + r)[j] = tc[r];
         }
+        __syncthreads();
+        if (tid >= 64 && tid < 128) {   // rows 8-15: first the terms of rows 0-7, then right-looking
+            float top[8];
 #pragma unroll
-        for (int ii = 0; ii < 16; ++ii) t_row(sm, 16 * b + ii)[j] = tc[ii];
+            for (int r = 0; r < 8; ++r) top[r] = t_row(sm, 16 * b + r)[j];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                float acc0 = tc[r], acc1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; k += 2) {
+                    acc0 = fmaf(-Ab[(8 + r) * A_LD + k], top[k], acc0);
+                    acc1 = fmaf(-Ab[(8 + r) * A_LD + k + 1], top[k + 1], acc1);
+                }
+                tc[r] = acc0 + acc1;
+            }
+#pragma unroll
+            for (int k = 0; k < 7; ++k)
+#pragma unroll
+                for (int r = k + 1; r < 8; ++r) tc[r] = fmaf(-Ab[(8 + r) * A_LD + 8 + k], tc[k], tc[r]);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) t_row(sm, 16 * b + 8 + r)[j] = tc[r];
+        }
     }
     __syncthreads();
+    const int par = tid >> 7, r = (tid >> 3) & 15, c = (tid & 7) * 2;
 #pragma unroll
     for (int I = 1; I < 4; ++I) {
-        // Y_J = sum_{K=J}^{I-1} A_IK T_KJ for J < I: I x 128 two-column strips, I per thread (warp-uniform J)
+        // Y_J = sum_{K=J}^{I-1} A_IK T_KJ for J < I
 #pragma unroll
-        for (int m = 0; m < I; ++m) {
-            const int e = tid + 128 * m, J = e >> 7, r = (e >> 3) & 15, c = (e & 7) * 2;
+        for (int J = 0; J < I; ++J) {
+            if ((J & 1) != par) continue;   // warp-uniform
             const float *arow = A + (16 * I + r) * A_LD;
             float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
+#pragma unroll
             for (int K = J; K < I; ++K) {
                 const float *tb = t_row(sm, 16 * K) + 16 * J + c;   // the 16 rows of block K are contiguous
 #pragma unroll
@@ -222,8 +248,8 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
         __syncthreads();
         // T_IJ = -T_II Y_J
 #pragma unroll
-        for (int m = 0; m < I; ++m) {
-            const int e = tid + 128 * m, J = e >> 7, r = (e >> 3) & 15, c = (e & 7) * 2;
+        for (int J = 0; J < I; ++J) {
+            if ((J & 1) != par) continue;
             float *trow = t_row(sm, 16 * I + r);
             const float *yb = Y + J * 256 + c;
             float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
@@ -251,7 +277,7 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
 
 // PREP: query/key preparation (qk_norm, or q_scale != 1); the plain instantiation has none of its arithmetic.
 template <bool PREP>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kPrepThreads, 3)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
                   const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
@@ -267,11 +293,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     const int h = blockIdx.y;
     const int hq = h / (hv / hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;   // TMEM lane quadrant; which column half the warp takes
     ChunkLoc loc;
     if (!locate_chunk(cu, n_seqs, total, gc, loc)) return;  // uniform for the CTA
     const int t0 = loc.t0, L = loc.len;
     const uint32_t base = smem_u32(sm);
-    const uint32_t tlane = (uint32_t)(32 * warp) << 16;
+    const uint32_t tlane = (uint32_t)(32 * quad) << 16;
 
     if (warp == 0) {
         tmem_alloc(&tmem_slot, PREP_TMEM_COLS);
@@ -331,7 +358,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         }
         mma_commit(&bar_mma);
     }
-    if (PREP) {   // Query/key preparation factors of the 64 k rows (threads 0-63) and 64 q rows (64-127), from the staged
+    if (PREP && tid < 128) {   // Query/key preparation factors of the 64 k rows (threads 0-63) and 64 q rows (64-127), from the staged
         // tiles (which the MMA above only reads).  The products use raw q and k; the factors scale rows and
         // columns of [K;Q]K^T and the rows of P = K^T diag(f_k) Gamma T.  The state pass reads them from the
         // workspace.
@@ -376,73 +403,80 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     {   // T (over the Q rows, which [K;Q]K^T no longer needs) starts at zero; its upper blocks stay zero
         float4 *t0q = reinterpret_cast<float4 *>(sm + PREP_KQ + 8192);
         float4 *t1q = reinterpret_cast<float4 *>(sm + PREP_KQ + 24576);
-        for (int x = tid; x < 512; x += kThreads) {
+        for (int x = tid; x < 512; x += kPrepThreads) {
             t0q[x] = make_float4(0.f, 0.f, 0.f, 0.f);
             t1q[x] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
 
-    // Warps 0-1 build A (fp32) from the K K^T rows; warps 2-3 build the Aqk tiles (split into bf16 hi/lo)
-    // from the Q K^T rows.  Then all warps solve for T and write the T operand tiles.  Rows 0-31 (warps 0
-    // and 2) have nothing left of the diagonal past column 31: they read and decay only columns 0-31.  The
-    // solve never reads A on or above the diagonal, so A is written only below it; the Aqk tiles feed an
-    // MMA and are written in full (zeros above the diagonal).
+    // Quadrants 0-1 build A (fp32) from the K K^T rows, quadrants 2-3 the Aqk tiles (split into bf16 hi/lo)
+    // from the Q K^T rows; the two warps of a quadrant split the columns.  Then all warps solve for T and
+    // write the T operand tiles.  Rows 0-31 have nothing left of the diagonal past column 31: their warps
+    // take 16 columns each of 0-31, those of rows 32-63 32 columns each.  The solve never reads A on or
+    // above the diagonal, so A is written only below it (rows past the chunk's end get zeros through their
+    // row factor); the Aqk tiles feed an MMA and are written in full (zeros above the diagonal).
     {
-        const int i = tid & 63;
-        const bool low_rows = (warp & 1) == 0;   // rows 0-31 (warp-uniform)
-        float vals[64];
+        const int i = 32 * (quad & 1) + lane;
+        const bool low_rows = (quad & 1) == 0;    // rows 0-31 (warp-uniform)
+        const int c0 = low_rows ? 16 * half : 32 * half, ncol = low_rows ? 16 : 32;
+        float vals[32];
         {
             float a16[16], b16[16];
-            tmem_ld16x2(tmem + tlane, tmem + tlane + 16, a16, b16);
+            if (low_rows) {
+                tmem_ld16(tmem + tlane + c0, a16);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                vals[jj] = a16[jj];
-                vals[16 + jj] = b16[jj];
-            }
-            if (!low_rows) {
-                tmem_ld16x2(tmem + tlane + 32, tmem + tlane + 48, a16, b16);
+                for (int jj = 0; jj < 16; ++jj) vals[jj] = a16[jj];
+            } else {
+                tmem_ld16x2(tmem + tlane + c0, tmem + tlane + c0 + 16, a16, b16);
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
-                    vals[32 + jj] = a16[jj];
-                    vals[48 + jj] = b16[jj];
+                    vals[jj] = a16[jj];
+                    vals[16 + jj] = b16[jj];
                 }
             }
         }
         if (PREP && qk_norm) {
 #pragma unroll
-            for (int jj = 0; jj < 64; ++jj)
-                if (jj < 32 || !low_rows) vals[jj] *= kf_s[jj];   // column factor f_k,j
+            for (int jj = 0; jj < 32; ++jj)
+                if (jj < ncol) vals[jj] *= kf_s[c0 + jj];   // column factor f_k,j
         }
         const float gi = g_s[i];
         const bool row_ok = ok && i < L;
-        if (warp < 2) {
-            const float bi = PREP ? b_s[i] * kf_s[i] : b_s[i];  // row factor f_k,i
-            float *arow = reinterpret_cast<float *>(sm + PREP_A) + i * A_LD;
+        if (quad < 2) {
+            const float bi = row_ok ? (PREP ? b_s[i] * kf_s[i] : b_s[i]) : 0.f;   // row factor f_k,i beta_i
+            float *arow = reinterpret_cast<float *>(sm + PREP_A) + i * A_LD + c0;
 #pragma unroll
-            for (int jj = 0; jj < 64; jj += 4) {
-                if (jj >= 32 && low_rows) break;
+            for (int jj = 0; jj < 32; jj += 4) {
+                if (jj >= ncol) break;
                 float4 a;
-                a.x = (row_ok && jj + 0 < i) ? bi * __expf(gi - g_s[jj + 0]) * vals[jj + 0] : 0.f;
-                a.y = (row_ok && jj + 1 < i) ? bi * __expf(gi - g_s[jj + 1]) * vals[jj + 1] : 0.f;
-                a.z = (row_ok && jj + 2 < i) ? bi * __expf(gi - g_s[jj + 2]) * vals[jj + 2] : 0.f;
-                a.w = (row_ok && jj + 3 < i) ? bi * __expf(gi - g_s[jj + 3]) * vals[jj + 3] : 0.f;
+                a.x = (c0 + jj + 0 < i) ? bi * __expf(gi - g_s[c0 + jj + 0]) * vals[jj + 0] : 0.f;
+                a.y = (c0 + jj + 1 < i) ? bi * __expf(gi - g_s[c0 + jj + 1]) * vals[jj + 1] : 0.f;
+                a.z = (c0 + jj + 2 < i) ? bi * __expf(gi - g_s[c0 + jj + 2]) * vals[jj + 2] : 0.f;
+                a.w = (c0 + jj + 3 < i) ? bi * __expf(gi - g_s[c0 + jj + 3]) * vals[jj + 3] : 0.f;
                 *reinterpret_cast<float4 *>(arow + jj) = a;
             }
         } else {
+            const float fqi = row_ok ? (PREP ? qf_s[i] : 1.f) : 0.f;   // row factor f_q,i
 #pragma unroll
-            for (int jj = 0; jj < 64; jj += 8) {
-                uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-                if (jj < 32 || !low_rows) {
-                    float x[8];
-                    const float fqi = PREP ? qf_s[i] : 1.f;     // row factor f_q,i
+            for (int jj = 0; jj < 32; jj += 8) {
+                if (jj >= ncol) break;
+                float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        x[e] = (row_ok && jj + e <= i) ? fqi * __expf(gi - g_s[jj + e]) * vals[jj + e] : 0.f;
-                    split8_bf16(x, hi, lo);
-                }
-                const uint32_t off = sw128_offset(i, jj);
+                for (int e = 0; e < 8; ++e)
+                    x[e] = (c0 + jj + e <= i) ? fqi * __expf(gi - g_s[c0 + jj + e]) * vals[jj + e] : 0.f;
+                uint4 hi, lo;
+                split8_bf16(x, hi, lo);
+                const uint32_t off = sw128_offset(i, c0 + jj);
                 *reinterpret_cast<uint4 *>(sm + PREP_AQK + off) = hi;
                 *reinterpret_cast<uint4 *>(sm + PREP_AQK + 8192 + off) = lo;
+            }
+            if (low_rows) {   // columns 32-63 of rows 0-31 are zero: 16 of them per warp
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint32_t off = sw128_offset(i, 32 + 16 * half + 8 * q);
+                    *reinterpret_cast<uint4 *>(sm + PREP_AQK + off) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(sm + PREP_AQK + 8192 + off) = make_uint4(0, 0, 0, 0);
+                }
             }
         }
     }
@@ -453,20 +487,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     // (A is no longer read: its space takes the (Gamma T)^T tiles.)
 
     // Operand tiles: row j of T^T (for R) and of (Gamma T)^T (for P) is column j of T, split into bf16 hi/lo.
-    // Thread t covers row j = t % 64, columns i in [32 (t / 64), 32 (t / 64) + 32) (the lanes of a warp read
+    // Thread t covers row j = t % 64, columns i in [16 (t / 64), 16 (t / 64) + 16) (the lanes of a warp read
     // 32 consecutive words of a row of T).  T is read into registers first, because the T^T tiles then
     // overwrite it.
     {
-        const int j = tid & 63, i0 = (tid >> 6) * 32;
-        float tv[32];
+        const int j = tid & 63, i0 = (tid >> 6) * 16;
+        float tv[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) tv[e] = t_row(sm, i0 + e)[j];
+        for (int e = 0; e < 16; ++e) tv[e] = t_row(sm, i0 + e)[j];
         __syncthreads();
         if (ok) {
             uint8_t *tth = sm + PREP_KQ + 8192, *ttl = sm + PREP_KQ + 24576;   // over T
             uint8_t *gth = sm + PREP_A, *gtl = sm + PREP_A + 8192;
 #pragma unroll
-            for (int c8 = 0; c8 < 32; c8 += 8) {
+            for (int c8 = 0; c8 < 16; c8 += 8) {
                 float g8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) g8[e] = gam_s[i0 + c8 + e] * tv[c8 + e];
@@ -508,35 +542,35 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     tc_fence_after();
 
     if (ok) {
-        // Stage P (rows d = lane, 64 columns) and R (rows 16*warp + lane for lane < 16, M = 64 accumulator) as
-        // bf16 hi / lo tiles in the same 128B-swizzled layout the TMA maps use, over operand tiles that the
-        // finished MMAs no longer read, then store each tile with one bulk tensor store.
+        // Stage P (rows d = TMEM lane, 64 columns) and R (rows 16 quad + lane for lane < 16, M = 64 accumulator)
+        // as bf16 hi / lo tiles in the same 128B-swizzled layout the TMA maps use, over operand tiles that the
+        // finished MMAs no longer read, then store each tile with one bulk tensor store.  The two warps of a
+        // quadrant take 32 columns each.
         uint8_t *sph = sm + PREP_KQ, *spl = sm + PREP_KQ + 16384;     // 16 KiB each
         uint8_t *srh = sm + PREP_A, *srl = sm + PREP_A + 8192;        // 8 KiB each
-#pragma unroll
-        for (int c = 0; c < 4; c += 2) {
+        const int cb = 32 * half;
+        {
             float a[16], b[16];
-            tmem_ld16x2(tmem + tlane + 64 + c * 16, tmem + tlane + 64 + (c + 1) * 16, a, b);
+            tmem_ld16x2(tmem + tlane + 64 + cb, tmem + tlane + 64 + cb + 16, a, b);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint4 hi, lo;
                 split8_bf16(q < 2 ? a + 8 * q : b + 8 * (q - 2), hi, lo);
-                const uint32_t off = sw128_offset(tid, c * 16 + 8 * q);
+                const uint32_t off = sw128_offset(32 * quad + lane, cb + 8 * q);
                 *reinterpret_cast<uint4 *>(sph + off) = hi;
                 *reinterpret_cast<uint4 *>(spl + off) = lo;
             }
         }
-        const int r = 16 * warp + lane;
-#pragma unroll
-        for (int c = 0; c < 4; c += 2) {
+        {
+            const int r = 16 * quad + lane;
             float a[16], b[16];
-            tmem_ld16x2(tmem + tlane + c * 16, tmem + tlane + (c + 1) * 16, a, b);
+            tmem_ld16x2(tmem + tlane + cb, tmem + tlane + cb + 16, a, b);
             if (lane < 16) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint4 hi, lo;
                     split8_bf16(q < 2 ? a + 8 * q : b + 8 * (q - 2), hi, lo);
-                    const uint32_t off = sw128_offset(r, c * 16 + 8 * q);
+                    const uint32_t off = sw128_offset(r, cb + 8 * q);
                     *reinterpret_cast<uint4 *>(srh + off) = hi;
                     *reinterpret_cast<uint4 *>(srl + off) = lo;
                 }
@@ -1091,11 +1125,11 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
     if ((phases & 1) && nch > 0) {
         dim3 grid((unsigned)nch, (unsigned)p.hv);
         if (p.qk_norm || p.q_scale != 1.f)
-            chunk_prep_kernel<true><<<grid, kThreads, PREP_SMEM, p.stream>>>(
+            chunk_prep_kernel<true><<<grid, kPrepThreads, PREP_SMEM, p.stream>>>(
                 qmap, kmap, phmap, plmap, rhmap, rlmap, p.log_alpha, p.beta, p.cu_seqlens, p.n_seqs, p.total_tokens,
                 p.hk, p.hv, norms, p.qk_norm, p.q_scale, p.err);
         else
-            chunk_prep_kernel<false><<<grid, kThreads, PREP_SMEM, p.stream>>>(
+            chunk_prep_kernel<false><<<grid, kPrepThreads, PREP_SMEM, p.stream>>>(
                 qmap, kmap, phmap, plmap, rhmap, rlmap, p.log_alpha, p.beta, p.cu_seqlens, p.n_seqs, p.total_tokens,
                 p.hk, p.hv, norms, p.qk_norm, p.q_scale, p.err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
