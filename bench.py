@@ -566,9 +566,25 @@ def cpu_baseline(budget_s: float = 20.0):
         if len(times) >= 3 or time.time() - t_start > budget_s:
             break
     t = statistics.median(times)
+    # single core: the same 4K layer once, and the 64-token tiny case (2 heads, d = 32) repeated for ~0.5 s
+    t0 = time.perf_counter()
+    oracle.prefill(*args, n_threads=1)
+    t_one = time.perf_counter() - t0
+    tiny = synth.tiny_case()
+    targs = (tiny.q.float().numpy(), tiny.k.float().numpy(), tiny.v.float().numpy(), tiny.log_alpha.numpy(),
+             tiny.beta.numpy(), tiny.cu_seqlens.numpy())
+    reps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < 0.5:
+        oracle.prefill(*targs, n_threads=1)
+        reps += 1
+    t_tiny = (time.perf_counter() - t0) / reps
     return {"value": T_TOKENS / t, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"full 4096-token layer, all 32 value heads, fp64, median of {len(times)} runs "
-                      f"({t:.2f} s each)"}
+                      f"({t:.2f} s each)",
+            "single_core": {"value": T_TOKENS / t_one, "unit": UNIT, "cores": 1,
+                            "sample": f"the same 4K layer once ({t_one:.2f} s)"},
+            "single_core_tiny": {"value": 64 / t_tiny, "unit": UNIT, "cores": 1,
+                                 "sample": f"64 tokens, 2 heads, d = 32, fp32 inputs, {reps} runs"}}
 
 
 # --------------------------------------------------------------------------- arms
