@@ -153,8 +153,9 @@ constexpr int A_LD = 68;
 constexpr uint32_t PREP_AQK = PREP_A + 64 * A_LD * 4;   // 50176: Aqk hi, Aqk lo tiles [64 x 64] bf16
 constexpr uint32_t PREP_Y = PREP_AQK + 16384;           // fp32 scratch [3][16][16]
 constexpr uint32_t PREP_G = PREP_Y + 3 * 256 * 4;       // g [64], beta [64], Gamma = e^{g_L - g} [64],
-                                                        // then the q/k preparation factors f_k [64], f_q [64]
-constexpr uint32_t PREP_SMEM = PREP_G + 1280 + 1024;    // + alignment slack: 3 CTAs per SM
+                                                        // the q/k preparation factors f_k [64], f_q [64],
+                                                        // then alpha = e^{log_alpha} [64]
+constexpr uint32_t PREP_SMEM = PREP_G + 1536 + 1024;    // + alignment slack: 3 CTAs per SM
 constexpr uint32_t PREP_TMEM_COLS = 128;
 
 // Row ii of T (fp32, 64 columns): rows 0-31 over the Q half of k-block 0, rows 32-63 over that of k-block 1.
@@ -319,6 +320,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     float *b_s = g_s + 64;                                // [64]
     float *gam_s = g_s + 128;                             // [64], 0 past the chunk's end
     float *kf_s = g_s + 192, *qf_s = g_s + 256;           // [64] each: f_k = 1/|k| (or 1), f_q = q_scale/|q| (or q_scale)
+    float *al_s = g_s + 320;                              // [64] per-token decay e^{log_alpha} (1 past the chunk's end)
     // warp 1 loads this chunk's gates now; their cumulative sum is formed while the TMA and MMA run
     float la0 = 0.f, la1 = 0.f, bt0 = 0.f, bt1 = 0.f;
     if (warp == 1) {
@@ -395,6 +397,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         b_s[2 * lane + 1] = bt1;
         gam_s[2 * lane] = 2 * lane < L ? __expf(gl - g2.x) : 0.f;
         gam_s[2 * lane + 1] = 2 * lane + 1 < L ? __expf(gl - g2.y) : 0.f;
+        al_s[2 * lane] = 2 * lane < L ? __expf(fminf(clamp_log_alpha(la0), 0.f)) : 1.f;
+        al_s[2 * lane + 1] = 2 * lane + 1 < L ? __expf(fminf(clamp_log_alpha(la1), 0.f)) : 1.f;
     }
     if (ok) ok = mbar_wait(&bar_mma, 0);
     ok = __syncthreads_and(ok);
@@ -440,7 +444,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             for (int jj = 0; jj < 32; ++jj)
                 if (jj < ncol) vals[jj] *= kf_s[c0 + jj];   // column factor f_k,j
         }
-        const float gi = g_s[i];
+        // Decays e^{g_i - g_j} for this thread's columns, j <= i: one exponential at the highest such column,
+        // then down the row d(i, j - 1) = d(i, j) alpha_j, so that the special-function unit (which shares
+        // the shared-memory instruction queue) runs one exponential per thread instead of one per element.
+        {
+            const int jstar = min(i, c0 + ncol - 1);
+            float dcy = jstar >= c0 ? __expf(g_s[i] - g_s[jstar]) : 0.f;
+#pragma unroll
+            for (int jj = 31; jj >= 0; --jj) {
+                if (jj >= ncol) continue;
+                const int j = c0 + jj;
+                vals[jj] = j <= jstar ? vals[jj] * dcy : 0.f;
+                if (j <= jstar) dcy *= al_s[j];
+            }
+        }
         const bool row_ok = ok && i < L;
         if (quad < 2) {
             const float bi = row_ok ? (PREP ? b_s[i] * kf_s[i] : b_s[i]) : 0.f;   // row factor f_k,i beta_i
@@ -449,10 +466,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             for (int jj = 0; jj < 32; jj += 4) {
                 if (jj >= ncol) break;
                 float4 a;
-                a.x = (c0 + jj + 0 < i) ? bi * __expf(gi - g_s[c0 + jj + 0]) * vals[jj + 0] : 0.f;
-                a.y = (c0 + jj + 1 < i) ? bi * __expf(gi - g_s[c0 + jj + 1]) * vals[jj + 1] : 0.f;
-                a.z = (c0 + jj + 2 < i) ? bi * __expf(gi - g_s[c0 + jj + 2]) * vals[jj + 2] : 0.f;
-                a.w = (c0 + jj + 3 < i) ? bi * __expf(gi - g_s[c0 + jj + 3]) * vals[jj + 3] : 0.f;
+                a.x = (c0 + jj + 0 < i) ? bi * vals[jj + 0] : 0.f;
+                a.y = (c0 + jj + 1 < i) ? bi * vals[jj + 1] : 0.f;
+                a.z = (c0 + jj + 2 < i) ? bi * vals[jj + 2] : 0.f;
+                a.w = (c0 + jj + 3 < i) ? bi * vals[jj + 3] : 0.f;
                 *reinterpret_cast<float4 *>(arow + jj) = a;
             }
         } else {
@@ -462,8 +479,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 if (jj >= ncol) break;
                 float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    x[e] = (c0 + jj + e <= i) ? fqi * __expf(gi - g_s[c0 + jj + e]) * vals[jj + e] : 0.f;
+                for (int e = 0; e < 8; ++e) x[e] = fqi * vals[jj + e];   // zero above the diagonal already
                 uint4 hi, lo;
                 split8_bf16(x, hi, lo);
                 const uint32_t off = sw128_offset(i, c0 + jj);
