@@ -100,15 +100,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return lo | (hi << 16);
 }
 
-// Split 8 floats into bf16 hi and lo parts packed as two 16-byte vectors (x = hi + lo to ~16 bits).
+// Split 8 floats into bf16 hi and lo parts packed as two 16-byte vectors (x = hi + lo to ~16 bits).  hi is
+// x with its low 16 bits dropped (a byte permute, no conversion); x - hi is then exact in fp32 and only lo
+// is rounded to bf16, which bounds the split's relative error by 2^-17.
 __device__ __forceinline__ void split8_bf16(const float *x, uint4 &hi, uint4 &lo) {
     uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 hh = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-        const float2 back = __bfloat1622float2(hh);
-        const __nv_bfloat162 ll = __floats2bfloat162_rn(x[2 * e] - back.x, x[2 * e + 1] - back.y);
-        h[e] = *reinterpret_cast<const uint32_t *>(&hh);
+        const uint32_t a = __float_as_uint(x[2 * e]), b = __float_as_uint(x[2 * e + 1]);
+        h[e] = __byte_perm(a, b, 0x7632);
+        const __nv_bfloat162 ll = __floats2bfloat162_rn(x[2 * e] - __uint_as_float(a & 0xffff0000u),
+                                                        x[2 * e + 1] - __uint_as_float(b & 0xffff0000u));
         l[e] = *reinterpret_cast<const uint32_t *>(&ll);
     }
     hi = make_uint4(h[0], h[1], h[2], h[3]);
