@@ -298,7 +298,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;   // TMEM lane quadrant; which column half the warp takes
     ChunkLoc loc;
-    if (!locate_chunk(cu, n_seqs, total, gc, loc)) return;  // uniform for the CTA
+    if (n_seqs == 1) {   // one sequence (the host checked cu_seqlens = {0, total}): chunk gc starts at 64 gc
+        if (gc * C >= total) return;
+        loc.seq = 0;
+        loc.t0 = gc * C;
+        loc.len = min(C, total - loc.t0);
+    } else if (!locate_chunk(cu, n_seqs, total, gc, loc)) {
+        return;   // uniform for the CTA
+    }
     const int t0 = loc.t0, L = loc.len;
     const uint32_t base = smem_u32(sm);
     const uint32_t tlane = (uint32_t)(32 * quad) << 16;
@@ -559,48 +566,52 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     ok = __syncthreads_and(ok);
     tc_fence_after();
 
+    // Stage P (rows d = TMEM lane, 64 columns), then R (rows 16 quad + lane for lane < 16, M = 64 accumulator),
+    // as bf16 hi / lo tiles in the same 128B-swizzled layout the TMA maps use, over operand tiles that the
+    // finished MMAs no longer read; each tile leaves with one bulk tensor store, P's while R is staged.  The
+    // two warps of a quadrant take 32 columns each.
+    const int cb = 32 * half;
     if (ok) {
-        // Stage P (rows d = TMEM lane, 64 columns) and R (rows 16 quad + lane for lane < 16, M = 64 accumulator)
-        // as bf16 hi / lo tiles in the same 128B-swizzled layout the TMA maps use, over operand tiles that the
-        // finished MMAs no longer read, then store each tile with one bulk tensor store.  The two warps of a
-        // quadrant take 32 columns each.
         uint8_t *sph = sm + PREP_KQ, *spl = sm + PREP_KQ + 16384;     // 16 KiB each
+        float a[16], b[16];
+        tmem_ld16x2(tmem + tlane + 64 + cb, tmem + tlane + 64 + cb + 16, a, b);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 hi, lo;
+            split8_bf16(q < 2 ? a + 8 * q : b + 8 * (q - 2), hi, lo);
+            const uint32_t off = sw128_offset(32 * quad + lane, cb + 8 * q);
+            *reinterpret_cast<uint4 *>(sph + off) = hi;
+            *reinterpret_cast<uint4 *>(spl + off) = lo;
+        }
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (ok && tid == 0) {
+        const int prow = (gc * hv + h) * D;
+        tma_store_2d(&phmap, sm + PREP_KQ, 0, prow);
+        tma_store_2d(&plmap, sm + PREP_KQ + 16384, 0, prow);
+        tma_store_commit();
+    }
+    if (ok) {
         uint8_t *srh = sm + PREP_A, *srl = sm + PREP_A + 8192;        // 8 KiB each
-        const int cb = 32 * half;
-        {
-            float a[16], b[16];
-            tmem_ld16x2(tmem + tlane + 64 + cb, tmem + tlane + 64 + cb + 16, a, b);
+        const int r = 16 * quad + lane;
+        float a[16], b[16];
+        tmem_ld16x2(tmem + tlane + cb, tmem + tlane + cb + 16, a, b);
+        if (lane < 16) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint4 hi, lo;
                 split8_bf16(q < 2 ? a + 8 * q : b + 8 * (q - 2), hi, lo);
-                const uint32_t off = sw128_offset(32 * quad + lane, cb + 8 * q);
-                *reinterpret_cast<uint4 *>(sph + off) = hi;
-                *reinterpret_cast<uint4 *>(spl + off) = lo;
-            }
-        }
-        {
-            const int r = 16 * quad + lane;
-            float a[16], b[16];
-            tmem_ld16x2(tmem + tlane + cb, tmem + tlane + cb + 16, a, b);
-            if (lane < 16) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 hi, lo;
-                    split8_bf16(q < 2 ? a + 8 * q : b + 8 * (q - 2), hi, lo);
-                    const uint32_t off = sw128_offset(r, cb + 8 * q);
-                    *reinterpret_cast<uint4 *>(srh + off) = hi;
-                    *reinterpret_cast<uint4 *>(srl + off) = lo;
-                }
+                const uint32_t off = sw128_offset(r, cb + 8 * q);
+                *reinterpret_cast<uint4 *>(srh + off) = hi;
+                *reinterpret_cast<uint4 *>(srl + off) = lo;
             }
         }
         fence_proxy_async_smem();
     }
     __syncthreads();
     if (ok && tid == 0) {
-        const int prow = (gc * hv + h) * D, rrow = (gc * hv + h) * C;
-        tma_store_2d(&phmap, sm + PREP_KQ, 0, prow);
-        tma_store_2d(&plmap, sm + PREP_KQ + 16384, 0, prow);
+        const int rrow = (gc * hv + h) * C;
         tma_store_2d(&rhmap, sm + PREP_A, 0, rrow);
         tma_store_2d(&rlmap, sm + PREP_A + 8192, 0, rrow);
         tma_store_commit();
@@ -780,10 +791,12 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     const int rowg = row0 + grp * DG;      // first value row of this thread's group
     const uint32_t base = smem_u32(sm);
 
-    int ta, tb;
-    seq_range(cu, n, total, ta, tb);
+    int ta = 0, tb = total, gc0 = 0;   // one sequence: the host checked cu_seqlens = {0, total}
+    if (n_seqs > 1) {
+        seq_range(cu, n, total, ta, tb);
+        gc0 = first_chunk_of(cu, n, total);
+    }
     const int nchunks = (tb - ta + C - 1) / C;
-    const int gc0 = first_chunk_of(cu, n, total);
     bool ok = gc0 + nchunks <= nch;
     if (!ok && tid == 0) raise_error(err, kErrInternal);
     const bool started = ok && nchunks > 0;   // chunk 0's tiles are requested below
