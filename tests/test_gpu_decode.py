@@ -57,3 +57,26 @@ def test_decode_zero_batch_is_noop(gdn):
     g = torch.zeros(0, 32, device="cuda")
     out = gdn.decode_step(st, e, e, v, g, g)
     assert out.shape == (0, 32, 128)
+
+
+def test_decode_30_layers_256_steps(gdn):
+    """The full decode workload: 30 layer states (32 v heads x 128 x 128 fp32), 256 chained steps with fresh
+    bf16 inputs, bf16 outputs.  Three sampled layers follow the oracle through every step; the error must not
+    grow past the tolerance over the chain."""
+    steps = 256
+    di = synth.decode_30(steps=steps)
+    layers = [0, 13, 29]
+    st_gpu = di.state.cuda()
+    q, k, v, la, b = (x.cuda() for x in (di.q, di.k, di.v, di.log_alpha, di.beta))
+    outs = []
+    for s in range(steps):
+        outs.append(gdn.decode_step(st_gpu, q[s], k[s], v[s], la[s], b[s]))
+    torch.cuda.synchronize()
+    st_ref = di.state[layers].double().numpy()
+    worst = 0.0
+    for s in range(steps):
+        args = [np32(x[s][layers]) for x in (di.q, di.k, di.v, di.log_alpha, di.beta)]
+        o_ref, st_ref = oracle.decode_step(st_ref, *args)
+        worst = max(worst, max_abs_err(outs[s][layers], o_ref))
+    assert worst <= OUT_ATOL, worst
+    assert state_rel_err(st_gpu[layers], st_ref) <= STATE_RTOL

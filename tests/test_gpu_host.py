@@ -86,3 +86,16 @@ def test_two_plans_alternated_on_two_streams(gdn):
         assert torch.equal(p.out, ref_out) and torch.equal(p.final_state, ref_fin)
     assert plans[0].h2d_bytes == sum(t.numel() * t.element_size() for t in plans[0].tensors[:6]) + 12
     assert plans[0].d2h_bytes == 345 * 32 * 128 * 2 + 2 * 32 * 128 * 128 * 4
+
+
+def test_host_call_with_query_key_preparation_and_output_norm(gdn):
+    """The host call forwards the in-kernel options: raw q/k normalised in the kernels, output norm fused."""
+    inp = synth.prefill_inputs([150, 90], seed=86, init_std=0.02, raw_qk=True)
+    (q, k, v, la, b), s0 = host_args(inp)
+    w = torch.linspace(0.5, 2.0, 128)
+    scale = 1.0 / np.sqrt(128)
+    out, fin = gdn.prefill_host(q, k, v, la, b, inp.cu_seqlens.tolist(), init_state=s0, out_dtype=torch.float32,
+                                qk_norm=True, q_scale=scale, norm_weight=w.cuda(), norm_eps=1e-6)
+    ref_out, ref_fin = oracle.prefill(*oracle_args(inp), qk_norm=True, q_scale=scale, norm_weight=w.numpy(),
+                                      norm_eps=1e-6)
+    check_prefill(out, fin, ref_out, ref_fin, what="host with options")
