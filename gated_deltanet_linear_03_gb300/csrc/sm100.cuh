@@ -157,6 +157,46 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)
     }
 }
 
+// Two loads of 32 lanes x 8 consecutive 32-bit columns and one wait.
+__device__ __forceinline__ void tmem_ld8x2(uint32_t ta, uint32_t tb, float (&a)[8], float (&b)[8]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(ta), "r"(tb)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        a[i] = __uint_as_float(r[i]);
+        b[i] = __uint_as_float(r[8 + i]);
+    }
+}
+
+// Two loads of N (8 or 16) columns each.
+template <int N>
+__device__ __forceinline__ void tmem_ldx2(uint32_t ta, uint32_t tb, float (&a)[N], float (&b)[N]) {
+    if constexpr (N == 16) {
+        tmem_ld16x2(ta, tb, a, b);
+    } else if constexpr (N == 8) {
+        tmem_ld8x2(ta, tb, a, b);
+    } else {
+        static_assert(N == 32, "8, 16 or 32 columns");
+        float a0[16], a1[16], b0[16], b1[16];
+        tmem_ld16x2(ta, ta + 16, a0, a1);
+        tmem_ld16x2(tb, tb + 16, b0, b1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            a[i] = a0[i];
+            a[16 + i] = a1[i];
+            b[i] = b0[i];
+            b[16 + i] = b1[i];
+        }
+    }
+}
+
 // ------------------------------------------------------------------ MMA
 // Shared-memory matrix descriptor: start address, leading- and stride-byte
 // offsets (all >> 4), descriptor version 1, swizzle mode in bits 61..63.
