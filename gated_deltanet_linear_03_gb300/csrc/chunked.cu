@@ -172,7 +172,8 @@ constexpr int kPrepThreads = 256;   // 8 warps: warps w and w + 4 share TMEM lan
 //                                              first takes rows 0-7 of its block, the second rows 8-15
 //                                              once those are in shared memory
 //   below them       T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ   level by level in I; threads 0-127 take the
-//                                              blocks of even J, threads 128-255 those of odd J
+//                                              blocks of even J, threads 128-255 those of odd J (the sums of
+//                                              the last level are balanced differently)
 // In the block products each thread owns a strip of two adjacent columns of one row: four consecutive
 // elements of the left factor come in one 16-byte load (the same address for the lanes of a row) and each
 // row of the right factor in one 8-byte load, so a pair of FMAs costs about one shared-memory load.
@@ -220,10 +221,12 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
     const int par = tid >> 7, r = (tid >> 3) & 15, c = (tid & 7) * 2;
 #pragma unroll
     for (int I = 1; I < 4; ++I) {
-        // Y_J = sum_{K=J}^{I-1} A_IK T_KJ for J < I
+        // Y_J = sum_{K=J}^{I-1} A_IK T_KJ for J < I (I - J block products); at I = 3 the second half takes
+        // J = 1 and 2 (three products against three for J = 0)
 #pragma unroll
         for (int J = 0; J < I; ++J) {
-            if ((J & 1) != par) continue;   // warp-uniform
+            const int owner = I == 3 ? (J > 0) : (J & 1);
+            if (owner != par) continue;   // warp-uniform
             const float *arow = A + (16 * I + r) * A_LD;
             float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
 #pragma unroll
