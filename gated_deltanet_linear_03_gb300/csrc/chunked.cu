@@ -170,7 +170,8 @@ constexpr int kPrepThreads = 256;   // 8 warps: warps w and w + 4 share TMEM lan
 // T = (I + A)^-1 for the strictly lower fp32 A (row stride A_LD), by 16 x 16 blocks, kPrepThreads threads:
 //   diagonal blocks  T_II = (I + A_II)^-1      forward substitution by threads 0-127, two per column: the
 //                                              first takes rows 0-7 of its block, the second rows 8-15
-//                                              once those are in shared memory
+//                                              once those are in shared memory (rows of A read as 16-byte
+//                                              words)
 //   below them       T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ   level by level in I; threads 0-127 take the
 //                                              blocks of even J, threads 128-255 those of odd J (the sums of
 //                                              the last level are balanced differently)
@@ -186,33 +187,52 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
         float tc[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) tc[r] = (8 * second + r == jj) ? 1.f : 0.f;
-        if (tid < 64) {   // rows 0-7: right-looking, row k final before rows below subtract A[r][k] T[k]
+        if (tid < 64) {   // rows 0-7, left-looking; each row's A entries come as 16-byte loads
 #pragma unroll
-            for (int k = 0; k < 7; ++k)
+            for (int r = 1; r < 8; ++r) {
+                float acc = tc[r];
 #pragma unroll
-                for (int r = k + 1; r < 8; ++r) tc[r] = fmaf(-Ab[r * A_LD + k], tc[k], tc[r]);
+                for (int k4 = 0; k4 < r; k4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r * A_LD + k4);
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (k4 + e < r) acc = fmaf(-av[e], tc[k4 + e], acc);
+                }
+                tc[r] = acc;
+            }
 #pragma unroll
             for (int r = 0; r < 8; ++r) t_row(sm, 16 * b + r)[j] = tc[r];
         }
         __syncthreads();
-        if (tid >= 64 && tid < 128) {   // rows 8-15: first the terms of rows 0-7, then right-looking
+        if (tid >= 64 && tid < 128) {   // rows 8-15: the terms of rows 0-7, then left-looking among themselves
             float top[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) top[r] = t_row(sm, 16 * b + r)[j];
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
+                const float *arow = Ab + (8 + r) * A_LD;
+                const float4 a0 = *reinterpret_cast<const float4 *>(arow);
+                const float4 a1 = *reinterpret_cast<const float4 *>(arow + 4);
                 float acc0 = tc[r], acc1 = 0.f;
+                acc0 = fmaf(-a0.x, top[0], acc0);
+                acc1 = fmaf(-a0.y, top[1], acc1);
+                acc0 = fmaf(-a0.z, top[2], acc0);
+                acc1 = fmaf(-a0.w, top[3], acc1);
+                acc0 = fmaf(-a1.x, top[4], acc0);
+                acc1 = fmaf(-a1.y, top[5], acc1);
+                acc0 = fmaf(-a1.z, top[6], acc0);
+                acc1 = fmaf(-a1.w, top[7], acc1);
 #pragma unroll
-                for (int k = 0; k < 8; k += 2) {
-                    acc0 = fmaf(-Ab[(8 + r) * A_LD + k], top[k], acc0);
-                    acc1 = fmaf(-Ab[(8 + r) * A_LD + k + 1], top[k + 1], acc1);
+                for (int k4 = 0; k4 < r; k4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(arow + 8 + k4);
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (k4 + e < r) acc0 = fmaf(-av[e], tc[k4 + e], acc0);
                 }
                 tc[r] = acc0 + acc1;
             }
-#pragma unroll
-            for (int k = 0; k < 7; ++k)
-#pragma unroll
-                for (int r = k + 1; r < 8; ++r) tc[r] = fmaf(-Ab[(8 + r) * A_LD + 8 + k], tc[k], tc[r]);
 #pragma unroll
             for (int r = 0; r < 8; ++r) t_row(sm, 16 * b + 8 + r)[j] = tc[r];
         }
@@ -536,7 +556,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             for (int c8 = 0; c8 < 16; c8 += 8) {
                 float g8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) g8[e] = gam_s[i0 + c8 + e] * tv[c8 + e];
+                for (int e4 = 0; e4 < 8; e4 += 4) {
+                    const float4 gm = *reinterpret_cast<const float4 *>(gam_s + i0 + c8 + e4);
+                    g8[e4] = gm.x * tv[c8 + e4];
+                    g8[e4 + 1] = gm.y * tv[c8 + e4 + 1];
+                    g8[e4 + 2] = gm.z * tv[c8 + e4 + 2];
+                    g8[e4 + 3] = gm.w * tv[c8 + e4 + 3];
+                }
                 const uint32_t off = sw128_offset(j, i0 + c8);
                 uint4 hi, lo;
                 split8_bf16(tv + c8, hi, lo);
