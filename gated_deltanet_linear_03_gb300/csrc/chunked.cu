@@ -18,13 +18,15 @@
 //        = e^{g_L} S0 + (P X)^T,                    P = K^T diag(e^{g_L-g}) T
 // A, T, R and P depend only on k, q and the gates, so they are computed for
 // every chunk in parallel by `chunk_prep_kernel`; only the X -> state step is
-// sequential over chunks, in `state_pass_kernel`.
+// sequential over chunks, in `state_pass_kernel` (or `state_pass_norm_kernel`
+// when the output normalisation is fused).
 //
 // Tensor-core use (tcgen05.mma, bf16 operands, fp32 accumulation in TMEM,
 // operands staged by TMA in 128B-swizzled shared memory):
-//   prep:  [K;Q] K^T (exact: q/k are bf16), P = K^T (Gamma T) with Gamma T split
-//          into bf16 hi + lo parts, R = Aqk T (single bf16 pass: output path only)
-//   pass:  [Q;K] [S_hi;S_lo]^T, P_hi [X_hi;X_lo]^T + P_lo X_hi^T, R X_hi^T
+//   prep:  [K;Q] K^T (exact: q/k are bf16), P = K^T (Gamma T) and R = Aqk T with
+//          Gamma T, T and Aqk split into bf16 hi + lo parts; P and R are stored
+//          as bf16 hi + lo pairs
+//   pass:  [Q;K] [S_hi;S_lo]^T, (P_hi + P_lo) [X_hi;X_lo]^T, (R_hi + R_lo) [X_hi;X_lo]^T
 // Everything that feeds the carried state is either an exact bf16 input or a
 // value split into two bf16 terms (about 16 significant bits), so the state
 // error stays far below the fp32-state tolerance; the output-only terms use
@@ -660,16 +662,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 }
 
 // ============================================================================
-// Kernel 2: state passing + outputs (sequential over chunks)
+// Kernel 2a: state passing + outputs with the fused output normalisation
+// (sequential over chunks; the four row slices of a head form a cluster)
 // ============================================================================
 // One pipeline stage: Q|K 32 KiB, P_hi 16, P_lo 16, R_hi 16, R_lo 16 KiB (each R tile holds 64 rows
 // loaded per chunk and 64 zero rows, so that R feeds an M = 128 MMA whose upper rows are unused).
 constexpr uint32_t PASS_STAGE = 98304;
 constexpr uint32_t ST_QK = 0, ST_PH = 32768, ST_PL = 49152, ST_RH = 65536, ST_RL = 81920;
 constexpr uint32_t PASS_SOP = 2 * PASS_STAGE;      // [S_hi ; S_lo] tile, 2 k-blocks x 8 KiB
-constexpr uint32_t PASS_XOP = PASS_SOP + 16384;    // [X_hi ; X_lo] tile [64 x 64] bf16
-constexpr uint32_t PASS_SMEM = PASS_XOP + 8192 + 1024;
-constexpr uint32_t kStageTx = 32768 + 16384 + 16384 + 8192 + 8192;
+constexpr uint32_t PASS_XOP = PASS_SOP + 16384;    // [X_hi ; X_lo] tile(s) [64 x 64] bf16 (state_pass_kernel: by chunk parity)
+constexpr uint32_t PASS_SMEM = PASS_XOP + 2 * 8192 + 1024;
+constexpr uint32_t kQkTx = 32768;                                   // Q|K of a stage
+constexpr uint32_t kStageTx = kQkTx + 16384 + 16384 + 8192 + 8192;   // all tiles of a stage
 constexpr uint32_t PASS_TMEM_COLS = 256;
 // TMEM columns (each accumulator 64 columns: 32 for the S_hi / X_hi part, 32 for the S_lo / X_lo part):
 //   [Q;K] [S_hi;S_lo]^T  (M = 128 token rows: Q rows in lanes 0-63, K rows in 64-127);
@@ -679,16 +683,23 @@ constexpr uint32_t PASS_TMEM_COLS = 256;
 // A chain of MMAs into one accumulator runs as fast as independent ones, so each product has one.
 constexpr uint32_t TM_D1 = 0, TM_PX = 64, TM_RX = 128;
 
-__device__ __forceinline__ void pass_issue_loads(uint8_t *st, uint64_t *bar, const CUtensorMap *qmap,
-                                                 const CUtensorMap *kmap, const CUtensorMap *phmap,
-                                                 const CUtensorMap *plmap, const CUtensorMap *rhmap,
-                                                 const CUtensorMap *rlmap, int hq, int t0, int gc, int hv, int h) {
-    mbar_arrive_expect_tx(bar, kStageTx);
+// Q and K rows of the chunk starting at token t0 (q/k head hq) into a stage (the caller arms the barrier).
+__device__ __forceinline__ void pass_load_qk(uint8_t *st, uint64_t *bar, const CUtensorMap *qmap,
+                                             const CUtensorMap *kmap, int hq, int t0) {
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
         tma_load_2d(st + ST_QK + kb * 16384, qmap, bar, hq * D + kb * 64, t0);
         tma_load_2d(st + ST_QK + kb * 16384 + 8192, kmap, bar, hq * D + kb * 64, t0);
     }
+}
+
+// All tiles of one chunk into a stage on one barrier: Q|K, then P_hi, P_lo, R_hi, R_lo of (chunk gc, head h).
+__device__ __forceinline__ void pass_issue_loads(uint8_t *st, uint64_t *bar, const CUtensorMap *qmap,
+                                                 const CUtensorMap *kmap, const CUtensorMap *phmap,
+                                                 const CUtensorMap *plmap, const CUtensorMap *rhmap,
+                                                 const CUtensorMap *rlmap, int hq, int t0, int gc, int hv, int h) {
+    mbar_arrive_expect_tx(bar, kStageTx);
+    pass_load_qk(st, bar, qmap, kmap, hq, t0);
     const int prow = (gc * hv + h) * D;
     tma_load_2d(st + ST_PH, phmap, bar, 0, prow);
     tma_load_2d(st + ST_PL, plmap, bar, 0, prow);
@@ -700,8 +711,9 @@ __device__ __forceinline__ void pass_issue_loads(uint8_t *st, uint64_t *bar, con
 // 128 and 512 threads (32 and 8 rows per thread) measured 119 and 146 us against 115 us at the 4K layer.
 constexpr int kPassThreads = 256;
 constexpr int NG = kPassThreads / 128;
-// MMA issuers: thread 0 (a Q-row warp, idle until the X barrier) issues [Q;K] S^T; lanes 0 of warps 2 and 3
-// (K-row warps, idle between the X barrier and the state update) issue P X and R X.
+
+// MMA issuers in state_pass_norm_kernel: thread 0 (a Q-row warp, idle until the X barrier) issues [Q;K] S^T;
+// lanes 0 of warps 2 and 3 (K-row warps, idle between the X barrier and the state update) issue P X and R X.
 constexpr int kPxIssuer = 64, kRxIssuer = 96;
 constexpr int DG = DS / NG;         // state rows per thread
 
@@ -799,9 +811,8 @@ __device__ __forceinline__ void outputs_end(float (&qs)[DG], int grp, int i, int
 // Thread 0 issues the [Q;K] S^T MMAs and thread 32 the TMA loads (both Q-row threads, which have nothing
 // to do before the X barrier); threads kPxIssuer and kRxIssuer (K-row threads, which have nothing to do
 // between the X barrier and the state update) issue P X and R X.
-template <bool NORM>
 __global__ void __launch_bounds__(kPassThreads, 1)
-state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
                   const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
                   const __nv_bfloat16 *__restrict__ v, const float *__restrict__ norms, float q_scale,
@@ -812,7 +823,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     extern __shared__ uint8_t pass_raw[];
     uint8_t *sm = align1024(pass_raw);
     __shared__ uint64_t bar_tma[2], bar_d1, bar_px, bar_rx[2];
-    __shared__ float ps_norm[2][NG][64];   // NORM: per-token sums of squares of each group's rows, by chunk parity
+    __shared__ float ps_norm[2][NG][64];   // per-token sums of squares of each group's rows, by chunk parity
     __shared__ uint32_t tmem_slot;
 
     constexpr int SLICES = D / DS;
@@ -914,12 +925,12 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     auto rx_parity = [](int cc) { return (uint32_t)((cc >> 1) & 1); };
 
     float qs[DG];
-    float qcur_n[DG];   // NORM: this chunk's e^g Q S^T, kept until the previous chunk's outputs have left
+    float qcur_n[DG];   // this chunk's e^g Q S^T, kept until the previous chunk's outputs have left
     int c = 0, prev_t0 = 0, prev_L = 0, c_stop = nchunks;
-    // With NORM every chunk keeps its cluster barrier round even after an error (the cluster barrier has no
-    // time limit, so no CTA may leave the sequence of rounds its peers still run): work stops, rounds do not.
-    for (; (NORM || ok) && c < nchunks; ++c) {
-        if (NORM && !ok) {
+    // Every chunk keeps its cluster barrier round even after an error (the cluster barrier has no time limit,
+    // so no CTA may leave the sequence of rounds its peers still run): work stops, rounds do not.
+    for (; c < nchunks; ++c) {
+        if (!ok) {
             if (c > 0) {
                 cluster_arrive();
                 cluster_wait();
@@ -1008,7 +1019,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 mma_bf16(rx, dRL0 + so + 2 * kk, dXOP + 128 * kk, idb, 1);
             mma_commit(&bar_rx[par]);
         }
-        if (NORM && krow && c > 0) cluster_arrive();   // K-row threads' share of this chunk's output round
+        if (krow && c > 0) cluster_arrive();   // K-row threads' share of this chunk's output round
         if (!krow) {
             // Q-row threads, off the state chain while P X runs: e^{g_i} (Q S^T)_i of this chunk (D1 is
             // rewritten only after the end-of-chunk barrier), then the previous chunk's outputs, whose R X
@@ -1022,24 +1033,15 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 #pragma unroll
                 for (int r = 0; r < DG; ++r) qcur[r] = (eg * cur.f) * (a[r] + b[r]);
             }
-            if (NORM) {
 #pragma unroll
-                for (int r = 0; r < DG; ++r) qcur_n[r] = qcur[r];
-            }
+            for (int r = 0; r < DG; ++r) qcur_n[r] = qcur[r];
             if (c > 0) {
                 if (!mbar_wait(&bar_rx[par ^ 1], rx_parity(c - 1))) ok = false;
                 tc_fence_after();
-                outputs_begin<NORM>(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, true,
+                // the outputs leave after the state update: the cluster round then overlaps the update instead
+                // of delaying it
+                outputs_begin<true>(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, true,
                                     ps_norm[(c - 1) & 1]);
-                // without the norm the outputs leave now; with it, after the state update (the cluster round
-                // then overlaps the update instead of delaying it)
-                if (!NORM)
-                    outputs_end<false>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, true, nullptr, norm_w,
-                                       norm_eps);
-            }
-            if (!NORM) {
-#pragma unroll
-                for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
             }
         }
 
@@ -1054,16 +1056,14 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             for (int e = 0; e < DG; ++e) S[e] = fmaf(eL, S[e], a[e] + b[e]);
         }
         write_sop();
-        if (NORM) {
-            if (krow) {
-                if (c > 0) cluster_wait();
-            } else {
-                if (c > 0)
-                    outputs_end<true>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, true,
-                                      ps_norm[(c - 1) & 1], norm_w, norm_eps);
+        if (krow) {
+            if (c > 0) cluster_wait();
+        } else {
+            if (c > 0)
+                outputs_end<true>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, true,
+                                  ps_norm[(c - 1) & 1], norm_w, norm_eps);
 #pragma unroll
-                for (int r = 0; r < DG; ++r) qs[r] = qcur_n[r];
-            }
+            for (int r = 0; r < DG; ++r) qs[r] = qcur_n[r];
         }
         prev_t0 = t0;
         prev_L = L;
@@ -1073,7 +1073,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         tc_fence_after();
         if (!ok && c_stop == nchunks) c_stop = c + 1;
     }
-    if (!NORM) c_stop = c;
 
     if (!ok) {
         // the loop's work stopped after chunk c_stop - 1; its prefetch of chunk c_stop may still be in flight
@@ -1081,7 +1080,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             raise_error(err, kErrTimeout);
             if (c_stop < nchunks) mbar_wait(&bar_tma[c_stop & 1], (c_stop >> 1) & 1);
         }
-        if (NORM && nchunks > 0) {   // the last chunk's output round, kept
+        if (nchunks > 0) {   // the last chunk's output round, kept
             cluster_arrive();
             cluster_wait();
         }
@@ -1092,10 +1091,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 const bool done = mbar_wait(&bar_rx[lp], rx_parity(nchunks - 1));
                 tc_fence_after();
                 if (!done) raise_error(err, kErrTimeout);
-                outputs_begin<NORM>(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, done, ps_norm[lp]);
-                outputs_end<NORM>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, done, ps_norm[lp], norm_w,
+                outputs_begin<true>(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, done, ps_norm[lp]);
+                outputs_end<true>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, done, ps_norm[lp], norm_w,
                                   norm_eps);
-            } else if (NORM) {
+            } else {
                 cluster_arrive();
                 cluster_wait();
             }
@@ -1106,9 +1105,363 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         }
     }
     tc_fence_before();
-    if (NORM) cluster_sync();   // no CTA leaves while a peer may still read its sums
-    else __syncthreads();
+    cluster_sync();   // no CTA leaves while a peer may still read its sums
     tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, PASS_TMEM_COLS);
+}
+
+// ============================================================================
+// Kernel 2b: state passing + outputs, warp-specialised (no output normalisation)
+// ============================================================================
+// Warps 0-7 compute exactly as in state_pass_norm_kernel (same TMEM quadrants, rows and arithmetic); lane 0
+// of warp 8 issues every MMA and lane 0 of warp 9 every tensor load.  The compute warps never wait behind an
+// issuing thread (a tensor load's issue can stall its thread for thousands of cycles when memory is busy):
+// they meet the issuers through mbarriers only, two per chunk.
+//   bar_x[b]  X buffer b written (128 arrivals, the K-row threads)              -> P X, later R X
+//   bar_s     state operand of the next chunk written (256 arrivals, after the state update) -> [Q;K] S^T
+// Per chunk c the MMA thread waits for the chunk's Q|K and bar_s, issues [Q;K] S^T (commit bar_d1), then chunk
+// c - 1's R X (the pipe runs it while the X values are computed), waits for P and bar_x and issues P X
+// (commit bar_px).  The tensor pipe runs small MMAs one after another, so the state chain's two groups never
+// queue behind R X.
+// Tiles: Q|K, P and R each have a full barrier (landed) and a free barrier per stage (the MMA thread commits
+// it once its reads of that stage are complete); the load thread refills a stage part only after its free
+// barrier.  Every wait is on a phase that cannot be overtaken before the waiter acts (each barrier's next
+// phase depends on work the waiter has still to do), so parities never alias.
+constexpr int kWsThreads = kPassThreads + 64;
+constexpr int kMmaWarp = kPassThreads / 32, kTmaWarp = kMmaWarp + 1;
+constexpr uint32_t kPTx = 16384 + 16384, kRTx = 8192 + 8192;
+
+__global__ void __launch_bounds__(kWsThreads, 1)
+state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
+                     const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
+                     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ norms, float q_scale,
+                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
+                     const float *__restrict__ init_state, const int32_t *__restrict__ cu, int n_seqs, int total,
+                     int nch, int hk, int hv, void *__restrict__ out, int out_f32, float *__restrict__ final_state,
+                     unsigned int *err) {
+    extern __shared__ uint8_t pass_raw[];
+    uint8_t *sm = align1024(pass_raw);
+    __shared__ uint64_t bar_qk[2], bar_p[2], bar_r[2], bar_qkf[2], bar_pf[2], bar_rf[2];
+    __shared__ uint64_t bar_s, bar_x[2], bar_d1, bar_px, bar_rx[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;   // set by any thread whose wait ran out; everyone stops at the next check
+
+    constexpr int SLICES = D / DS;
+    const int slice = blockIdx.x % SLICES;
+    const int h = (blockIdx.x / SLICES) % hv;
+    const int n = blockIdx.x / (SLICES * hv);
+    const int hq = h / (hv / hk);
+    const int row0 = slice * DS;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t base = smem_u32(sm);
+
+    int ta = 0, tb = total, gc0 = 0;   // one sequence: the host checked cu_seqlens = {0, total}
+    if (n_seqs > 1) {
+        seq_range(cu, n, total, ta, tb);
+        gc0 = first_chunk_of(cu, n, total);
+    }
+    const int nchunks = (tb - ta + C - 1) / C;
+    const bool range_ok = gc0 + nchunks <= nch;
+    if (!range_ok && tid == 0) raise_error(err, kErrInternal);
+    const bool started = range_ok && nchunks > 0;
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, PASS_TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bar_qk[b], 1);
+            mbar_init(&bar_p[b], 1);
+            mbar_init(&bar_r[b], 1);
+            mbar_init(&bar_qkf[b], 1);
+            mbar_init(&bar_pf[b], 1);
+            mbar_init(&bar_rf[b], 1);
+            mbar_init(&bar_x[b], 128);
+            mbar_init(&bar_rx[b], 1);
+        }
+        mbar_init(&bar_s, kPassThreads);
+        mbar_init(&bar_d1, 1);
+        mbar_init(&bar_px, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    // zero the padding rows of the R tiles once (rows 64..127 feed only unused accumulator rows)
+    for (int x = tid; x < 4 * 512; x += kWsThreads) {
+        const int st = x / 1024, t = (x / 512) & 1, o = x % 512;
+        reinterpret_cast<uint4 *>(sm + st * PASS_STAGE + (t ? ST_RL : ST_RH) + 8192)[o] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();   // the zeros are read by the tensor cores
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    // Shared-memory descriptors, as in state_pass_norm_kernel.
+    const uint64_t dQK0 = smem_desc(base + ST_QK, 16, 1024, kSW);
+    const uint64_t dPH0 = smem_desc(base + ST_PH, 16, 1024, kSW);
+    const uint64_t dPL0 = smem_desc(base + ST_PL, 16, 1024, kSW);
+    const uint64_t dRH0 = smem_desc(base + ST_RH, 16, 1024, kSW);
+    const uint64_t dRL0 = smem_desc(base + ST_RL, 16, 1024, kSW);
+    const uint64_t dSOP = smem_desc(base + PASS_SOP, 8192, 1024, kSW);
+    const uint64_t dXOP = smem_desc(base + PASS_XOP, 8192, 1024, kSW);   // + parity * (8192 >> 4)
+    constexpr uint64_t kStageStep = PASS_STAGE >> 4;
+    constexpr uint32_t idb = idesc_bf16_f32(128, 64, false, true);
+    auto ph = [](int cc) { return (uint32_t)((cc >> 1) & 1); };   // phase parity of chunk cc on a per-stage barrier
+    auto stop = [&]() { return abort_flag != 0; };
+    auto fail = [&]() { abort_flag = 1; };
+
+    if (warp == kMmaWarp) {
+        if (lane == 0 && started) {
+            // R X of chunk cc (64 (+64 pad) x 64) = (R_hi + R_lo) [X_hi ; X_lo]^T into TMEM buffer cc & 1
+            auto issue_rx = [&](int cc) -> bool {
+                const int sc = cc & 1;
+                if (!mbar_wait(&bar_r[sc], ph(cc))) return false;
+                const uint64_t soc = sc * kStageStep, dx = dXOP + sc * (8192 >> 4);
+                const uint32_t rx = tmem + TM_RX + 64 * sc;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) mma_bf16(rx, dRH0 + soc + 2 * kk, dx + 128 * kk, idb, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) mma_bf16(rx, dRL0 + soc + 2 * kk, dx + 128 * kk, idb, 1);
+                mma_commit(&bar_rx[sc]);
+                mma_commit(&bar_rf[sc]);
+                return true;
+            };
+            bool ok = true;
+            for (int c = 0; ok && c < nchunks; ++c) {
+                if (stop()) break;
+                const int s = c & 1;
+                const uint64_t so = s * kStageStep;
+                // D1[128 x 64] = [Q ; K] [S_hi ; S_lo]^T once this chunk's Q|K and the state operand are in place
+                // (tiles first: they land early, the state operand is the chain)
+                ok = mbar_wait(&bar_qk[s], ph(c)) && mbar_wait(&bar_s, (uint32_t)(c & 1));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                    mma_bf16(tmem + TM_D1, dQK0 + so + off, dSOP + 128 * kk, idb, kk > 0);
+                }
+                mma_commit(&bar_d1);
+                mma_commit(&bar_qkf[s]);
+                if (c > 0 && !(ok = issue_rx(c - 1))) break;   // X of chunk c - 1 is complete: its P X ran
+                // P X (dk x 64) = P_hi [X_hi ; X_lo]^T + P_lo [X_hi ; X_lo]^T once this chunk's P and X are in place
+                ok = mbar_wait(&bar_p[s], ph(c)) && mbar_wait(&bar_x[s], ph(c));
+                if (!ok) break;
+                const uint64_t dx = dXOP + s * (8192 >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    mma_bf16(tmem + TM_PX, dPH0 + so + 2 * kk, dx + 128 * kk, idb, kk > 0);
+                    mma_bf16(tmem + TM_PX, dPL0 + so + 2 * kk, dx + 128 * kk, idb, 1);
+                }
+                mma_commit(&bar_px);
+                mma_commit(&bar_pf[s]);
+            }
+            // the last chunk's R X, once its X is written
+            if (ok && !stop()) ok = mbar_wait(&bar_x[(nchunks - 1) & 1], ph(nchunks - 1)) && issue_rx(nchunks - 1);
+            if (!ok) fail();
+        }
+        __syncwarp();
+    } else if (warp == kTmaWarp) {
+        if (lane == 0 && started) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&phmap);
+            tma_prefetch_desc(&plmap);
+            tma_prefetch_desc(&rhmap);
+            tma_prefetch_desc(&rlmap);
+            // Q|K, P and R of chunk cc into stage cc & 1
+            auto load_qk = [&](int cc) {
+                mbar_arrive_expect_tx(&bar_qk[cc & 1], kQkTx);
+                pass_load_qk(sm + (cc & 1) * PASS_STAGE, &bar_qk[cc & 1], &qmap, &kmap, hq, ta + cc * C);
+            };
+            auto load_p = [&](int cc) {
+                uint8_t *st = sm + (cc & 1) * PASS_STAGE;
+                const int prow = ((gc0 + cc) * hv + h) * D;
+                mbar_arrive_expect_tx(&bar_p[cc & 1], kPTx);
+                tma_load_2d(st + ST_PH, &phmap, &bar_p[cc & 1], 0, prow);
+                tma_load_2d(st + ST_PL, &plmap, &bar_p[cc & 1], 0, prow);
+            };
+            auto load_r = [&](int cc) {
+                uint8_t *st = sm + (cc & 1) * PASS_STAGE;
+                const int rrow = ((gc0 + cc) * hv + h) * C;
+                mbar_arrive_expect_tx(&bar_r[cc & 1], kRTx);
+                tma_load_2d(st + ST_RH, &rhmap, &bar_r[cc & 1], 0, rrow);
+                tma_load_2d(st + ST_RL, &rlmap, &bar_r[cc & 1], 0, rrow);
+            };
+            // both stages start empty
+            int nq = min(2, nchunks), np = nq, nr = nq;   // chunks < nq (np, nr) have had Q|K (P, R) requested
+            for (int cc = 0; cc < nq; ++cc) {
+                load_qk(cc);
+                load_p(cc);
+                load_r(cc);
+            }
+            // stage c & 1 takes chunk c + 2 once chunk c has finished with it: Q|K after [Q;K] S^T, P after
+            // P X, R after R X (which runs during chunk c + 1)
+            bool ok = true;
+            for (int c = 0; c + 2 < nchunks; ++c) {
+                if (stop()) break;
+                const int s = c & 1;
+                if (!(ok = mbar_wait(&bar_qkf[s], ph(c)))) break;
+                load_qk(c + 2);
+                nq = c + 3;
+                if (!(ok = mbar_wait(&bar_pf[s], ph(c)))) break;
+                load_p(c + 2);
+                np = c + 3;
+                if (!(ok = mbar_wait(&bar_rf[s], ph(c)))) break;
+                load_r(c + 2);
+                nr = c + 3;
+            }
+            if (!ok) fail();
+            // every requested tile has landed before the CTA can end (normally all were consumed); each
+            // barrier has at most one phase outstanding, the last one armed
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int aq = (nq - b + 1) / 2, ap = (np - b + 1) / 2, ar = (nr - b + 1) / 2;
+                if (aq > 0) mbar_wait(&bar_qk[b], (uint32_t)((aq - 1) & 1));
+                if (ap > 0) mbar_wait(&bar_p[b], (uint32_t)((ap - 1) & 1));
+                if (ar > 0) mbar_wait(&bar_r[b], (uint32_t)((ar - 1) & 1));
+            }
+        }
+        __syncwarp();
+    } else {
+        // compute warps: roles as in state_pass_norm_kernel
+        const int quad = warp & 3, grp = warp >> 2;
+        const int lrow = 32 * quad + lane;
+        const int d = lrow;
+        const int i = lrow & 63;
+        const bool krow = quad >= 2;
+        const int rowg = row0 + grp * DG;
+        const uint32_t tlane = (uint32_t)(32 * quad) << 16;
+
+        ChunkInputs nxt;
+        if (started)
+            load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0, ta, min(C, tb - ta), hv, h, rowg, lane,
+                              krow, i);
+        float S[DG];
+        const size_t sbase = (((size_t)n * hv + h) * D + rowg) * D + d;
+#pragma unroll
+        for (int r = 0; r < DG; ++r) S[r] = init_state ? init_state[sbase + (size_t)r * D] : 0.f;
+        auto write_sop = [&]() {
+#pragma unroll
+            for (int j = 0; j < DG / 8; ++j) {
+                uint4 hi, lo;
+                split8_bf16(&S[8 * j], hi, lo);
+                *reinterpret_cast<uint4 *>(sm + PASS_SOP + sw128_offset(d, grp * DG + 8 * j)) = hi;
+                *reinterpret_cast<uint4 *>(sm + PASS_SOP + sw128_offset(d, DS + grp * DG + 8 * j)) = lo;
+            }
+        };
+        // publish the state operand: generic writes made visible to the tensor cores, TMEM reads of this
+        // thread ordered before the MMAs that follow
+        auto publish_sop = [&]() {
+            write_sop();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar_s);
+        };
+        if (started) publish_sop();
+
+        float qs[DG];
+        int prev_t0 = 0, prev_L = 0;
+        bool ok = range_ok;   // an empty sequence runs no chunk and returns its initial state
+        int c = 0;
+        for (; ok && c < nchunks; ++c) {
+            if (stop()) {
+                ok = false;
+                break;
+            }
+            const uint32_t par = c & 1;
+            const int t0 = ta + c * C, L = min(C, tb - t0);
+            const ChunkInputs cur = nxt;
+            if (c + 1 < nchunks)
+                load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0 + c + 1, t0 + C, min(C, tb - t0 - C),
+                                  hv, h, rowg, lane, krow, i);
+            const float2 g2 = cumsum_pairs(cur.la0, cur.la1, L, lane);
+            const float gL = g_of(g2, L - 1);
+            const float eg = __expf(g_of(g2, i));
+
+            if (!mbar_wait(&bar_d1, par)) ok = false;
+            tc_fence_after();
+            if (krow) {
+                // X_i = beta_i (v_i - e^{g_i} (K S^T)_i) into X buffer c & 1, whose last reader (R X of chunk
+                // c - 2) must be complete
+                if (c > 1 && !mbar_wait(&bar_rx[par], ph(c - 2))) ok = false;
+                tc_fence_after();
+                float a[DG], b[DG];
+                tmem_ldx2<DG>(tmem + tlane + TM_D1 + grp * DG, tmem + tlane + TM_D1 + 32 + grp * DG, a, b);
+                const float bi = cur.b, be = cur.b * eg * cur.f;
+#pragma unroll
+                for (int q4 = 0; q4 < DG / 8; ++q4) {
+                    const uint4 x = cur.v[q4];
+                    const float vv[8] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y),
+                                         bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w)};
+                    float xv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xv[e] = bi * vv[e] - be * (a[q4 * 8 + e] + b[q4 * 8 + e]);
+                    uint4 hi, lo;
+                    split8_bf16(xv, hi, lo);
+                    *reinterpret_cast<uint4 *>(sm + PASS_XOP + par * 8192 + sw128_offset(i, grp * DG + 8 * q4)) = hi;
+                    *reinterpret_cast<uint4 *>(sm + PASS_XOP + par * 8192 + sw128_offset(i, DS + grp * DG + 8 * q4)) =
+                        lo;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bar_x[par]);
+            } else {
+                // Q-row threads: e^{g_i} (Q S^T)_i of this chunk, then the previous chunk's outputs
+                float qcur[DG];
+                {
+                    float a[DG], b[DG];
+                    tmem_ldx2<DG>(tmem + tlane + TM_D1 + grp * DG, tmem + tlane + TM_D1 + 32 + grp * DG, a, b);
+#pragma unroll
+                    for (int r = 0; r < DG; ++r) qcur[r] = (eg * cur.f) * (a[r] + b[r]);
+                }
+                if (c > 0) {
+                    if (!mbar_wait(&bar_rx[par ^ 1], ph(c - 1))) ok = false;
+                    tc_fence_after();
+                    outputs_begin<false>(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, ok, nullptr);
+                    outputs_end<false>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, ok, nullptr, nullptr,
+                                       0.f);
+                }
+#pragma unroll
+                for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
+            }
+
+            // state: S[r][d] <- e^{g_L} S[r][d] + (P X)[d][r] + (P X)[d][32 + r]
+            if (!mbar_wait(&bar_px, par)) ok = false;
+            tc_fence_after();
+            if (!ok) break;
+            {
+                const float eL = __expf(gL);
+                float a[DG], b[DG];
+                tmem_ldx2<DG>(tmem + tlane + TM_PX + grp * DG, tmem + tlane + TM_PX + 32 + grp * DG, a, b);
+#pragma unroll
+                for (int e = 0; e < DG; ++e) S[e] = fmaf(eL, S[e], a[e] + b[e]);
+            }
+            publish_sop();
+            prev_t0 = t0;
+            prev_L = L;
+        }
+        if (!ok && range_ok) fail();
+        if (ok) {
+            if (!krow && nchunks > 0) {
+                const uint32_t lp = (nchunks - 1) & 1;
+                const bool done = mbar_wait(&bar_rx[lp], ph(nchunks - 1));
+                tc_fence_after();
+                if (!done) fail();
+                outputs_begin<false>(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, done, nullptr);
+                outputs_end<false>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, done, nullptr, nullptr, 0.f);
+            }
+            if (final_state) {
+#pragma unroll
+                for (int r = 0; r < DG; ++r) final_state[sbase + (size_t)r * D] = S[r];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && started && abort_flag) raise_error(err, kErrTimeout);
     if (warp == 0) tmem_dealloc(tmem, PASS_TMEM_COLS);
 }
 
@@ -1175,9 +1528,9 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(state_pass_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
+            e = cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(state_pass_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
+            e = cudaFuncSetAttribute(state_pass_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
         if (e != cudaSuccess) return e;
         attrs_set[dev] = true;
     }
@@ -1212,22 +1565,25 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
         attr[0].val.clusterDim.x = D / DS;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid2);
-        cfg.blockDim = dim3(kPassThreads);
-        cfg.dynamicSmemBytes = PASS_SMEM;
-        cfg.stream = p.stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = p.norm_w ? 1 : 0;
         const float *nrm = p.qk_norm ? norms : nullptr;
-        e = p.norm_w ? cudaLaunchKernelEx(&cfg, state_pass_kernel<true>, qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm,
-                                          p.q_scale, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.n_seqs,
-                                          p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state,
-                                          p.norm_w, p.norm_eps, p.err)
-                     : cudaLaunchKernelEx(&cfg, state_pass_kernel<false>, qmap, kmap, phmap, plmap, rhmap, rlmap, p.v,
-                                          nrm, p.q_scale, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.n_seqs,
-                                          p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state,
-                                          p.norm_w, p.norm_eps, p.err);
+        if (p.norm_w) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(grid2);
+            cfg.blockDim = dim3(kPassThreads);
+            cfg.dynamicSmemBytes = PASS_SMEM;
+            cfg.stream = p.stream;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, state_pass_norm_kernel, qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm,
+                                   p.q_scale, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.n_seqs,
+                                   p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state, p.norm_w,
+                                   p.norm_eps, p.err);
+        } else {
+            state_pass_kernel<<<grid2, kWsThreads, PASS_SMEM, p.stream>>>(
+                qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm, p.q_scale, p.log_alpha, p.beta, p.init_state,
+                p.cu_seqlens, p.n_seqs, p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state, p.err);
+            e = cudaSuccess;
+        }
         if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
