@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include "gdn_internal.cuh"
+#include "sm100.cuh"
 
 namespace {
 
@@ -71,6 +72,18 @@ unsigned int *device_error_ptr() {
         dev_cached = dev;
     }
     return ptr;
+}
+
+// One CTA waits for the first phase of a shared-memory mbarrier that nothing arrives on: the same bounded
+// wait and error word as every kernel of the library, with the caller's limit in place of the kernels' 1 s.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned int *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        gdn::sm100::mbar_init(&bar, 1);
+        gdn::sm100::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !gdn::sm100::mbar_wait_for(&bar, 0, limit_ns)) gdn::raise_error(err, gdn::kErrTimeout);
 }
 
 }  // namespace
@@ -374,6 +387,14 @@ gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
     p.err = nullptr;
     p.stream = static_cast<cudaStream_t>(stream);
     return gdn::launch_decode(p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_selftest_bounded_wait(int limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 1000000) return GDN_ERR_INVALID_ARG;
+    unsigned int *err = device_error_ptr();
+    if (!err) return GDN_ERR_CUDA;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((uint64_t)limit_us * 1000ull, err);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 gdn_status gdn_device_error(void *stream) {

@@ -46,13 +46,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false once `limit_ns` of %globaltimer have passed.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity))
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     return true;
+}
+// The kernels' wait: false on timeout (kWaitTimeoutNs).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitTimeoutNs);
 }
 
 // ------------------------------------------------------------------ clusters

@@ -24,7 +24,7 @@ DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 # every symbol include/gdn.h declares
 EXPORTS = ("gdn_prefill", "gdn_prefill_chunked_phase", "gdn_prefill_workspace_size", "gdn_decode_step",
            "gdn_device_error", "gdn_status_string", "gdn_version", "gdn_prefill_noalloc", "gdn_prefill_algo",
-           "gdn_prefill_host", "gdn_prefill_host_staging_size")
+           "gdn_prefill_host", "gdn_prefill_host_staging_size", "gdn_selftest_bounded_wait")
 NOALLOC_SCRATCH_BYTES = 97 * 1024 * 1024
 PHASE = {"prep": 1, "pass": 2}
 
@@ -67,6 +67,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdn_decode_step.restype = I
     lib.gdn_device_error.argtypes = [P]
     lib.gdn_device_error.restype = I
+    lib.gdn_selftest_bounded_wait.argtypes = [I, P]
+    lib.gdn_selftest_bounded_wait.restype = I
     lib.gdn_status_string.argtypes = [I]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_version.restype = I
@@ -394,3 +396,11 @@ def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.
 def device_error(stream=None) -> int:
     """Synchronise and return the device-side error status (0 = none)."""
     return int(load_library().gdn_device_error(_stream_ptr(stream)))
+
+
+def selftest_bounded_wait(limit_us: int, stream=None) -> None:
+    """Run ``gdn_selftest_bounded_wait``: one CTA waits for a barrier phase that nothing completes and gives
+    up after ``limit_us`` microseconds, recording GDN_ERR_TIMEOUT for ``device_error`` to report."""
+    st = load_library().gdn_selftest_bounded_wait(int(limit_us), _stream_ptr(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_selftest_bounded_wait")

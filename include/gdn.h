@@ -217,6 +217,21 @@ GDN_API gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float 
 GDN_API gdn_status gdn_device_error(void *stream);
 
 /*
+ * gdn_selftest_bounded_wait: a check of the failure path that every kernel of
+ * the library shares; it computes nothing (the pages have no counterpart).
+ * Every device-side wait of the kernels gives up after 1 s, records
+ * GDN_ERR_TIMEOUT in the device error word and lets the kernel return, so a
+ * stalled kernel ends with an error status instead of hanging the GPU.  This
+ * call launches one CTA on `stream` that waits, through the same code, for a
+ * barrier phase that nothing completes, giving up after `limit_us`
+ * microseconds (1 to 1000000).  Afterwards gdn_device_error(stream) returns
+ * GDN_ERR_TIMEOUT (and clears the word), and the CUDA context stays usable.
+ * Returns GDN_ERR_INVALID_ARG for a limit outside that range (nothing is
+ * launched), GDN_ERR_CUDA if the launch fails, else GDN_OK.
+ */
+GDN_API gdn_status gdn_selftest_bounded_wait(int limit_us, void *stream);
+
+/*
  * gdn_prefill_noalloc: the chunked prefill (GDN_ALGO_CHUNKED) for callers that
  * cannot allocate device memory, so cannot supply the workspace gdn_prefill
  * needs: code that must not call cudaMalloc while it runs (an allocation can

@@ -234,3 +234,9 @@ def test_prefill_host_validates_before_enqueueing(lib):
     assert prefill_host(lib, hk=3, hv=4) == 1
     assert prefill_host(lib, cu_host=_cu([0, 65])) == 1
     assert prefill_host(lib, T=0, cu_host=_cu([0, 0]), fin=None) == 0   # nothing to do: returns at once
+
+
+def test_selftest_bounded_wait_rejects_limits_out_of_range(lib):
+    # validated on the host before anything is launched
+    for bad in (0, -5, 1000001):
+        assert lib.gdn_selftest_bounded_wait(bad, None) == 1  # GDN_ERR_INVALID_ARG
