@@ -676,6 +676,15 @@ def run_gb300(args):
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)",
                 "flops_per_launch": flops_prep if dom == "chunk_prep_kernel" else flops_pass}
+    # the whole prefill call (both kernels) against both rooflines: dense-equivalent FLOPs and the algorithmic
+    # bytes (q, k, v, gates read once, outputs written once, the final state written; no initial state)
+    step_s = total_ms * 1e-3 / args.steps
+    call_bytes = T_TOKENS * (2 * HK * D * 2 + HV * D * 2 + 2 * HV * 4 + HV * D * 2) + HV * D * D * 4
+    roofline["whole_call"] = {
+        "tflops": (flops_prep + flops_pass) / step_s / 1e12,
+        "frac_tensor": (flops_prep + flops_pass) / step_s / 1e12 / peaks["bf16_tflops"],
+        "hbm_gbs": call_bytes / step_s / 1e9, "frac_hbm": call_bytes / step_s / 1e9 / peaks["hbm_gbs"],
+        "bytes": call_bytes, "flops": flops_prep + flops_pass}
     dec_gbs = DECODE_STATE_BYTES / (decode_us * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
