@@ -54,6 +54,27 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, ui
         if (global_timer_ns() - t0 > limit_ns) return false;
     return true;
 }
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait by spinning on test_wait (no suspension, so the thread sees the phase complete as soon as it does);
+// false on timeout (kWaitTimeoutNs).  For waits on a latency-critical chain.
+__device__ __forceinline__ bool mbar_spin(uint64_t *bar, uint32_t parity) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_test_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+}
 // The kernels' wait: false on timeout (kWaitTimeoutNs).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return mbar_wait_for(bar, parity, kWaitTimeoutNs);
