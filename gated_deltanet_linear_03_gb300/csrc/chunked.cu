@@ -1136,13 +1136,13 @@ constexpr uint32_t kPTx = 16384 + 16384, kRTx = 8192 + 8192;
 
 __global__ void __launch_bounds__(kWsThreads, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
-                     const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
-                     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ norms, float q_scale,
-                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
-                     const float *__restrict__ init_state, const int32_t *__restrict__ cu, int n_seqs, int total,
-                     int nch, int hk, int hv, void *__restrict__ out, int out_f32, float *__restrict__ final_state,
-                     unsigned int *err) {
+                  const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
+                  const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
+                  const __nv_bfloat16 *__restrict__ v, const float *__restrict__ norms, float q_scale,
+                  const float *__restrict__ log_alpha, const float *__restrict__ beta,
+                  const float *__restrict__ init_state, const int32_t *__restrict__ cu, int n_seqs, int total,
+                  int nch, int hk, int hv, void *__restrict__ out, int out_f32, float *__restrict__ final_state,
+                  unsigned int *err) {
     extern __shared__ uint8_t pass_raw[];
     uint8_t *sm = align1024(pass_raw);
     __shared__ uint64_t bar_qk[2], bar_p[2], bar_r[2], bar_qkf[2], bar_pf[2], bar_rf[2];
