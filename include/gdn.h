@@ -175,7 +175,7 @@ GDN_API size_t gdn_prefill_workspace_size(int n_seqs, int total_tokens, int hk, 
  * value heads):
  *   - the scan when the longest sequence has at most 16 tokens, or at most 32
  *     tokens with n_seqs * hv <= 64 (the chunked path pays a fixed cost of
- *     about 16 us for one short sequence and 45 us for eight);
+ *     about 13 us for one short sequence and 45 us for eight);
  *   - the scan whenever dk != 128 (the chunked path implements d = 128 only);
  *   - the chunked path otherwise.
  * It needs no CUDA call.  gdn_prefill and gdn_prefill_workspace_size apply the
