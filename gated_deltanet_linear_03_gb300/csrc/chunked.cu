@@ -1469,16 +1469,17 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 }
 
 // ---------------------------------------------------------------- host side
+// The driver's tensor-map encoder, looked up once per process (a function-local static: thread-safe).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         cudaDriverEntryPointQueryResult q;
         void *p = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -1525,8 +1526,9 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static bool attrs_set[128] = {};
-    if (dev < 128 && !attrs_set[dev]) {
+    static std::atomic<bool> attrs_set[kMaxDevices];
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (!cached || !attrs_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
@@ -1535,7 +1537,7 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(state_pass_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
         if (e != cudaSuccess) return e;
-        attrs_set[dev] = true;
+        if (cached) attrs_set[dev].store(true, std::memory_order_release);
     }
 
     CUtensorMap qmap{}, kmap{}, phmap{}, plmap{}, rhmap{}, rlmap{};

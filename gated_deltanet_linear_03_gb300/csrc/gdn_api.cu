@@ -50,28 +50,63 @@ int resolve_auto(int n_seqs, int hv, int dk, const int32_t *cu_host) {
 
 // Multiprocessors of the current device (cached per device; 1 if the query fails).
 int sm_count() {
-    static int cached[64] = {};
+    static std::atomic<int> cached[gdn::kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    const bool in_table = dev < gdn::kMaxDevices;
+    if (in_table) {
+        const int n = cached[dev].load(std::memory_order_relaxed);
+        if (n > 0) return n;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-    if (dev < 64) cached[dev] = n;
+    if (in_table) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
+// Device address of the error word of the current device.  Every device that loads the library has its own
+// word; the address is looked up once per device (with that device current) and kept in a table of atomics.
 unsigned int *device_error_ptr() {
-    static unsigned int *ptr = nullptr;
-    static int dev_cached = -1;
+    static std::atomic<unsigned int *> table[gdn::kMaxDevices];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    if (ptr == nullptr || dev != dev_cached) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-        ptr = static_cast<unsigned int *>(p);
-        dev_cached = dev;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+    const bool in_table = dev < gdn::kMaxDevices;
+    if (in_table) {
+        unsigned int *p = table[dev].load(std::memory_order_relaxed);
+        if (p) return p;
     }
-    return ptr;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    if (in_table) table[dev].store(static_cast<unsigned int *>(p), std::memory_order_relaxed);
+    return static_cast<unsigned int *>(p);
+}
+
+// Device pointers given to an entry point must belong to the current device: the kernels are launched there,
+// on a stream of that device.  A pointer to host memory, to no allocation or to another GPU's memory is
+// refused with GDN_ERR_INVALID_ARG before anything is launched.  While `stream` is being captured into a CUDA
+// graph the query is skipped (it is not a stream operation, but a check that the capture mode refused would
+// end the capture): calls recorded into a graph are the caller's to get right.
+gdn_status check_on_current_device(const void *p, cudaStream_t stream) {
+    if (!p) return GDN_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return GDN_OK;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_INVALID_ARG;
+    }
+    if ((a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) || a.device != dev)
+        return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
 }
 
 // One CTA waits for the first phase of a shared-memory mbarrier that nothing arrives on: the same bounded
@@ -178,6 +213,12 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
             if (overlaps(workspace, need, a.p, a.n)) return GDN_ERR_INVALID_ARG;
     }
     if (total_tokens == 0 && !final_state) return GDN_OK;
+    {
+        const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+        const void *anchors[] = {q, out, final_state, workspace};
+        for (const void *a : anchors)
+            if ((st = check_on_current_device(a, cs)) != GDN_OK) return st;
+    }
 
     gdn::PrefillProblem p{};
     p.n_seqs = n_seqs; p.total_tokens = total_tokens; p.hk = hk; p.hv = hv; p.d = dk;
@@ -324,6 +365,7 @@ gdn_status gdn_prefill_host(int n_seqs, int total_tokens, int hk, int hv, int dk
     if (!staging || staging_bytes < s.total) return GDN_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(staging) & 255u) return GDN_ERR_ALIGNMENT;
     if (total_tokens == 0 && !final_state_host) return GDN_OK;
+    if ((st = check_on_current_device(staging, static_cast<cudaStream_t>(stream))) != GDN_OK) return st;
 
     uint8_t *base = static_cast<uint8_t *>(staging);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -375,6 +417,9 @@ gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
     if (overlaps(out, out_bytes, q, (size_t)n * hk * dk * 2) || overlaps(out, out_bytes, k, (size_t)n * hk * dk * 2) ||
         overlaps(out, out_bytes, v, (size_t)n * hv * dv * 2))
         return GDN_ERR_INVALID_ARG;
+    if ((st = check_on_current_device(state, static_cast<cudaStream_t>(stream))) != GDN_OK ||
+        (st = check_on_current_device(out, static_cast<cudaStream_t>(stream))) != GDN_OK)
+        return st;
 
     gdn::DecodeProblem p{};
     p.n = n; p.hk = hk; p.hv = hv; p.d = dk; p.state = state;

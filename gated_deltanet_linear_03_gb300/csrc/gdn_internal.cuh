@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/gdn.h"
 
 namespace gdn {
@@ -26,6 +28,10 @@ __device__ __forceinline__ float qk_inv_norm(float sum_sq, int qk_norm) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xffff0000u); }
+
+// Per-device host caches (kernel attributes set, symbol addresses looked up) hold at most this many devices;
+// their entries are atomics, so host threads that fill the same entry at once only repeat the work.
+constexpr int kMaxDevices = 256;
 
 // Error word bits set by kernels (read back by gdn_device_error).
 enum : unsigned int { kErrTimeout = 1u, kErrInternal = 2u };

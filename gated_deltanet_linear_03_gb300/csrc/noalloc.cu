@@ -16,7 +16,9 @@
 // Use rules (also stated in include/gdn.h):
 //   - The first call on a device looks up the array's device address with
 //     cudaGetSymbolAddress (once per device, with that device current).  Make
-//     that first call before any CUDA stream capture.
+//     that first call before any CUDA stream capture.  First calls made at the
+//     same time from several host threads are safe: each stores the same
+//     address.
 //   - All calls share the one array and it keeps the last call's contents;
 //     nothing in it has to start at zero (each call writes all the scratch it
 //     later reads).  Calls whose GPU work overlaps in time (different streams,
@@ -36,17 +38,20 @@ static_assert(kNoAllocScratchBytes == (size_t)GDN_NOALLOC_SCRATCH_BYTES, "header
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the scratch on the current device.  In host code the name
-// g_noalloc_scratch is only a host-side stand-in, never a device address.
+// g_noalloc_scratch is only a host-side stand-in, never a device address.  The
+// table entries are atomics: host threads that make their first call on the
+// same device at the same time each look the address up and store the same
+// value, which is harmless.
 void *scratch_device_address() {
-    static void *addr[256] = {};
+    static std::atomic<void *> addr[gdn::kMaxDevices];
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
-    if (addr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= gdn::kMaxDevices) return nullptr;
+    void *cached = addr[dev].load(std::memory_order_relaxed);
+    if (cached) return cached;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    addr[dev].store(p, std::memory_order_relaxed);
+    return p;
 }
 
 }  // namespace

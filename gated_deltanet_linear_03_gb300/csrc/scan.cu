@@ -265,12 +265,13 @@ cudaError_t launch_scan_dp(const PrefillProblem &p) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static bool attr_set[128] = {};
-    if (dev < 128 && !attr_set[dev]) {
+    static std::atomic<bool> attr_set[kMaxDevices];
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (!cached || !attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(scan_prefill_kernel<D, PREP, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        if (cached) attr_set[dev].store(true, std::memory_order_release);
     }
     // with the output normalisation the D / kRows slices of a head form one cluster
     const unsigned grid = (unsigned)(p.n_seqs * p.hv * (D / kRows));

@@ -87,10 +87,19 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream_ptr(stream) -> ctypes.c_void_p:
+def _stream_ptr(stream, device=None) -> ctypes.c_void_p:
+    """The stream to enqueue on: ``stream``, else the current stream of ``device`` (the tensors' device)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _same_device(device: torch.device, **tensors):
+    """Every tensor lives on ``device``: the library launches on the current device, which the wrappers make
+    the tensors' device, and refuses pointers of any other device."""
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the other tensors on {device}")
 
 
 def _need(t: torch.Tensor, name: str, dtype, ndim: int):
@@ -174,10 +183,13 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
     if need and workspace is None:
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.gdn_prefill(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
-                         _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out), DTYPE[out.dtype],
-                         _ptr(final_state), int(bool(qk_norm)), float(q_scale), _ptr(norm_weight),
-                         float(norm_eps), ALGO[algo], _ptr(workspace), ws_bytes, _stream_ptr(stream))
+    _same_device(q.device, k=k, v=v, log_alpha=log_alpha, beta=beta, cu_seqlens=cu_seqlens, init_state=init_state,
+                 out=out, final_state=final_state, norm_weight=norm_weight, workspace=workspace)
+    with torch.cuda.device(q.device):
+        st = lib.gdn_prefill(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                             _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out), DTYPE[out.dtype],
+                             _ptr(final_state), int(bool(qk_norm)), float(q_scale), _ptr(norm_weight),
+                             float(norm_eps), ALGO[algo], _ptr(workspace), ws_bytes, _stream_ptr(stream, q.device))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill")
     return out, final_state
@@ -212,10 +224,13 @@ def prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha
     elif final_state is False:
         final_state = None
     cu_arr, _ = _host_cu(cu_seqlens, cu_seqlens_host)
-    st = lib.gdn_prefill_noalloc(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
-                                 _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out), DTYPE[out.dtype],
-                                 _ptr(final_state), int(bool(qk_norm)), float(q_scale), _ptr(norm_weight),
-                                 float(norm_eps), _stream_ptr(stream))
+    _same_device(q.device, k=k, v=v, log_alpha=log_alpha, beta=beta, cu_seqlens=cu_seqlens, init_state=init_state,
+                 out=out, final_state=final_state, norm_weight=norm_weight)
+    with torch.cuda.device(q.device):   # the scratch used is the one of the current device
+        st = lib.gdn_prefill_noalloc(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                     _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out),
+                                     DTYPE[out.dtype], _ptr(final_state), int(bool(qk_norm)), float(q_scale),
+                                     _ptr(norm_weight), float(norm_eps), _stream_ptr(stream, q.device))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill_noalloc")
     return out, final_state
@@ -287,6 +302,9 @@ class HostPrefillPlan:
                                  final_state is not None, algo)
         if staging is None:
             staging = torch.empty(need, dtype=torch.uint8, device=device or torch.device("cuda"))
+        if norm_weight is not None:
+            _same_device(staging.device, norm_weight=norm_weight)
+        self.device = staging.device
         self.out, self.final_state, self.staging = out, final_state, staging
         self.tensors = (q, k, v, log_alpha, beta, init_state, norm_weight)
         self.head = (n_seqs, T, hk, hv, dk, dv)
@@ -299,7 +317,9 @@ class HostPrefillPlan:
         self.d2h_bytes = sum(t.numel() * t.element_size() for t in (out, final_state) if t is not None)
 
     def run(self, stream=None):
-        st = self.lib.gdn_prefill_host(*self.head, *self.ptrs, *self.qk, *self.tail, _stream_ptr(stream))
+        with torch.cuda.device(self.device):
+            st = self.lib.gdn_prefill_host(*self.head, *self.ptrs, *self.qk, *self.tail,
+                                           _stream_ptr(stream, self.device))
         if st != GDN_OK:
             raise GdnError(st, "gdn_prefill_host")
         return self.out, self.final_state
@@ -311,7 +331,7 @@ def prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: t
     memory.  Keyword arguments as for ``HostPrefillPlan``."""
     plan = HostPrefillPlan(q, k, v, log_alpha, beta, cu_seqlens_host, **kw)
     plan.run(stream)
-    (stream or torch.cuda.current_stream()).synchronize()
+    (stream or torch.cuda.current_stream(plan.device)).synchronize()
     return plan.out, plan.final_state
 
 
@@ -353,16 +373,23 @@ class PrefillPlan:
         self.ws = (_ptr(workspace), ws_bytes)
         self.qk = (int(bool(qk_norm)), float(q_scale), _ptr(norm_weight), float(norm_eps))
         self.norm_weight = norm_weight
+        _same_device(q.device, k=k, v=v, log_alpha=log_alpha, beta=beta, cu_seqlens=cu_seqlens,
+                     init_state=init_state, out=out, final_state=final_state, norm_weight=norm_weight,
+                     workspace=workspace)
+        self.device = q.device
 
     def run(self, stream=None):
-        st = self.lib.gdn_prefill(*self.head, *self.ptrs, *self.qk, self.algo, *self.ws, _stream_ptr(stream))
+        with torch.cuda.device(self.device):
+            st = self.lib.gdn_prefill(*self.head, *self.ptrs, *self.qk, self.algo, *self.ws,
+                                      _stream_ptr(stream, self.device))
         if st != GDN_OK:
             raise GdnError(st, "gdn_prefill")
         return self.out, self.final_state
 
     def run_phase(self, phase: str, stream=None):
-        st = self.lib.gdn_prefill_chunked_phase(PHASE[phase], *self.head, *self.ptrs, *self.qk, *self.ws,
-                                                _stream_ptr(stream))
+        with torch.cuda.device(self.device):
+            st = self.lib.gdn_prefill_chunked_phase(PHASE[phase], *self.head, *self.ptrs, *self.qk, *self.ws,
+                                                    _stream_ptr(stream, self.device))
         if st != GDN_OK:
             raise GdnError(st, "gdn_prefill_chunked_phase")
 
@@ -385,17 +412,22 @@ def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.
     hv, dv = v.shape[1], v.shape[2]
     if out is None:
         out = torch.empty(n, hv, dv, device=q.device, dtype=out_dtype)
-    st = lib.gdn_decode_step(n, hk, hv, dk, dv, _ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
-                             _ptr(beta), _ptr(out), DTYPE[out.dtype], int(bool(qk_norm)), float(q_scale),
-                             _ptr(norm_weight), float(norm_eps), _stream_ptr(stream))
+    _same_device(state.device, q=q, k=k, v=v, log_alpha=log_alpha, beta=beta, out=out, norm_weight=norm_weight)
+    with torch.cuda.device(state.device):
+        st = lib.gdn_decode_step(n, hk, hv, dk, dv, _ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                 _ptr(beta), _ptr(out), DTYPE[out.dtype], int(bool(qk_norm)), float(q_scale),
+                                 _ptr(norm_weight), float(norm_eps), _stream_ptr(stream, state.device))
     if st != GDN_OK:
         raise GdnError(st, "gdn_decode_step")
     return out
 
 
-def device_error(stream=None) -> int:
-    """Synchronise and return the device-side error status (0 = none)."""
-    return int(load_library().gdn_device_error(_stream_ptr(stream)))
+def device_error(stream=None, device=None) -> int:
+    """Synchronise and return the device-side error status (0 = none) of ``device`` (default: the current
+    device; the error word is per device, shared by all of its streams)."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        return int(load_library().gdn_device_error(_stream_ptr(stream, device)))
 
 
 def selftest_bounded_wait(limit_us: int, stream=None) -> None:

@@ -21,12 +21,24 @@
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller, except the
  *     ones whose name ends in _host.  The library allocates nothing on these
- *     calls and keeps no state between calls, apart from one device-side
- *     error word (see gdn_device_error).
+ *     calls.  Between calls it keeps only:
+ *       - one error word per device, shared by all streams of that device
+ *         (see gdn_device_error);
+ *       - the fixed scratch array of gdn_prefill_noalloc, one per device,
+ *         which holds the last gdn_prefill_noalloc call's intermediates;
+ *       - host-side caches per device (kernel attributes, symbol addresses).
+ *   - Every device pointer, and the stream, must belong to the CURRENT device
+ *     (cudaSetDevice): the kernels are launched there.  Before launching, the
+ *     prefill calls check q, out, final_state and the workspace (decode:
+ *     state and out) with cudaPointerGetAttributes and return
+ *     GDN_ERR_INVALID_ARG for host memory or another device's memory.  The
+ *     check is skipped while the stream is capturing a CUDA graph.
  *   - Every tensor is dense, row-major, with the shape given below, and its
  *     base address is 16-byte aligned.
- *   - q and k are already L2-normalised and q is already scaled (e.g. by
- *     1/sqrt(dk)) by the caller; the library applies no normalisation.
+ *   - By default q and k are used exactly as given: the caller has already
+ *     L2-normalised them and scaled q (e.g. by 1/sqrt(dk)).  The qk_norm and
+ *     q_scale arguments are the one exception: they ask the kernels to do
+ *     that preparation themselves.
  *   - log_alpha must be <= 0 (it may be -INFINITY) and beta in [0, 1].  The
  *     GPU paths clamp log_alpha to >= -20 (alpha >= 2.1e-9) so that decay
  *     ratios inside a chunk stay finite; the effect is below fp32 resolution
@@ -212,7 +224,10 @@ GDN_API gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float 
 /*
  * Synchronise `stream` and return (and clear) the device-side error word the
  * kernels set when a bounded wait gives up (GDN_ERR_TIMEOUT) or an internal
- * check fails (GDN_ERR_INTERNAL).  GDN_OK when nothing was recorded.
+ * check fails (GDN_ERR_INTERNAL).  GDN_OK when nothing was recorded.  The word
+ * belongs to the current device, not to the stream: it collects what every
+ * call on that device recorded, whatever its stream, and reading it clears it
+ * for all of them.
  */
 GDN_API gdn_status gdn_device_error(void *stream);
 

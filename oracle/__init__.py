@@ -8,7 +8,8 @@ this module only compiles that file with the host C compiler and marshals
 numpy arrays across ctypes.
 
 Functions (all inputs numpy, see ``gdn_oracle.c`` for the definition):
-  prefill          sequential scan over packed sequences
+  prefill          sequential scan over packed sequences (optionally with the
+                   gates computed from raw inputs: gate_scale / gate_bias)
   prefill_chunked  blocked (chunked) evaluation of the same recurrence
   decode_step      one token applied to a batch of independent states
 
@@ -53,9 +54,9 @@ def _load():
             P = ctypes.c_void_p
             I = ctypes.c_int
             Dbl = ctypes.c_double
-            lib.gdn_oracle_prefill.argtypes = [I, P, I, I, I, I, P, P, P, P, P, P, P, P, I, Dbl, I]
+            lib.gdn_oracle_prefill.argtypes = [I, P, I, I, I, I, P, P, P, P, P, P, P, P, I, Dbl, P, P, I]
             lib.gdn_oracle_prefill_chunked.argtypes = [I, P, I, I, I, I, P, P, P, P, P, P, P, P, I, I, Dbl, I]
-            lib.gdn_oracle_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, Dbl, I]
+            lib.gdn_oracle_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, Dbl, P, P, I]
             for f in (lib.gdn_oracle_prefill, lib.gdn_oracle_prefill_chunked, lib.gdn_oracle_decode_step):
                 f.restype = I
             lib.gdn_oracle_max_threads.restype = I
@@ -98,12 +99,27 @@ def rms_norm(out, weight, eps):
     return o / np.sqrt((o * o).mean(axis=-1, keepdims=True) + float(eps)) * w
 
 
+def _gate_params(gate_scale, gate_bias, hv):
+    if (gate_scale is None) != (gate_bias is None):
+        raise ValueError("gate_scale and gate_bias go together")
+    if gate_scale is None:
+        return None, None
+    c, b = _f32(gate_scale), _f32(gate_bias)
+    if c.shape != (hv,) or b.shape != (hv,):
+        raise ValueError("gate_scale and gate_bias must be [hv]")
+    return c, b
+
+
 def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, n_threads=None,
-            want_out=True, qk_norm=False, q_scale=1.0, norm_weight=None, norm_eps=1e-6):
+            want_out=True, qk_norm=False, q_scale=1.0, norm_weight=None, norm_eps=1e-6,
+            gate_scale=None, gate_bias=None):
     """Sequential fp64 scan.  Returns (out [T,hv,dv] fp64 or None, final_state [N,hv,dv,dk] fp64).
 
     ``qk_norm``: L2-normalise every q and k head vector first (x / sqrt(|x|^2 + 1e-6)); q is then
-    multiplied by ``q_scale``.  ``norm_weight`` ([dv]): apply :func:`rms_norm` to the outputs."""
+    multiplied by ``q_scale``.  ``norm_weight`` ([dv]): apply :func:`rms_norm` to the outputs.
+    ``gate_scale`` / ``gate_bias`` ([hv] each): ``log_alpha`` and ``beta`` hold the raw per-token inputs
+    a and y, and the gates are log_alpha = -c_h softplus(a + b_h), beta = sigmoid(y) (see
+    ``gdn_oracle.c``)."""
     q, k, v = _f32(q), _f32(k), _f32(v)
     la, b = _f32(log_alpha), _f32(beta)
     T, hk, dk, hv, dv = _shapes(q, k, v)
@@ -112,11 +128,13 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, n_threads=
     if cu[0] != 0 or cu[-1] != T:
         raise ValueError("cu_seqlens must start at 0 and end at T")
     s0 = None if init_state is None else _f64(init_state)
+    gc, gb = _gate_params(gate_scale, gate_bias, hv)
     out = np.zeros((T, hv, dv), np.float64) if want_out else None
     fin = np.zeros((N, hv, dv, dk), np.float64)
     rc = _load().gdn_oracle_prefill(N, _ptr(cu), hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v),
                                     _ptr(la), _ptr(b), _ptr(s0), _ptr(out), _ptr(fin),
-                                    int(bool(qk_norm)), float(q_scale), int(n_threads or max_threads()))
+                                    int(bool(qk_norm)), float(q_scale), _ptr(gc), _ptr(gb),
+                                    int(n_threads or max_threads()))
     if rc:
         raise RuntimeError(f"gdn_oracle_prefill failed: {rc}")
     if norm_weight is not None and out is not None:
@@ -145,7 +163,7 @@ def prefill_chunked(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, ch
 
 
 def decode_step(state, q, k, v, log_alpha, beta, *, n_threads=None, qk_norm=False, q_scale=1.0,
-                norm_weight=None, norm_eps=1e-6):
+                norm_weight=None, norm_eps=1e-6, gate_scale=None, gate_bias=None):
     """One token per state.  state [n,hv,dv,dk]; q,k [n,hk,dk]; v [n,hv,dv]; gates [n,hv].
 
     Returns (out [n,hv,dv] fp64, new_state fp64); the input array is not modified.
@@ -156,10 +174,11 @@ def decode_step(state, q, k, v, log_alpha, beta, *, n_threads=None, qk_norm=Fals
     st = np.array(state, dtype=np.float64, order="C", copy=True)
     if st.shape != (n, hv, dv, dk):
         raise ValueError("state must be [n, hv, dv, dk]")
+    gc, gb = _gate_params(gate_scale, gate_bias, hv)
     out = np.zeros((n, hv, dv), np.float64)
     rc = _load().gdn_oracle_decode_step(n, hk, hv, dk, dv, _ptr(st), _ptr(q), _ptr(k), _ptr(v),
                                         _ptr(la), _ptr(b), _ptr(out), int(bool(qk_norm)), float(q_scale),
-                                        int(n_threads or max_threads()))
+                                        _ptr(gc), _ptr(gb), int(n_threads or max_threads()))
     if rc:
         raise RuntimeError(f"gdn_oracle_decode_step failed: {rc}")
     if norm_weight is not None:

@@ -34,8 +34,22 @@
  * replaced by x / sqrt(sum_j x_j^2 + 1e-6) before the recurrence; in every
  * case q is then multiplied by q_scale (1 leaves q as given).
  *
+ * Gates from raw inputs (optional, gate_scale != NULL): the pages' kernels
+ * carry "the state and its gate" in fp32 ("Keep recurrent state on chip") but
+ * print no gate formula.  The configured workloads draw the gates as
+ *     log_alpha = -c softplus(x + b),   beta = sigmoid(y),
+ * with x, y ~ N(0, 1) and (c, b) = (0.5, 2) for the model-shaped layers or
+ * (1, 0) for the tiny case.  Our reading of "computing the gates" is that map
+ * with one (c_h, b_h) per value head h: the log_alpha and beta arrays then
+ * hold the raw per-token projections a and y, gate_scale[h] = c_h >= 0 and
+ * gate_bias[h] = b_h, and per token
+ *     log_alpha = -c_h log(1 + e^{a + b_h}),   beta = 1 / (1 + e^{-y}),
+ * evaluated here in fp64 (softplus(x) as max(x, 0) + log(1 + e^{-|x|}), which
+ * neither overflows nor loses the small-x tail).
+ *
  * Layouts (row-major): q,k [T, hk, dk]; v [T, hv, dv]; log_alpha, beta
- * [T, hv]; state [n_seqs, hv, dv, dk] (row = value index); out [T, hv, dv].
+ * [T, hv]; state [n_seqs, hv, dv, dk] (row = value index); out [T, hv, dv];
+ * gate_scale, gate_bias [hv].
  * cu_seqlens [n_seqs + 1] holds token offsets of the packed sequences.
  *
  * Return value: 0 on success, a negative number for invalid arguments.
@@ -77,6 +91,22 @@ static void prep_qk(const float *q, const float *k, int dk, int qk_norm, double 
     }
 }
 
+/* The gates of one token of value head h (see the header): finished gates as given, or computed from the
+ * raw inputs when gate_scale is not NULL. */
+static void token_gates(const float *la, const float *bt, size_t idx, int h, const float *gate_scale,
+                        const float *gate_bias, double *log_alpha, double *beta)
+{
+    if (!gate_scale) {
+        *log_alpha = (double)la[idx];
+        *beta = (double)bt[idx];
+        return;
+    }
+    const double x = (double)la[idx] + (double)gate_bias[h];
+    const double softplus = (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
+    *log_alpha = -(double)gate_scale[h] * softplus;
+    *beta = 1.0 / (1.0 + exp(-(double)bt[idx]));
+}
+
 /* One token of the recurrence on one (sequence, head) state, fp64. */
 static void token_update(double *S, int dk, int dv, const double *q, const double *k,
                          const float *v, double log_alpha, double beta, double *o,
@@ -104,10 +134,12 @@ int gdn_oracle_prefill(int n_seqs, const int32_t *cu_seqlens, int hk, int hv, in
                        const float *q, const float *k, const float *v,
                        const float *log_alpha, const float *beta,
                        const double *init_state, double *out, double *final_state,
-                       int qk_norm, double q_scale, int n_threads)
+                       int qk_norm, double q_scale, const float *gate_scale, const float *gate_bias,
+                       int n_threads)
 {
     int rc = check_common(n_seqs, cu_seqlens, hk, hv, dk, dv);
     if (rc) return rc;
+    if ((gate_scale == NULL) != (gate_bias == NULL)) return -6;
     const int group = hv / hk;
     const long n_units = (long)n_seqs * hv;
     if (n_threads <= 0) n_threads = 1;
@@ -124,8 +156,9 @@ int gdn_oracle_prefill(int n_seqs, const int32_t *cu_seqlens, int hk, int hv, in
         else memset(S, 0, sizeof(double) * dv * dk);
         for (int t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
             prep_qk(q + ((size_t)t * hk + hq) * dk, k + ((size_t)t * hk + hq) * dk, dk, qk_norm, q_scale, qd, kd);
-            token_update(S, dk, dv, qd, kd, v + ((size_t)t * hv + h) * dv, log_alpha[(size_t)t * hv + h],
-                         beta[(size_t)t * hv + h], o, sk);
+            double la_t, b_t;
+            token_gates(log_alpha, beta, (size_t)t * hv + h, h, gate_scale, gate_bias, &la_t, &b_t);
+            token_update(S, dk, dv, qd, kd, v + ((size_t)t * hv + h) * dv, la_t, b_t, o, sk);
             if (out) memcpy(out + ((size_t)t * hv + h) * dv, o, sizeof(double) * dv);
         }
         if (final_state) memcpy(final_state + soff, S, sizeof(double) * dv * dk);
@@ -137,14 +170,17 @@ int gdn_oracle_prefill(int n_seqs, const int32_t *cu_seqlens, int hk, int hv, in
 /*
  * One decode step: the same token update applied to n independent states
  * (a batch of one token each), in place.  q,k [n, hk, dk]; v [n, hv, dv];
- * log_alpha, beta [n, hv]; state [n, hv, dv, dk]; out [n, hv, dv].
+ * log_alpha, beta [n, hv] (raw a, y with gate_scale / gate_bias [hv], as for
+ * the prefill); state [n, hv, dv, dk]; out [n, hv, dv].
  */
 int gdn_oracle_decode_step(int n, int hk, int hv, int dk, int dv, double *state,
                            const float *q, const float *k, const float *v,
                            const float *log_alpha, const float *beta, double *out,
-                           int qk_norm, double q_scale, int n_threads)
+                           int qk_norm, double q_scale, const float *gate_scale, const float *gate_bias,
+                           int n_threads)
 {
     if (n < 0 || hk <= 0 || hv <= 0 || dk <= 0 || dv <= 0 || hv % hk) return -1;
+    if ((gate_scale == NULL) != (gate_bias == NULL)) return -6;
     const int group = hv / hk;
     const long n_units = (long)n * hv;
     if (n_threads <= 0) n_threads = 1;
@@ -157,8 +193,9 @@ int gdn_oracle_decode_step(int n, int hk, int hv, int dk, int dv, double *state,
         double *qd = tmp + 2 * (size_t)dv, *kd = qd + dk;
         double *S = state + ((size_t)b * hv + h) * dv * dk;
         prep_qk(q + ((size_t)b * hk + hq) * dk, k + ((size_t)b * hk + hq) * dk, dk, qk_norm, q_scale, qd, kd);
-        token_update(S, dk, dv, qd, kd, v + ((size_t)b * hv + h) * dv, log_alpha[(size_t)b * hv + h],
-                     beta[(size_t)b * hv + h], tmp + dv, tmp);
+        double la_t, b_t;
+        token_gates(log_alpha, beta, (size_t)b * hv + h, h, gate_scale, gate_bias, &la_t, &b_t);
+        token_update(S, dk, dv, qd, kd, v + ((size_t)b * hv + h) * dv, la_t, b_t, tmp + dv, tmp);
         if (out) memcpy(out + ((size_t)b * hv + h) * dv, tmp + dv, sizeof(double) * dv);
         free(tmp);
     }

@@ -240,3 +240,44 @@ def test_selftest_bounded_wait_rejects_limits_out_of_range(lib):
     # validated on the host before anything is launched
     for bad in (0, -5, 1000001):
         assert lib.gdn_selftest_bounded_wait(bad, None) == 1  # GDN_ERR_INVALID_ARG
+
+
+def test_pointers_off_the_current_device_are_refused(lib):
+    """A well-formed call whose pointers are not device memory of the current device is refused before any
+    launch: GDN_ERR_INVALID_ARG where a GPU is present, GDN_ERR_CUDA (the runtime cannot be asked) without
+    one.  FAKE is an address that no allocation owns."""
+    allowed = {1, 4}
+    assert prefill(lib) in allowed
+    assert prefill_host(lib, stgb=1 << 40) in allowed
+
+    def dec():
+        P = ctypes.c_void_p
+        return lib.gdn_decode_step(1, 1, 2, 128, 128, P(FAKE), P(FAKE * 2), P(FAKE * 3), P(FAKE * 4), P(FAKE * 5),
+                                   P(FAKE * 6), P(FAKE * 7), 0, 0, 1.0, None, 1e-6, None)
+    assert dec() in allowed
+
+
+@pytest.mark.gpu
+def test_host_memory_is_refused_on_a_gpu(lib):
+    """Host tensors in place of device tensors: GDN_ERR_INVALID_ARG, nothing launched, no device error."""
+    import torch
+    from gated_deltanet_linear_03_gb300 import gdn, synth
+    inp = synth.prefill_inputs([64], hk=1, hv=2, seed=3)
+    dev = torch.device("cuda:0")
+    d = [t.to(dev) for t in (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.cu_seqlens)]
+    out_dev = torch.empty(64, 2, 128, dtype=torch.bfloat16, device=dev)
+    P = ctypes.c_void_p
+    host_q = inp.q.contiguous()
+    cu = _cu(inp.cu_seqlens.tolist())
+    with torch.cuda.device(dev):
+        for q_ptr, out_ptr in ((host_q.data_ptr(), out_dev.data_ptr()), (d[0].data_ptr(), host_q.data_ptr())):
+            st = lib.gdn_prefill(1, 64, 1, 2, 128, 128, P(q_ptr), P(d[1].data_ptr()), P(d[2].data_ptr()),
+                                 P(d[3].data_ptr()), P(d[4].data_ptr()), None, P(d[5].data_ptr()), cu, P(out_ptr), 0,
+                                 None, 0, 1.0, None, 1e-6, 1, None, 0, None)
+            assert st == 1
+        state = torch.zeros(1, 2, 128, 128, dtype=torch.float32)            # host state
+        st = lib.gdn_decode_step(1, 1, 2, 128, 128, P(state.data_ptr()), P(d[0].data_ptr()), P(d[1].data_ptr()),
+                                 P(d[2].data_ptr()), P(d[3].data_ptr()), P(d[4].data_ptr()), P(out_dev.data_ptr()),
+                                 0, 0, 1.0, None, 1e-6, None)
+        assert st == 1
+    assert gdn.device_error() == 0

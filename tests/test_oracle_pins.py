@@ -438,3 +438,95 @@ def test_pins_catch_a_planted_mistake():
     _, ref = literal(q, k, v, la, b, s0)
     np.testing.assert_allclose(fin, ref, atol=1e-12)
     assert np.max(np.abs(S - ref[0, 0])) > 1e-3
+
+
+# ---------------------------------------------------------------- gates computed from raw inputs
+# log_alpha = -c_h softplus(a + b_h), beta = sigmoid(y) (the configured workloads' gate recipe with per-head
+# parameters).  A one-token step from S0 = e_0 e_1^T with k = e_0 and q = e_1 gives, by hand,
+#     S1 = alpha S0 (I - beta e_0 e_0^T) + beta v e_0^T = [[0, alpha], [beta v_1 ... ]]
+# (S0 e_0 = 0), so S1[0, 1] = alpha and, with v = e_1, S1[1, 0] = beta: the gates can be read off the state.
+
+def _gate_probe(a, y, c, b):
+    """alpha and beta the oracle applies for raw inputs a, y (arrays [n]) and head parameters c, b."""
+    n = len(a)
+    s0 = np.zeros((n, 1, 2, 2))
+    s0[:, 0, 0, 1] = 1.0
+    e0 = np.tile(np.array([1, 0], np.float32), (n, 1, 1))
+    e1 = np.tile(np.array([0, 1], np.float32), (n, 1, 1))
+    la = np.asarray(a, np.float32).reshape(n, 1)
+    bt = np.asarray(y, np.float32).reshape(n, 1)
+    out, s1 = oracle.decode_step(s0, e1, e0, e1, la, bt, gate_scale=np.array([c], np.float32),
+                                 gate_bias=np.array([b], np.float32))
+    np.testing.assert_array_equal(s1[:, 0, 0, 0], 0.0)
+    np.testing.assert_allclose(out[:, 0, 0], s1[:, 0, 0, 1], rtol=1e-15)   # o = S1 e_1: (alpha, 0)
+    return s1[:, 0, 0, 1], s1[:, 0, 1, 0]
+
+
+def test_gates_by_hand():
+    # softplus(ln(e - 1)) = 1 and sigmoid(ln 3) = 3/4; softplus(0) = ln 2 and sigmoid(0) = 1/2
+    a = np.float32(math.log(math.e - 1.0))
+    alpha, beta = _gate_probe([a, 0.0], [math.log(3.0), 0.0], 0.5, 0.0)
+    np.testing.assert_allclose(alpha[0], math.exp(-0.5 * math.log1p(math.exp(float(a)))), rtol=1e-14)
+    np.testing.assert_allclose(alpha[0], math.exp(-0.5), rtol=1e-6)       # a is ln(e - 1) rounded to fp32
+    np.testing.assert_allclose(beta[0], 0.75, rtol=1e-7)                  # ln 3 rounded to fp32
+    np.testing.assert_allclose(alpha[1], 2.0 ** -0.5, rtol=1e-15)         # exp(-0.5 ln 2)
+    np.testing.assert_allclose(beta[1], 0.5, rtol=1e-15)
+    # the bias shifts the argument: a + b = 0 with b = 3
+    alpha, _ = _gate_probe([-3.0], [0.0], 2.0, 3.0)
+    np.testing.assert_allclose(alpha[0], 0.25, rtol=1e-15)                # exp(-2 ln 2)
+
+
+def test_gates_tails():
+    # softplus(x) -> x for large x, -> e^x for very negative x (kept, not rounded to 0)
+    alpha, beta = _gate_probe([30.0, -40.0], [40.0, -40.0], 0.5, 0.0)
+    np.testing.assert_allclose(alpha[0], math.exp(-0.5 * (30.0 + math.exp(-30.0))), rtol=1e-14)
+    np.testing.assert_allclose(beta[0], 1.0, rtol=1e-15)
+    np.testing.assert_allclose(beta[1], math.exp(-40.0), rtol=1e-6)
+    # a large scale makes the small-x tail visible in alpha: -log alpha = c softplus(-30) = c e^-30 (1 - ...)
+    alpha, _ = _gate_probe([-30.0], [0.0], 1.0e6, 0.0)
+    np.testing.assert_allclose(-math.log(alpha[0]), 1.0e6 * math.log1p(math.exp(-30.0)), rtol=1e-8)
+    np.testing.assert_allclose(-math.log(alpha[0]), 1.0e6 * math.exp(-30.0), rtol=1e-8)
+
+
+def test_gates_are_in_range_and_monotone():
+    rng = np.random.default_rng(5)
+    a = np.sort(rng.standard_normal(64).astype(np.float32) * 4)
+    y = np.sort(rng.standard_normal(64).astype(np.float32) * 4)
+    alpha, beta = _gate_probe(a, y, 0.7, 1.3)
+    assert np.all(alpha > 0) and np.all(alpha <= 1) and np.all(beta > 0) and np.all(beta < 1)
+    assert np.all(np.diff(alpha) <= 0) and np.all(np.diff(beta) >= 0)    # alpha falls with a, beta rises with y
+    alpha0, _ = _gate_probe(a, y, 0.0, 1.3)
+    np.testing.assert_array_equal(alpha0, 1.0)                            # c = 0: nothing decays
+
+
+def test_gates_reproduce_the_configured_recipe():
+    """With c = 0.5, b = 2 (model) or c = 1, b = 0 (tiny) the map is the configs' own gate recipe, drawn by the
+    input generator with a library softplus/sigmoid on the same normal variates."""
+    from gated_deltanet_linear_03_gb300 import synth
+    for kind, kw in (("model", dict(hk=2, hv=4, dk=8, dv=8)), ("tiny", dict(hk=2, hv=2, dk=8, dv=8))):
+        fin_gates = synth.prefill_inputs([50, 30], seed=11, gates=kind, init_std=0.1, **kw)
+        raw = synth.prefill_inputs([50, 30], seed=11, gates=kind, init_std=0.1, raw_gates="config", **kw)
+        args = lambda x: (x.q.float().numpy(), x.k.float().numpy(), x.v.float().numpy())
+        cu = raw.cu_seqlens.numpy()
+        s0 = raw.init_state.double().numpy()
+        o1, f1 = oracle.prefill(*args(fin_gates), fin_gates.log_alpha.numpy(), fin_gates.beta.numpy(), cu, s0)
+        o2, f2 = oracle.prefill(*args(raw), raw.log_alpha.numpy(), raw.beta.numpy(), cu, s0,
+                                gate_scale=raw.gate_scale.numpy(), gate_bias=raw.gate_bias.numpy())
+        # the generator's gates are fp32 values of the same map: agreement to fp32 rounding of the gates
+        np.testing.assert_allclose(o2, o1, rtol=2e-5, atol=2e-6)
+        np.testing.assert_allclose(f2, f1, rtol=2e-5, atol=2e-6)
+
+
+def test_gates_decode_chain_equals_prefill():
+    from gated_deltanet_linear_03_gb300 import synth
+    inp = synth.prefill_inputs([40], hk=2, hv=4, dk=8, dv=8, seed=12, init_std=0.1, raw_gates="per_head")
+    g = dict(gate_scale=inp.gate_scale.numpy(), gate_bias=inp.gate_bias.numpy())
+    q, k, v = inp.q.float().numpy(), inp.k.float().numpy(), inp.v.float().numpy()
+    out, fin = oracle.prefill(q, k, v, inp.log_alpha.numpy(), inp.beta.numpy(), inp.cu_seqlens.numpy(),
+                              inp.init_state.double().numpy(), **g)
+    st = inp.init_state.double().numpy()
+    for t in range(40):
+        o, st = oracle.decode_step(st, q[t:t + 1], k[t:t + 1], v[t:t + 1], inp.log_alpha.numpy()[t:t + 1],
+                                   inp.beta.numpy()[t:t + 1], **g)
+        np.testing.assert_allclose(o[0], out[t], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(st, fin, rtol=1e-12, atol=1e-14)

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from gated_deltanet_linear_03_gb300 import synth
-from helpers import OUT_ATOL, STATE_RTOL, to_device
+from helpers import to_device
 
 
 @pytest.fixture(scope="module")
@@ -39,13 +39,15 @@ def _pair(gdn, inp):
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_twice(gdn):
-    cases = [synth.prefill_inputs([300, 65, 1], hk=4, hv=8, seed=71, init_std=0.02),
-             synth.prefill_inputs([4096], seed=72)]          # the largest size the scratch holds
-    for inp in cases:                                         # two calls in a row on the shared scratch
+    """The same kernels on the same inputs as gdn_prefill, so the results must be identical bit for bit.  The
+    small ragged case runs again after the 4096-token case, so that its second call finds the larger call's
+    contents still in the shared scratch."""
+    small = synth.prefill_inputs([300, 65, 1], hk=4, hv=8, seed=71, init_std=0.02)
+    large = synth.prefill_inputs([4096], seed=72)             # the largest size the scratch holds
+    for inp in (small, large, small):                         # calls in a row on the shared scratch
         out, fin, ref_out, ref_fin = _pair(gdn, inp)
-        assert (out - ref_out).abs().max().item() <= OUT_ATOL
-        rel = ((fin - ref_fin).flatten(2).norm(dim=-1) / ref_fin.flatten(2).norm(dim=-1).clamp_min(1e-30)).max()
-        assert rel.item() <= STATE_RTOL
+        assert torch.equal(out, ref_out)
+        assert torch.equal(fin, ref_fin)
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(gdn):
