@@ -307,7 +307,9 @@ def time_decode_per_layer(dev, stream, steps=64, n_rep=5):
 
 def time_qk_prep(dev, stream, iters=20):
     """The 4K layer from raw q/k projections: L2 normalisation and q scaling fused into the kernels
-    (qk_norm), against the same done as a separate PyTorch pass before the plain call."""
+    (qk_norm), against the same done as a separate PyTorch pass before the plain call; then also from raw
+    gate projections (log_alpha = -c softplus(a + b), beta = sigmoid(y) formed in the kernels), against
+    PyTorch computing q/k and the gates before the plain call."""
     import torch
     import torch.nn.functional as F
     from gated_deltanet_linear_03_gb300 import gdn, synth
@@ -327,9 +329,27 @@ def time_qk_prep(dev, stream, iters=20):
 
     w = torch.linspace(0.5, 2.0, D, device=dev)
     normed = gdn.PrefillPlan(q, k, v, la, b, cu, cu_seqlens_host=cu_host, qk_norm=True, q_scale=scale, norm_weight=w)
+    # raw gates with the model recipe's parameters (c = 0.5, b = 2 on every value head)
+    rg = synth.prefill_inputs([T_TOKENS], hk=HK, hv=HV, dk=D, dv=D, seed=1001, raw_qk=True, raw_gates="config")
+    ga, gy = rg.log_alpha.to(dev), rg.beta.to(dev)
+    gc, gbias = rg.gate_scale.to(dev), rg.gate_bias.to(dev)
+    gated = gdn.PrefillPlan(q, k, v, ga, gy, cu, cu_seqlens_host=cu_host, qk_norm=True, q_scale=scale,
+                            gate_scale=gc, gate_bias=gbias)
+    la_s, b_s = torch.empty_like(ga), torch.empty_like(gy)
+    plain_g = gdn.PrefillPlan(qn, kn, v, la_s, b_s, cu, cu_seqlens_host=cu_host)
+
+    def separate_gates():
+        qn.copy_((F.normalize(q.float(), dim=-1, eps=1e-3) * scale).to(torch.bfloat16))
+        kn.copy_(F.normalize(k.float(), dim=-1, eps=1e-3).to(torch.bfloat16))
+        la_s.copy_(-gc * F.softplus(ga + gbias))
+        b_s.copy_(torch.sigmoid(gy))
+        plain_g.run(stream=stream)
+
     res = {}
     for name, fn in (("fused_us", lambda: fused.run(stream=stream)), ("separate_pass_us", separate),
-                     ("fused_with_output_norm_us", lambda: normed.run(stream=stream))):
+                     ("fused_with_output_norm_us", lambda: normed.run(stream=stream)),
+                     ("fused_with_gates_us", lambda: gated.run(stream=stream)),
+                     ("separate_pass_with_gates_us", separate_gates)):
         with torch.cuda.stream(stream):
             for _ in range(3):
                 fn()
@@ -341,8 +361,9 @@ def time_qk_prep(dev, stream, iters=20):
             e0.record(stream)
         torch.cuda.synchronize()
         res[name] = s0.elapsed_time(e0) * 1e3 / iters
-    res["workload"] = ("4K layer from raw q/k projections (L2-normalise q and k, q / sqrt(d)); the last key also "
-                       "fuses the output normalisation")
+    res["workload"] = ("4K layer from raw q/k projections (L2-normalise q and k, q / sqrt(d)); "
+                       "fused_with_output_norm_us also fuses the output normalisation; *_with_gates_us start from "
+                       "raw gate projections too (log_alpha = -0.5 softplus(a + 2), beta = sigmoid(y))")
     return res
 
 

@@ -304,14 +304,16 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
 }
 
 // PREP: query/key preparation (qk_norm, or q_scale != 1); the plain instantiation has none of its arithmetic.
-template <bool PREP>
+// GATE: the gates are formed from raw inputs (gdn.h: gate_scale, gate_bias).
+template <bool PREP, bool GATE>
 __global__ void __launch_bounds__(kPrepThreads, 3)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
                   const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
                   const float *__restrict__ log_alpha, const float *__restrict__ beta,
                   const int32_t *__restrict__ cu, int n_seqs, int total, int hk, int hv, float *__restrict__ norms,
-                  int qk_norm, float q_scale, unsigned int *err) {
+                  int qk_norm, float q_scale, const float *__restrict__ gate_c, const float *__restrict__ gate_b,
+                  unsigned int *err) {
     extern __shared__ uint8_t prep_raw[];
     uint8_t *sm = align1024(prep_raw);
     __shared__ uint64_t bar_tma, bar_mma;
@@ -423,6 +425,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         if (ok && qk_norm) norms[((size_t)gc * hv + h) * 128 + tid] = f;   // read by the pass only with qk_norm
     }
     if (warp == 1) {
+        if (GATE) {   // the gates from raw inputs, formed while the loads' latency was covered by the MMA wait
+            if (2 * lane < L) {
+                la0 = gate_log_alpha(la0, gate_c, gate_b, h);
+                bt0 = gate_beta(bt0, gate_c);
+            }
+            if (2 * lane + 1 < L) {
+                la1 = gate_log_alpha(la1, gate_c, gate_b, h);
+                bt1 = gate_beta(bt1, gate_c);
+            }
+        }
         const float2 g2 = cumsum_pairs(la0, la1, L, lane);
         const float gl = g_of(g2, L - 1);
         g_s[2 * lane] = g2.x;
@@ -747,6 +759,19 @@ __device__ __forceinline__ void load_chunk_inputs(ChunkInputs &in, const float *
 }
 
 
+// GATE: the gates of a chunk from raw inputs, formed when the chunk is used (one chunk after its loads were
+// issued, so their latency stays hidden): log_alpha of tokens 2 lane and 2 lane + 1, beta of this thread's
+// token.  Positions past the chunk's end keep their zeros.
+template <bool GATE>
+__device__ __forceinline__ void finish_gates(ChunkInputs &in, int L, int lane, bool krow, int i,
+                                             const float *__restrict__ gate_c, const float *__restrict__ gate_b,
+                                             int h) {
+    if (!GATE) return;
+    if (2 * lane < L) in.la0 = gate_log_alpha(in.la0, gate_c, gate_b, h);
+    if (2 * lane + 1 < L) in.la1 = gate_log_alpha(in.la1, gate_c, gate_b, h);
+    if (krow && i < L) in.b = gate_beta(in.b, gate_c);
+}
+
 // Outputs of one chunk for this thread's token and 16 value rows (Q-row threads):
 // O_i = e^{g_i} (Q S^T)_i (in qs) + (R X)_i ((R_hi + R_lo) X_hi, and (R_hi + R_lo) X_lo).
 // outputs_begin adds R X into qs; outputs_end writes them.  NORM: the output normalisation over the head's
@@ -811,6 +836,8 @@ __device__ __forceinline__ void outputs_end(float (&qs)[DG], int grp, int i, int
 // Thread 0 issues the [Q;K] S^T MMAs and thread 32 the TMA loads (both Q-row threads, which have nothing
 // to do before the X barrier); threads kPxIssuer and kRxIssuer (K-row threads, which have nothing to do
 // between the X barrier and the state update) issue P X and R X.
+// GATE: the gates are formed from raw inputs (gdn.h: gate_scale, gate_bias).
+template <bool GATE>
 __global__ void __launch_bounds__(kPassThreads, 1)
 state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
@@ -819,7 +846,8 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
                   const float *__restrict__ log_alpha, const float *__restrict__ beta,
                   const float *__restrict__ init_state, const int32_t *__restrict__ cu, int n_seqs, int total,
                   int nch, int hk, int hv, void *__restrict__ out, int out_f32, float *__restrict__ final_state,
-                  const float *__restrict__ norm_w, float norm_eps, unsigned int *err) {
+                  const float *__restrict__ norm_w, float norm_eps, const float *__restrict__ gate_c,
+                  const float *__restrict__ gate_b, unsigned int *err) {
     extern __shared__ uint8_t pass_raw[];
     uint8_t *sm = align1024(pass_raw);
     __shared__ uint64_t bar_tma[2], bar_d1, bar_px, bar_rx[2];
@@ -941,7 +969,8 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         const uint32_t par = c & 1;
         const int t0 = ta + c * C, L = min(C, tb - t0);
         const int gc = gc0 + c;
-        const ChunkInputs cur = nxt;
+        ChunkInputs cur = nxt;
+        finish_gates<GATE>(cur, L, lane, krow, i, gate_c, gate_b, h);
         const uint64_t so = s * kStageStep;
 
         if (tid == 0) {
@@ -1134,6 +1163,7 @@ constexpr int kWsThreads = kPassThreads + 64;
 constexpr int kMmaWarp = kPassThreads / 32, kTmaWarp = kMmaWarp + 1;
 constexpr uint32_t kPTx = 16384 + 16384, kRTx = 8192 + 8192;
 
+template <bool GATE>
 __global__ void __launch_bounds__(kWsThreads, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
@@ -1142,7 +1172,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                   const float *__restrict__ log_alpha, const float *__restrict__ beta,
                   const float *__restrict__ init_state, const int32_t *__restrict__ cu, int n_seqs, int total,
                   int nch, int hk, int hv, void *__restrict__ out, int out_f32, float *__restrict__ final_state,
-                  unsigned int *err) {
+                  const float *__restrict__ gate_c, const float *__restrict__ gate_b, unsigned int *err) {
     extern __shared__ uint8_t pass_raw[];
     uint8_t *sm = align1024(pass_raw);
     __shared__ uint64_t bar_qk[2], bar_p[2], bar_r[2], bar_qkf[2], bar_pf[2], bar_rf[2];
@@ -1376,7 +1406,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             }
             const uint32_t par = c & 1;
             const int t0 = ta + c * C, L = min(C, tb - t0);
-            const ChunkInputs cur = nxt;
+            ChunkInputs cur = nxt;
+            finish_gates<GATE>(cur, L, lane, krow, i, gate_c, gate_b, h);
             if (c + 1 < nchunks)
                 load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0 + c + 1, t0 + C, min(C, tb - t0 - C),
                                   hv, h, rowg, lane, krow, i);
@@ -1529,13 +1560,14 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
     static std::atomic<bool> attrs_set[kMaxDevices];
     const bool cached = dev >= 0 && dev < kMaxDevices;
     if (!cached || !attrs_set[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(state_pass_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
+        const void *prep[] = {(const void *)chunk_prep_kernel<false, false>, (const void *)chunk_prep_kernel<true, false>,
+                              (const void *)chunk_prep_kernel<false, true>, (const void *)chunk_prep_kernel<true, true>};
+        const void *pass[] = {(const void *)state_pass_kernel<false>, (const void *)state_pass_kernel<true>,
+                              (const void *)state_pass_norm_kernel<false>, (const void *)state_pass_norm_kernel<true>};
+        for (const void *f : prep)
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+        for (const void *f : pass)
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, PASS_SMEM);
         if (e != cudaSuccess) return e;
         if (cached) attrs_set[dev].store(true, std::memory_order_release);
     }
@@ -1550,16 +1582,14 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
             return cudaErrorInvalidValue;
     }
 
+    const bool prep_qk = p.qk_norm || p.q_scale != 1.f, gate = p.gate_c != nullptr;
     if ((phases & 1) && nch > 0) {
         dim3 grid((unsigned)nch, (unsigned)p.hv);
-        if (p.qk_norm || p.q_scale != 1.f)
-            chunk_prep_kernel<true><<<grid, kPrepThreads, PREP_SMEM, p.stream>>>(
-                qmap, kmap, phmap, plmap, rhmap, rlmap, p.log_alpha, p.beta, p.cu_seqlens, p.n_seqs, p.total_tokens,
-                p.hk, p.hv, norms, p.qk_norm, p.q_scale, p.err);
-        else
-            chunk_prep_kernel<false><<<grid, kPrepThreads, PREP_SMEM, p.stream>>>(
-                qmap, kmap, phmap, plmap, rhmap, rlmap, p.log_alpha, p.beta, p.cu_seqlens, p.n_seqs, p.total_tokens,
-                p.hk, p.hv, norms, p.qk_norm, p.q_scale, p.err);
+        auto prep = prep_qk ? (gate ? chunk_prep_kernel<true, true> : chunk_prep_kernel<true, false>)
+                            : (gate ? chunk_prep_kernel<false, true> : chunk_prep_kernel<false, false>);
+        prep<<<grid, kPrepThreads, PREP_SMEM, p.stream>>>(qmap, kmap, phmap, plmap, rhmap, rlmap, p.log_alpha,
+                                                           p.beta, p.cu_seqlens, p.n_seqs, p.total_tokens, p.hk, p.hv,
+                                                           norms, p.qk_norm, p.q_scale, p.gate_c, p.gate_b, p.err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
@@ -1579,14 +1609,16 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
             cfg.stream = p.stream;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            e = cudaLaunchKernelEx(&cfg, state_pass_norm_kernel, qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm,
-                                   p.q_scale, p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.n_seqs,
-                                   p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state, p.norm_w,
-                                   p.norm_eps, p.err);
+            e = cudaLaunchKernelEx(&cfg, gate ? state_pass_norm_kernel<true> : state_pass_norm_kernel<false>, qmap,
+                                   kmap, phmap, plmap, rhmap, rlmap, p.v, nrm, p.q_scale, p.log_alpha, p.beta,
+                                   p.init_state, p.cu_seqlens, p.n_seqs, p.total_tokens, (int)nch, p.hk, p.hv, p.out,
+                                   p.out_f32, p.final_state, p.norm_w, p.norm_eps, p.gate_c, p.gate_b, p.err);
         } else {
-            state_pass_kernel<<<grid2, kWsThreads, PASS_SMEM, p.stream>>>(
+            auto pass = gate ? state_pass_kernel<true> : state_pass_kernel<false>;
+            pass<<<grid2, kWsThreads, PASS_SMEM, p.stream>>>(
                 qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm, p.q_scale, p.log_alpha, p.beta, p.init_state,
-                p.cu_seqlens, p.n_seqs, p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state, p.err);
+                p.cu_seqlens, p.n_seqs, p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state,
+                p.gate_c, p.gate_b, p.err);
             e = cudaSuccess;
         }
         if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;

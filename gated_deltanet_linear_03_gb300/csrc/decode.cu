@@ -66,7 +66,8 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
                    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                    const __nv_bfloat16 *__restrict__ v, const float *__restrict__ log_alpha,
                    const float *__restrict__ beta, void *__restrict__ out, int out_f32, int qk_norm,
-                   float q_scale, const float *__restrict__ norm_w, float norm_eps) {
+                   float q_scale, const float *__restrict__ norm_w, float norm_eps,
+                   const float *__restrict__ gate_c, const float *__restrict__ gate_b) {
     constexpr int LPR = D / 4;                  // lanes per row
     constexpr int GROUPS = 32 / LPR;            // lane groups per warp
     constexpr int WARP_ROWS = GROUPS * kRowsPerGroup;
@@ -117,9 +118,9 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
     }
     if (PREP) kq *= fk * fq;
 
-    const float la = clamp_log_alpha(log_alpha[head]);
+    const float la = clamp_log_alpha(gate_log_alpha(log_alpha[head], gate_c, gate_b, h));
     const float alpha = __expf(la);
-    const float b = beta[head];
+    const float b = gate_beta(beta[head], gate_c);
 
     float part[16];
 #pragma unroll
@@ -240,7 +241,8 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
                      const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
                      void *__restrict__ out, int out_f32, float *__restrict__ final_state, int qk_norm,
-                     float q_scale, const float *__restrict__ norm_w, float norm_eps) {
+                     float q_scale, const float *__restrict__ norm_w, float norm_eps,
+                     const float *__restrict__ gate_c, const float *__restrict__ gate_b) {
     constexpr int LPR = D / 4, GROUPS = 32 / LPR, ROWS = short_rows<D>(), SLICES = D / ROWS;
     constexpr int NT = short_warps<D>() * 32;
     constexpr int PER = (16 / LPR) > 0 ? (16 / LPR) : 1;
@@ -270,8 +272,8 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
             *reinterpret_cast<const uint4 *>(v + ((size_t)(tbeg + t) * hv + h) * D + slice * ROWS + c * 8);
     }
     for (int t = tid; t < L; t += NT) {
-        sm.alpha[t] = __expf(clamp_log_alpha(log_alpha[(size_t)(tbeg + t) * hv + h]));
-        sm.beta[t] = beta[(size_t)(tbeg + t) * hv + h];
+        sm.alpha[t] = __expf(clamp_log_alpha(gate_log_alpha(log_alpha[(size_t)(tbeg + t) * hv + h], gate_c, gate_b, h)));
+        sm.beta[t] = gate_beta(beta[(size_t)(tbeg + t) * hv + h], gate_c);
     }
 
     // this lane group's 8 state rows, 4 columns per lane
@@ -437,7 +439,8 @@ cudaError_t launch_short_dn(const PrefillProblem &p) {
     cfg.numAttrs = (NORM && SLICES > 1) ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, short_prefill_kernel<D, NORM>, p.total_tokens, p.hk, p.hv, p.q, p.k, p.v,
                                              p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.out, p.out_f32,
-                                             p.final_state, p.qk_norm, p.q_scale, p.norm_w, p.norm_eps);
+                                             p.final_state, p.qk_norm, p.q_scale, p.norm_w, p.norm_eps, p.gate_c,
+                                             p.gate_b);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -475,7 +478,7 @@ cudaError_t launch_decode_d(const DecodeProblem &p, unsigned grid) {
     cfg.numAttrs = (NORM && D == 128) ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_step_kernel<D, PREP, NORM>, (int)((long)p.n * p.hv * p.d), p.hk,
                                              p.hv, p.state, p.q, p.k, p.v, p.log_alpha, p.beta, p.out, p.out_f32,
-                                             p.qk_norm, p.q_scale, p.norm_w, p.norm_eps);
+                                             p.qk_norm, p.q_scale, p.norm_w, p.norm_eps, p.gate_c, p.gate_b);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -30,6 +30,13 @@ gdn_status check_heads(int hk, int hv, int dk, int dv) {
     return GDN_OK;
 }
 
+// The gate parameters come as a pair (both null: log_alpha and beta are the gates themselves).
+gdn_status check_gate_params(const float *gate_scale, const float *gate_bias) {
+    if ((gate_scale == nullptr) != (gate_bias == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (gate_scale && (!aligned16(gate_scale) || !aligned16(gate_bias))) return GDN_ERR_ALIGNMENT;
+    return GDN_OK;
+}
+
 gdn_status check_cu(int n_seqs, int total_tokens, const int32_t *cu_host) {
     if (n_seqs <= 0 || total_tokens < 0 || !cu_host) return GDN_ERR_INVALID_ARG;
     if (cu_host[0] != 0 || cu_host[n_seqs] != total_tokens) return GDN_ERR_INVALID_ARG;
@@ -125,7 +132,7 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned int *err) {
 
 extern "C" {
 
-int gdn_version(void) { return 103; }
+int gdn_version(void) { return 200; }
 
 const char *gdn_status_string(gdn_status s) {
     switch (s) {
@@ -166,10 +173,11 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
                        const float *init_state,
                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                        void *out, int out_dtype, float *final_state, int qk_norm, float q_scale,
-                       const float *norm_weight, float norm_eps,
+                       const float *norm_weight, float norm_eps, const float *gate_scale, const float *gate_bias,
                        int algo, void *workspace, size_t workspace_bytes, void *stream, int phases) {
     gdn_status st = check_heads(hk, hv, dk, dv);
     if (st != GDN_OK) return st;
+    if ((st = check_gate_params(gate_scale, gate_bias)) != GDN_OK) return st;
     if ((qk_norm != 0 && qk_norm != 1) || !isfinite(q_scale)) return GDN_ERR_INVALID_ARG;
     if (norm_weight && (!isfinite(norm_eps) || norm_eps < 0.f)) return GDN_ERR_INVALID_ARG;
     if (norm_weight && !aligned16(norm_weight)) return GDN_ERR_ALIGNMENT;
@@ -190,7 +198,7 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
     const struct { const void *p; size_t n; } inputs[] = {
         {q, T * hk * dk * 2}, {k, T * hk * dk * 2}, {v, T * hv * dv * 2},
         {log_alpha, T * hv * 4}, {beta, T * hv * 4}, {cu_seqlens, (size_t)(n_seqs + 1) * 4},
-        {init_state, state_bytes}};
+        {init_state, state_bytes}, {gate_scale, (size_t)hv * 4}, {gate_bias, (size_t)hv * 4}};
     for (const auto &in : inputs) {
         if (overlaps(out, out_bytes, in.p, in.n)) return GDN_ERR_INVALID_ARG;
         if (in.p != init_state && overlaps(final_state, state_bytes, in.p, in.n)) return GDN_ERR_INVALID_ARG;
@@ -230,6 +238,7 @@ static gdn_status prefill_impl(int n_seqs, int total_tokens, int hk, int hv, int
     p.out = out; p.out_f32 = out_dtype == GDN_DTYPE_F32; p.final_state = final_state;
     p.qk_norm = qk_norm; p.q_scale = q_scale;
     p.norm_w = norm_weight; p.norm_eps = norm_eps;
+    p.gate_c = gate_scale; p.gate_b = gate_bias;
     p.workspace = workspace; p.workspace_bytes = workspace_bytes;
     p.err = device_error_ptr();
     p.stream = static_cast<cudaStream_t>(stream);
@@ -260,11 +269,11 @@ gdn_status gdn_prefill(int n_seqs, int total_tokens, int hk, int hv, int dk, int
                        const float *init_state,
                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                        void *out, int out_dtype, float *final_state, int qk_norm, float q_scale,
-                       const float *norm_weight, float norm_eps,
+                       const float *norm_weight, float norm_eps, const float *gate_scale, const float *gate_bias,
                        int algo, void *workspace, size_t workspace_bytes, void *stream) {
     return prefill_impl(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
-                        cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, norm_weight, norm_eps, algo,
-                        workspace, workspace_bytes, stream, 3);
+                        cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, norm_weight, norm_eps,
+                        gate_scale, gate_bias, algo, workspace, workspace_bytes, stream, 3);
 }
 
 gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
@@ -273,12 +282,13 @@ gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_tokens, in
                                      const float *init_state,
                                      const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                                      void *out, int out_dtype, float *final_state, int qk_norm, float q_scale,
-                                     const float *norm_weight, float norm_eps,
-                                     void *workspace, size_t workspace_bytes, void *stream) {
+                                     const float *norm_weight, float norm_eps, const float *gate_scale,
+                                     const float *gate_bias, void *workspace, size_t workspace_bytes, void *stream) {
     if (phase != GDN_PHASE_PREP && phase != GDN_PHASE_PASS) return GDN_ERR_INVALID_ARG;
     return prefill_impl(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
                         cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, norm_weight, norm_eps,
-                        GDN_ALGO_CHUNKED, workspace, workspace_bytes, stream, phase == GDN_PHASE_PREP ? 1 : 2);
+                        gate_scale, gate_bias, GDN_ALGO_CHUNKED, workspace, workspace_bytes, stream,
+                        phase == GDN_PHASE_PREP ? 1 : 2);
 }
 
 }  // extern "C"
@@ -352,9 +362,11 @@ gdn_status gdn_prefill_host(int n_seqs, int total_tokens, int hk, int hv, int dk
                             const float *log_alpha_host, const float *beta_host, const float *init_state_host,
                             const int32_t *cu_seqlens_host, void *out_host, int out_dtype, float *final_state_host,
                             int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
+                            const float *gate_scale, const float *gate_bias,
                             int algo, void *staging, size_t staging_bytes, void *stream) {
     gdn_status st = check_host_problem(n_seqs, total_tokens, hk, hv, dk, dv, cu_seqlens_host, out_dtype, algo);
     if (st != GDN_OK) return st;
+    if ((st = check_gate_params(gate_scale, gate_bias)) != GDN_OK) return st;
     if ((qk_norm != 0 && qk_norm != 1) || !isfinite(q_scale)) return GDN_ERR_INVALID_ARG;
     if (norm_weight && (!isfinite(norm_eps) || norm_eps < 0.f)) return GDN_ERR_INVALID_ARG;
     if (norm_weight && !aligned16(norm_weight)) return GDN_ERR_ALIGNMENT;
@@ -380,7 +392,8 @@ gdn_status gdn_prefill_host(int n_seqs, int total_tokens, int hk, int hv, int dk
                       init_state_host ? reinterpret_cast<const float *>(base + s.init) : nullptr,
                       reinterpret_cast<const int32_t *>(base + s.cu), cu_seqlens_host, base + s.out, out_dtype,
                       final_state_host ? reinterpret_cast<float *>(base + s.fin) : nullptr, qk_norm, q_scale,
-                      norm_weight, norm_eps, algo, s.ws_n ? base + s.ws : nullptr, s.ws_n, stream, 3);
+                      norm_weight, norm_eps, gate_scale, gate_bias, algo, s.ws_n ? base + s.ws : nullptr, s.ws_n,
+                      stream, 3);
     if (st != GDN_OK) return st;
     if (s.out_n && cudaMemcpyAsync(out_host, base + s.out, s.out_n, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
         return GDN_ERR_CUDA;
@@ -394,9 +407,11 @@ gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
                            const void *q, const void *k, const void *v,
                            const float *log_alpha, const float *beta,
                            void *out, int out_dtype, int qk_norm, float q_scale,
-                           const float *norm_weight, float norm_eps, void *stream) {
+                           const float *norm_weight, float norm_eps, const float *gate_scale,
+                           const float *gate_bias, void *stream) {
     gdn_status st = check_heads(hk, hv, dk, dv);
     if (st != GDN_OK) return st;
+    if ((st = check_gate_params(gate_scale, gate_bias)) != GDN_OK) return st;
     if (n < 0) return GDN_ERR_INVALID_ARG;
     if ((qk_norm != 0 && qk_norm != 1) || !isfinite(q_scale)) return GDN_ERR_INVALID_ARG;
     if (norm_weight && (!isfinite(norm_eps) || norm_eps < 0.f)) return GDN_ERR_INVALID_ARG;
@@ -411,7 +426,8 @@ gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
     const size_t out_bytes = (size_t)n * hv * dv * (out_dtype == GDN_DTYPE_F32 ? 4 : 2);
     const struct { const void *p; size_t n; } inputs[] = {
         {q, (size_t)n * hk * dk * 2}, {k, (size_t)n * hk * dk * 2}, {v, (size_t)n * hv * dv * 2},
-        {log_alpha, (size_t)n * hv * 4}, {beta, (size_t)n * hv * 4}, {out, out_bytes}};
+        {log_alpha, (size_t)n * hv * 4}, {beta, (size_t)n * hv * 4}, {out, out_bytes},
+        {gate_scale, (size_t)hv * 4}, {gate_bias, (size_t)hv * 4}};
     for (const auto &in : inputs)
         if (overlaps(state, state_bytes, in.p, in.n)) return GDN_ERR_INVALID_ARG;
     if (overlaps(out, out_bytes, q, (size_t)n * hk * dk * 2) || overlaps(out, out_bytes, k, (size_t)n * hk * dk * 2) ||
@@ -429,6 +445,7 @@ gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
     p.log_alpha = log_alpha; p.beta = beta; p.out = out; p.out_f32 = out_dtype == GDN_DTYPE_F32;
     p.qk_norm = qk_norm; p.q_scale = q_scale;
     p.norm_w = norm_weight; p.norm_eps = norm_eps;
+    p.gate_c = gate_scale; p.gate_b = gate_bias;
     p.err = nullptr;
     p.stream = static_cast<cudaStream_t>(stream);
     return gdn::launch_decode(p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

@@ -26,6 +26,22 @@ __device__ __forceinline__ float qk_inv_norm(float sum_sq, int qk_norm) {
     return qk_norm ? rsqrtf(sum_sq + kQkNormEps) : 1.f;
 }
 
+// Gates computed from raw per-token inputs (gdn.h: gate_scale, gate_bias).  With gate parameters c, b ([hv]
+// device arrays) the log_alpha and beta arrays hold the raw projections a and y of each token and value head h:
+//     log_alpha = -c_h softplus(a + b_h),   beta = sigmoid(y),
+// with softplus(x) = max(x, 0) + log(1 + e^{-|x|}) (no overflow, small-x tail kept).  Without them (c null)
+// the arrays hold the gates themselves.  Every kernel that reads a gate goes through these two functions, so
+// the preparation and state-passing kernels of the chunked path see identical values.
+__device__ __forceinline__ float gate_log_alpha(float a, const float *__restrict__ c, const float *__restrict__ b,
+                                                int h) {
+    if (c == nullptr) return a;
+    const float x = a + __ldg(b + h);
+    return -__ldg(c + h) * (fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))));
+}
+__device__ __forceinline__ float gate_beta(float y, const float *__restrict__ c) {
+    return c == nullptr ? y : 1.f / (1.f + expf(-y));
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xffff0000u); }
 
@@ -54,6 +70,7 @@ struct PrefillProblem {
     float q_scale;      // then multiply q by this
     const float *norm_w;   // fused output normalisation weight [d], or null
     float norm_eps;
+    const float *gate_c, *gate_b;   // gate parameters [hv] (log_alpha/beta hold raw inputs), or both null
     void *workspace;
     size_t workspace_bytes;
     unsigned int *err;
@@ -71,6 +88,7 @@ struct DecodeProblem {
     float q_scale;
     const float *norm_w;   // fused output normalisation weight [d], or null
     float norm_eps;
+    const float *gate_c, *gate_b;   // gate parameters [hv] (log_alpha/beta hold raw inputs), or both null
     unsigned int *err;
     cudaStream_t stream;
 };

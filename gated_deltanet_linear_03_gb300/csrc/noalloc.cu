@@ -63,7 +63,7 @@ extern "C" gdn_status gdn_prefill_noalloc(int n_seqs, int total_tokens, int hk, 
                                           const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                                           void *out, int out_dtype, float *final_state, int qk_norm,
                                           float q_scale, const float *norm_weight, float norm_eps,
-                                          void *stream) {
+                                          const float *gate_scale, const float *gate_bias, void *stream) {
     gdn_status st = GDN_OK;
     const size_t need = gdn_prefill_workspace_size(n_seqs, total_tokens, hk, hv, dk, dv, cu_seqlens_host,
                                                    GDN_ALGO_CHUNKED, &st);
@@ -73,5 +73,5 @@ extern "C" gdn_status gdn_prefill_noalloc(int n_seqs, int total_tokens, int hk, 
     if (scratch == nullptr) return GDN_ERR_CUDA;
     return gdn_prefill(n_seqs, total_tokens, hk, hv, dk, dv, q, k, v, log_alpha, beta, init_state, cu_seqlens,
                        cu_seqlens_host, out, out_dtype, final_state, qk_norm, q_scale, norm_weight, norm_eps,
-                       GDN_ALGO_CHUNKED, scratch, kNoAllocScratchBytes, stream);
+                       gate_scale, gate_bias, GDN_ALGO_CHUNKED, scratch, kNoAllocScratchBytes, stream);
 }

@@ -95,7 +95,8 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
                     const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
                     void *__restrict__ out, int out_f32, float *__restrict__ final_state, int qk_norm,
-                    float q_scale, const float *__restrict__ norm_w, float norm_eps) {
+                    float q_scale, const float *__restrict__ norm_w, float norm_eps,
+                    const float *__restrict__ gate_c, const float *__restrict__ gate_b) {
     constexpr int COLS = D / kTPR;        // state columns per thread
     constexpr int SLICES = D / kRows;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -166,6 +167,10 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
                 qq += __shfl_xor_sync(0xffffffffu, qq, off);
             }
             if (l == 0 && t < nt) {
+                if (gate_c) {   // gates from raw inputs: mapped once per token, in place
+                    sm.la[buf][t] = gate_log_alpha(sm.la[buf][t], gate_c, gate_b, h);
+                    sm.b[buf][t] = gate_beta(sm.b[buf][t], gate_c);
+                }
                 if (PREP) {
                     const float fk = qk_inv_norm(kk, qk_norm), fq = q_scale * qk_inv_norm(qq, qk_norm);
                     sm.fk[t] = fk;
@@ -289,7 +294,7 @@ cudaError_t launch_scan_dp(const PrefillProblem &p) {
     cfg.numAttrs = NORM ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, scan_prefill_kernel<D, PREP, NORM>, p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha,
                            p.beta, p.init_state, p.cu_seqlens, p.out, p.out_f32, p.final_state, p.qk_norm, p.q_scale,
-                           p.norm_w, p.norm_eps);
+                           p.norm_w, p.norm_eps, p.gate_c, p.gate_b);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -49,21 +49,23 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     F = ctypes.c_float
-    lib.gdn_prefill.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, F, I, P, Z, P]
+    lib.gdn_prefill.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, F, P, P, I, P, Z, P]
     lib.gdn_prefill.restype = I
-    lib.gdn_prefill_chunked_phase.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, F, P, Z, P]
+    lib.gdn_prefill_chunked_phase.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, F, P, P,
+                                              P, Z, P]
     lib.gdn_prefill_chunked_phase.restype = I
-    lib.gdn_prefill_noalloc.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, F, P]
+    lib.gdn_prefill_noalloc.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I, F, P, F, P, P, P]
     lib.gdn_prefill_noalloc.restype = I
     lib.gdn_prefill_workspace_size.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
     lib.gdn_prefill_workspace_size.restype = Z
-    lib.gdn_prefill_host.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, I, P, I, F, P, F, I, P, Z, P]
+    lib.gdn_prefill_host.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, I, P, I, F, P, F, P, P, I, P, Z, P]
     lib.gdn_prefill_host.restype = I
     lib.gdn_prefill_host_staging_size.argtypes = [I, I, I, I, I, I, P, I, I, I, I, ctypes.POINTER(I)]
     lib.gdn_prefill_host_staging_size.restype = Z
     lib.gdn_prefill_algo.argtypes = [I, I, I, I, I, I, P]
     lib.gdn_prefill_algo.restype = I
-    lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, I, ctypes.c_float, P, ctypes.c_float, P]
+    lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, I, ctypes.c_float, P, ctypes.c_float, P,
+                                    P, P]
     lib.gdn_decode_step.restype = I
     lib.gdn_device_error.argtypes = [P]
     lib.gdn_device_error.restype = I
@@ -92,6 +94,17 @@ def _stream_ptr(stream, device=None) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _gate_tensors(gate_scale, gate_bias, hv: int):
+    """The optional gate parameters: both or neither, fp32 [hv]."""
+    if (gate_scale is None) != (gate_bias is None):
+        raise ValueError("gate_scale and gate_bias go together")
+    if gate_scale is not None:
+        _need(gate_scale, "gate_scale", torch.float32, 1)
+        _need(gate_bias, "gate_bias", torch.float32, 1)
+        if gate_scale.numel() != hv or gate_bias.numel() != hv:
+            raise ValueError(f"gate_scale and gate_bias must have hv = {hv} entries")
 
 
 def _same_device(device: torch.device, **tensors):
@@ -146,8 +159,12 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
             out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
             final_state=True, algo: str = "chunked", workspace: Optional[torch.Tensor] = None,
             cu_seqlens_host: Optional[Sequence[int]] = None, stream=None, qk_norm: bool = False,
-            q_scale: float = 1.0, norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6):
+            q_scale: float = 1.0, norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6,
+            gate_scale: Optional[torch.Tensor] = None, gate_bias: Optional[torch.Tensor] = None):
     """Run ``gdn_prefill``.  Returns ``(out, final_state)``.
+
+    ``gate_scale`` / ``gate_bias`` (fp32 [hv] each): ``log_alpha`` and ``beta`` hold raw per-token inputs a, y and
+    the kernels compute log_alpha = -gate_scale softplus(a + gate_bias), beta = sigmoid(y).
 
     ``qk_norm`` / ``q_scale``: the in-kernel query/key preparation (every q and k head vector
     L2-normalised, then q multiplied by ``q_scale``); the defaults use q and k as given.
@@ -183,13 +200,16 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
     if need and workspace is None:
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _gate_tensors(gate_scale, gate_bias, hv)
     _same_device(q.device, k=k, v=v, log_alpha=log_alpha, beta=beta, cu_seqlens=cu_seqlens, init_state=init_state,
-                 out=out, final_state=final_state, norm_weight=norm_weight, workspace=workspace)
+                 out=out, final_state=final_state, norm_weight=norm_weight, workspace=workspace,
+                 gate_scale=gate_scale, gate_bias=gate_bias)
     with torch.cuda.device(q.device):
         st = lib.gdn_prefill(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                              _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out), DTYPE[out.dtype],
                              _ptr(final_state), int(bool(qk_norm)), float(q_scale), _ptr(norm_weight),
-                             float(norm_eps), ALGO[algo], _ptr(workspace), ws_bytes, _stream_ptr(stream, q.device))
+                             float(norm_eps), _ptr(gate_scale), _ptr(gate_bias), ALGO[algo], _ptr(workspace),
+                             ws_bytes, _stream_ptr(stream, q.device))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill")
     return out, final_state
@@ -199,7 +219,8 @@ def prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha
                     beta: torch.Tensor, cu_seqlens: torch.Tensor, *, init_state: Optional[torch.Tensor] = None,
                     out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16, final_state=True,
                     cu_seqlens_host: Optional[Sequence[int]] = None, stream=None, qk_norm: bool = False,
-                    q_scale: float = 1.0, norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6):
+                    q_scale: float = 1.0, norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6,
+                    gate_scale: Optional[torch.Tensor] = None, gate_bias: Optional[torch.Tensor] = None):
     """Run ``gdn_prefill_noalloc``: the chunked prefill using the library's fixed
     scratch instead of a workspace (for callers that cannot allocate device
     memory; see include/gdn.h for its size limit and sharing rules).
@@ -224,13 +245,15 @@ def prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha
     elif final_state is False:
         final_state = None
     cu_arr, _ = _host_cu(cu_seqlens, cu_seqlens_host)
+    _gate_tensors(gate_scale, gate_bias, hv)
     _same_device(q.device, k=k, v=v, log_alpha=log_alpha, beta=beta, cu_seqlens=cu_seqlens, init_state=init_state,
-                 out=out, final_state=final_state, norm_weight=norm_weight)
+                 out=out, final_state=final_state, norm_weight=norm_weight, gate_scale=gate_scale, gate_bias=gate_bias)
     with torch.cuda.device(q.device):   # the scratch used is the one of the current device
         st = lib.gdn_prefill_noalloc(n_seqs, T, hk, hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
                                      _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), cu_arr, _ptr(out),
                                      DTYPE[out.dtype], _ptr(final_state), int(bool(qk_norm)), float(q_scale),
-                                     _ptr(norm_weight), float(norm_eps), _stream_ptr(stream, q.device))
+                                     _ptr(norm_weight), float(norm_eps), _ptr(gate_scale), _ptr(gate_bias),
+                                     _stream_ptr(stream, q.device))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill_noalloc")
     return out, final_state
@@ -272,7 +295,7 @@ class HostPrefillPlan:
 
     def __init__(self, q, k, v, log_alpha, beta, cu_seqlens_host, *, init_state=None, out=None,
                  out_dtype=torch.bfloat16, final_state=True, algo="chunked", staging=None, device=None,
-                 qk_norm=False, q_scale=1.0, norm_weight=None, norm_eps=1e-6):
+                 qk_norm=False, q_scale=1.0, norm_weight=None, norm_eps=1e-6, gate_scale=None, gate_bias=None):
         self.lib = load_library()
         _need_host(q, "q", torch.bfloat16, 3)
         _need_host(k, "k", torch.bfloat16, 3)
@@ -302,15 +325,16 @@ class HostPrefillPlan:
                                  final_state is not None, algo)
         if staging is None:
             staging = torch.empty(need, dtype=torch.uint8, device=device or torch.device("cuda"))
-        if norm_weight is not None:
-            _same_device(staging.device, norm_weight=norm_weight)
+        _gate_tensors(gate_scale, gate_bias, hv)
+        _same_device(staging.device, norm_weight=norm_weight, gate_scale=gate_scale, gate_bias=gate_bias)
         self.device = staging.device
         self.out, self.final_state, self.staging = out, final_state, staging
-        self.tensors = (q, k, v, log_alpha, beta, init_state, norm_weight)
+        self.tensors = (q, k, v, log_alpha, beta, init_state, norm_weight, gate_scale, gate_bias)
         self.head = (n_seqs, T, hk, hv, dk, dv)
         self.ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state), self.cu_arr,
                      _ptr(out), DTYPE[out.dtype], _ptr(final_state))
-        self.qk = (int(bool(qk_norm)), float(q_scale), _ptr(norm_weight), float(norm_eps))
+        self.qk = (int(bool(qk_norm)), float(q_scale), _ptr(norm_weight), float(norm_eps), _ptr(gate_scale),
+                   _ptr(gate_bias))
         self.tail = (ALGO[algo], _ptr(staging), staging.numel() * staging.element_size())
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, log_alpha, beta, init_state)
                              if t is not None) + 4 * len(cu_vals)
@@ -342,7 +366,8 @@ class PrefillPlan:
 
     def __init__(self, q, k, v, log_alpha, beta, cu_seqlens, *, init_state=None, out=None,
                  out_dtype=torch.bfloat16, final_state=True, algo="chunked", workspace=None,
-                 cu_seqlens_host=None, qk_norm=False, q_scale=1.0, norm_weight=None, norm_eps=1e-6):
+                 cu_seqlens_host=None, qk_norm=False, q_scale=1.0, norm_weight=None, norm_eps=1e-6,
+                 gate_scale=None, gate_bias=None):
         self.lib = load_library()
         _need(q, "q", torch.bfloat16, 3)
         _need(k, "k", torch.bfloat16, 3)
@@ -364,18 +389,20 @@ class PrefillPlan:
         if need and workspace is None:
             workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
         self.out, self.final_state, self.workspace = out, final_state, workspace
-        self.tensors = (q, k, v, log_alpha, beta, cu_seqlens, init_state)
+        self.tensors = (q, k, v, log_alpha, beta, cu_seqlens, init_state, gate_scale, gate_bias)
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         self.algo = ALGO[algo]
         self.head = (n_seqs, T, hk, hv, dk, dv)
         self.ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
                      self.cu_arr, _ptr(out), DTYPE[out.dtype], _ptr(final_state))
         self.ws = (_ptr(workspace), ws_bytes)
-        self.qk = (int(bool(qk_norm)), float(q_scale), _ptr(norm_weight), float(norm_eps))
+        self.qk = (int(bool(qk_norm)), float(q_scale), _ptr(norm_weight), float(norm_eps), _ptr(gate_scale),
+                   _ptr(gate_bias))
         self.norm_weight = norm_weight
+        _gate_tensors(gate_scale, gate_bias, hv)
         _same_device(q.device, k=k, v=v, log_alpha=log_alpha, beta=beta, cu_seqlens=cu_seqlens,
                      init_state=init_state, out=out, final_state=final_state, norm_weight=norm_weight,
-                     workspace=workspace)
+                     workspace=workspace, gate_scale=gate_scale, gate_bias=gate_bias)
         self.device = q.device
 
     def run(self, stream=None):
@@ -397,7 +424,8 @@ class PrefillPlan:
 def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                 log_alpha: torch.Tensor, beta: torch.Tensor, *, out: Optional[torch.Tensor] = None,
                 out_dtype=torch.bfloat16, stream=None, qk_norm: bool = False, q_scale: float = 1.0,
-                norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6) -> torch.Tensor:
+                norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6,
+                gate_scale: Optional[torch.Tensor] = None, gate_bias: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Run ``gdn_decode_step`` (state updated in place).  Returns ``out``.
 
     ``norm_weight`` (fp32 [dv]): fuse the output normalisation o / sqrt(mean(o^2) + norm_eps) * weight."""
@@ -412,11 +440,14 @@ def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.
     hv, dv = v.shape[1], v.shape[2]
     if out is None:
         out = torch.empty(n, hv, dv, device=q.device, dtype=out_dtype)
-    _same_device(state.device, q=q, k=k, v=v, log_alpha=log_alpha, beta=beta, out=out, norm_weight=norm_weight)
+    _gate_tensors(gate_scale, gate_bias, hv)
+    _same_device(state.device, q=q, k=k, v=v, log_alpha=log_alpha, beta=beta, out=out, norm_weight=norm_weight,
+                 gate_scale=gate_scale, gate_bias=gate_bias)
     with torch.cuda.device(state.device):
         st = lib.gdn_decode_step(n, hk, hv, dk, dv, _ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
                                  _ptr(beta), _ptr(out), DTYPE[out.dtype], int(bool(qk_norm)), float(q_scale),
-                                 _ptr(norm_weight), float(norm_eps), _stream_ptr(stream, state.device))
+                                 _ptr(norm_weight), float(norm_eps), _ptr(gate_scale), _ptr(gate_bias),
+                                 _stream_ptr(stream, state.device))
     if st != GDN_OK:
         raise GdnError(st, "gdn_decode_step")
     return out

@@ -127,6 +127,18 @@ typedef enum {
  *                    vector o of every token becomes
  *                    o / sqrt(mean(o^2) + norm_eps) * norm_weight; NULL
  *                    leaves the outputs as computed.
+ *   gate_scale,      gates computed inside the kernels.  Both NULL: log_alpha
+ *   gate_bias        and beta are the gates.  Both given (fp32 [hv] device
+ *                    arrays; gate_scale[h] finite and >= 0): log_alpha and
+ *                    beta hold each token's raw projections a and y, and the
+ *                    kernels use, per token and value head h,
+ *                        log_alpha = -gate_scale[h] * softplus(a + gate_bias[h])
+ *                        beta      = 1 / (1 + exp(-y))
+ *                    in fp32 (the section "Keep recurrent state on chip" keeps
+ *                    the state and its gate in fp32; the form is the
+ *                    configured workloads' gate recipe with per-head
+ *                    parameters, our reading).  One without the other:
+ *                    GDN_ERR_INVALID_ARG.
  *   algo             GDN_ALGO_CHUNKED, GDN_ALGO_SCAN or GDN_ALGO_AUTO
  *   workspace        device scratch of at least gdn_prefill_workspace_size()
  *                    bytes (may be NULL when that size is 0), 256-byte aligned.
@@ -140,6 +152,7 @@ GDN_API gdn_status gdn_prefill(int n_seqs, int total_tokens, int hk, int hv, int
                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                        void *out, int out_dtype, float *final_state,
                        int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
+                       const float *gate_scale, const float *gate_bias,
                        int algo, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -166,6 +179,7 @@ GDN_API gdn_status gdn_prefill_chunked_phase(int phase, int n_seqs, int total_to
                                              const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                                              void *out, int out_dtype, float *final_state,
                                              int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
+                                             const float *gate_scale, const float *gate_bias,
                                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -214,12 +228,15 @@ GDN_API int gdn_prefill_algo(int n_seqs, int total_tokens, int hk, int hv, int d
  *                    decode path fuses the recurrent update with its
  *                    normalisation; the form of the norm is our reading).
  *   norm_eps         finite, >= 0; used only with norm_weight
+ *   gate_scale,      as for gdn_prefill: the gates computed from raw inputs
+ *   gate_bias        in log_alpha and beta ([n, hv]), or both NULL
  */
 GDN_API gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
                            const void *q, const void *k, const void *v,
                            const float *log_alpha, const float *beta,
                            void *out, int out_dtype, int qk_norm, float q_scale,
-                           const float *norm_weight, float norm_eps, void *stream);
+                           const float *norm_weight, float norm_eps,
+                           const float *gate_scale, const float *gate_bias, void *stream);
 
 /*
  * Synchronise `stream` and return (and clear) the device-side error word the
@@ -278,7 +295,7 @@ GDN_API gdn_status gdn_prefill_noalloc(int n_seqs, int total_tokens, int hk, int
                                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                                        void *out, int out_dtype, float *final_state,
                                        int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
-                                       void *stream);
+                                       const float *gate_scale, const float *gate_bias, void *stream);
 
 /*
  * gdn_prefill_host: gdn_prefill on inputs and outputs in HOST memory, for
@@ -292,8 +309,8 @@ GDN_API gdn_status gdn_prefill_noalloc(int n_seqs, int total_tokens, int hk, int
  *      final_state_host.
  * Shapes, dtypes, options and errors are those of gdn_prefill; the host arrays
  * are dense with gdn_prefill's layouts and need no particular alignment.
- * norm_weight, when given, is a DEVICE array (a model parameter that stays
- * resident).  init_state_host NULL means zero initial states; final_state_host
+ * norm_weight, gate_scale and gate_bias, when given, are DEVICE arrays (model
+ * parameters that stay resident).  init_state_host NULL means zero initial states; final_state_host
  * NULL skips the final states.
  *
  *   staging        device memory of at least gdn_prefill_host_staging_size()
@@ -319,6 +336,7 @@ GDN_API gdn_status gdn_prefill_host(int n_seqs, int total_tokens, int hk, int hv
                                     const float *init_state_host, const int32_t *cu_seqlens_host,
                                     void *out_host, int out_dtype, float *final_state_host,
                                     int qk_norm, float q_scale, const float *norm_weight, float norm_eps,
+                                    const float *gate_scale, const float *gate_bias,
                                     int algo, void *staging, size_t staging_bytes, void *stream);
 
 /* Static, human-readable name of a status code. */

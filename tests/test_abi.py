@@ -49,13 +49,13 @@ FAKE = 0x10000  # an aligned address that is never dereferenced: validation fail
 def prefill(lib, **kw):
     a = dict(n_seqs=1, T=64, hk=1, hv=2, dk=128, dv=128, q=FAKE, k=FAKE * 2, v=FAKE * 3, la=FAKE * 4,
              b=FAKE * 5, s0=None, cu=FAKE * 6, cu_host=_cu([0, 64]), out=FAKE * 7, odt=0, fin=None,
-             algo=1, ws=None, wsb=0, qkn=0, qs=1.0, nw=None, ne=1e-6)
+             algo=1, ws=None, wsb=0, qkn=0, qs=1.0, nw=None, ne=1e-6, gc=None, gb=None)
     a.update(kw)
     P = ctypes.c_void_p
     return lib.gdn_prefill(a["n_seqs"], a["T"], a["hk"], a["hv"], a["dk"], a["dv"], P(a["q"]), P(a["k"]),
                            P(a["v"]), P(a["la"]), P(a["b"]), P(a["s0"]), P(a["cu"]), a["cu_host"], P(a["out"]),
-                           a["odt"], P(a["fin"]), a["qkn"], a["qs"], P(a["nw"]), a["ne"], a["algo"], P(a["ws"]),
-                           a["wsb"], None)
+                           a["odt"], P(a["fin"]), a["qkn"], a["qs"], P(a["nw"]), a["ne"], P(a["gc"]), P(a["gb"]),
+                           a["algo"], P(a["ws"]), a["wsb"], None)
 
 
 def test_prefill_rejects_bad_heads(lib):
@@ -87,6 +87,10 @@ def test_prefill_rejects_bad_dtype_algo_pointers(lib):
     assert prefill(lib, q=FAKE + 4) == 3          # misaligned
     assert prefill(lib, out=FAKE * 2) == 1        # out overlaps k
     assert prefill(lib, fin=FAKE * 3, s0=FAKE * 40) == 1   # final_state overlaps v
+    assert prefill(lib, gc=FAKE * 60) == 1                 # gate_scale without gate_bias
+    assert prefill(lib, gb=FAKE * 60) == 1
+    assert prefill(lib, gc=FAKE * 60 + 4, gb=FAKE * 61) == 3   # misaligned gate parameters
+    assert prefill(lib, gc=FAKE * 7, gb=FAKE * 61) == 1    # out overlaps gate_scale
 
 
 def test_chunked_requires_workspace(lib):
@@ -115,9 +119,9 @@ def test_decode_rejects_bad_args(lib):
     P = ctypes.c_void_p
 
     def dec(n=1, hk=1, hv=2, d=128, state=FAKE, q=FAKE * 2, k=FAKE * 3, v=FAKE * 4, la=FAKE * 5, b=FAKE * 6,
-            out=FAKE * 7, odt=0, qkn=0, qs=1.0, nw=None, ne=1e-6):
+            out=FAKE * 7, odt=0, qkn=0, qs=1.0, nw=None, ne=1e-6, gc=None, gb=None):
         return lib.gdn_decode_step(n, hk, hv, d, d, P(state), P(q), P(k), P(v), P(la), P(b), P(out), odt, qkn, qs,
-                                   P(nw), ne, None)
+                                   P(nw), ne, P(gc), P(gb), None)
 
     assert dec(hk=3, hv=4) == 1
     assert dec(d=96) == 2
@@ -131,6 +135,9 @@ def test_decode_rejects_bad_args(lib):
     assert dec(qs=float("inf")) == 1
     assert dec(nw=FAKE * 9, ne=-1.0) == 1    # negative eps
     assert dec(nw=FAKE * 9 + 4) == 3         # misaligned weight
+    assert dec(gc=FAKE * 20) == 1            # gate_scale without gate_bias
+    assert dec(gc=FAKE * 20, gb=FAKE * 21 + 8) == 3
+    assert dec(gc=FAKE, gb=FAKE * 21) == 1   # gate_scale overlaps state
 
 
 def test_auto_algo_rule(lib):
@@ -208,14 +215,14 @@ def test_host_staging_size_rejects_invalid_problems(lib):
 
 def prefill_host(lib, **kw):
     a = dict(n_seqs=1, T=64, hk=1, hv=2, dk=128, dv=128, q=FAKE, k=FAKE, v=FAKE, la=FAKE, b=FAKE, s0=None,
-             cu_host=_cu([0, 64]), out=FAKE, odt=0, fin=FAKE, qkn=0, qs=1.0, nw=None, ne=1e-6, algo=0,
-             stg=FAKE * 16, stgb=1 << 40)
+             cu_host=_cu([0, 64]), out=FAKE, odt=0, fin=FAKE, qkn=0, qs=1.0, nw=None, ne=1e-6, gc=None,
+             gb=None, algo=0, stg=FAKE * 16, stgb=1 << 40)
     a.update(kw)
     P = ctypes.c_void_p
     return lib.gdn_prefill_host(a["n_seqs"], a["T"], a["hk"], a["hv"], a["dk"], a["dv"], P(a["q"]), P(a["k"]),
                                 P(a["v"]), P(a["la"]), P(a["b"]), P(a["s0"]), a["cu_host"], P(a["out"]), a["odt"],
-                                P(a["fin"]), a["qkn"], a["qs"], P(a["nw"]), a["ne"], a["algo"], P(a["stg"]),
-                                a["stgb"], None)
+                                P(a["fin"]), a["qkn"], a["qs"], P(a["nw"]), a["ne"], P(a["gc"]), P(a["gb"]),
+                                a["algo"], P(a["stg"]), a["stgb"], None)
 
 
 def test_prefill_host_validates_before_enqueueing(lib):
@@ -233,6 +240,7 @@ def test_prefill_host_validates_before_enqueueing(lib):
     assert prefill_host(lib, odt=3) == 2
     assert prefill_host(lib, hk=3, hv=4) == 1
     assert prefill_host(lib, cu_host=_cu([0, 65])) == 1
+    assert prefill_host(lib, gb=FAKE) == 1                   # gate_bias without gate_scale
     assert prefill_host(lib, T=0, cu_host=_cu([0, 0]), fin=None) == 0   # nothing to do: returns at once
 
 
@@ -253,7 +261,7 @@ def test_pointers_off_the_current_device_are_refused(lib):
     def dec():
         P = ctypes.c_void_p
         return lib.gdn_decode_step(1, 1, 2, 128, 128, P(FAKE), P(FAKE * 2), P(FAKE * 3), P(FAKE * 4), P(FAKE * 5),
-                                   P(FAKE * 6), P(FAKE * 7), 0, 0, 1.0, None, 1e-6, None)
+                                   P(FAKE * 6), P(FAKE * 7), 0, 0, 1.0, None, 1e-6, None, None, None)
     assert dec() in allowed
 
 
@@ -273,11 +281,11 @@ def test_host_memory_is_refused_on_a_gpu(lib):
         for q_ptr, out_ptr in ((host_q.data_ptr(), out_dev.data_ptr()), (d[0].data_ptr(), host_q.data_ptr())):
             st = lib.gdn_prefill(1, 64, 1, 2, 128, 128, P(q_ptr), P(d[1].data_ptr()), P(d[2].data_ptr()),
                                  P(d[3].data_ptr()), P(d[4].data_ptr()), None, P(d[5].data_ptr()), cu, P(out_ptr), 0,
-                                 None, 0, 1.0, None, 1e-6, 1, None, 0, None)
+                                 None, 0, 1.0, None, 1e-6, None, None, 1, None, 0, None)
             assert st == 1
         state = torch.zeros(1, 2, 128, 128, dtype=torch.float32)            # host state
         st = lib.gdn_decode_step(1, 1, 2, 128, 128, P(state.data_ptr()), P(d[0].data_ptr()), P(d[1].data_ptr()),
                                  P(d[2].data_ptr()), P(d[3].data_ptr()), P(d[4].data_ptr()), P(out_dev.data_ptr()),
-                                 0, 0, 1.0, None, 1e-6, None)
+                                 0, 0, 1.0, None, 1e-6, None, None, None)
         assert st == 1
     assert gdn.device_error() == 0

@@ -60,5 +60,5 @@ def test_noalloc_rejects_problems_beyond_the_scratch(gdn):
     assert st.value == 0 and need > gdn.NOALLOC_SCRATCH_BYTES
     fake = ctypes.c_void_p(0x10000)
     r = lib.gdn_prefill_noalloc(1, T, 16, 32, 128, 128, fake, fake, fake, fake, fake, None, fake, cu, fake, 0,
-                                None, 0, 1.0, None, 1e-6, None)
+                                None, 0, 1.0, None, 1e-6, None, None, None)
     assert r == 7   # GDN_ERR_WORKSPACE
