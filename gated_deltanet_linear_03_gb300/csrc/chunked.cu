@@ -346,10 +346,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         mbar_init(&bar_mma, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(&bar_tma, 32768);
+        // (bounds-checking build: the tile's columns inside the q/k rows, its first token inside the tokens)
+        if (GDN_INB(hq * D + 127, hk * D, err) && GDN_INB(t0, total, err)) {
 #pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            tma_load_2d(sm + PREP_KQ + kb * 16384, &kmap, &bar_tma, hq * D + kb * 64, t0);
-            tma_load_2d(sm + PREP_KQ + kb * 16384 + 8192, &qmap, &bar_tma, hq * D + kb * 64, t0);
+            for (int kb = 0; kb < 2; ++kb) {
+                tma_load_2d(sm + PREP_KQ + kb * 16384, &kmap, &bar_tma, hq * D + kb * 64, t0);
+                tma_load_2d(sm + PREP_KQ + kb * 16384 + 8192, &qmap, &bar_tma, hq * D + kb * 64, t0);
+            }
         }
     }
     float *g_s = reinterpret_cast<float *>(sm + PREP_G);  // [64]
@@ -361,11 +364,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     float la0 = 0.f, la1 = 0.f, bt0 = 0.f, bt1 = 0.f;
     if (warp == 1) {
         const int i0 = 2 * lane, i1 = 2 * lane + 1;
-        if (i0 < L) {
+        if (i0 < L && GDN_INB((size_t)(t0 + i0) * hv + h, (long)total * hv, err)) {
             la0 = log_alpha[(size_t)(t0 + i0) * hv + h];
             bt0 = beta[(size_t)(t0 + i0) * hv + h];
         }
-        if (i1 < L) {
+        if (i1 < L && GDN_INB((size_t)(t0 + i1) * hv + h, (long)total * hv, err)) {
             la1 = log_alpha[(size_t)(t0 + i1) * hv + h];
             bt1 = beta[(size_t)(t0 + i1) * hv + h];
         }
@@ -422,7 +425,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             f *= qk_inv_norm(ss, 1);
         }
         (isq ? qf_s : kf_s)[r] = f;
-        if (ok && qk_norm) norms[((size_t)gc * hv + h) * 128 + tid] = f;   // read by the pass only with qk_norm
+        if (ok && qk_norm && GDN_INB(((size_t)gc * hv + h) * 128 + tid, (long)gridDim.x * hv * 128, err))
+            norms[((size_t)gc * hv + h) * 128 + tid] = f;   // read by the pass only with qk_norm
     }
     if (warp == 1) {
         if (GATE) {   // the gates from raw inputs, formed while the loads' latency was covered by the MMA wait
@@ -636,8 +640,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     __syncthreads();
     if (ok && tid == 0) {
         const int prow = (gc * hv + h) * D;
-        tma_store_2d(&phmap, sm + PREP_KQ, 0, prow);
-        tma_store_2d(&plmap, sm + PREP_KQ + 16384, 0, prow);
+        if (GDN_INB((long)prow + D - 1, (long)gridDim.x * hv * D, err)) {
+            tma_store_2d(&phmap, sm + PREP_KQ, 0, prow);
+            tma_store_2d(&plmap, sm + PREP_KQ + 16384, 0, prow);
+        }
         tma_store_commit();
     }
     if (ok) {
@@ -660,8 +666,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     __syncthreads();
     if (ok && tid == 0) {
         const int rrow = (gc * hv + h) * C;
-        tma_store_2d(&rhmap, sm + PREP_A, 0, rrow);
-        tma_store_2d(&rlmap, sm + PREP_A + 8192, 0, rrow);
+        if (GDN_INB((long)rrow + C - 1, (long)gridDim.x * hv * C, err)) {
+            tma_store_2d(&rhmap, sm + PREP_A, 0, rrow);
+            tma_store_2d(&rlmap, sm + PREP_A + 8192, 0, rrow);
+        }
         tma_store_commit();
         tma_store_wait_read();
     } else if (tid == 0) {
@@ -697,7 +705,11 @@ constexpr uint32_t TM_D1 = 0, TM_PX = 64, TM_RX = 128;
 
 // Q and K rows of the chunk starting at token t0 (q/k head hq) into a stage (the caller arms the barrier).
 __device__ __forceinline__ void pass_load_qk(uint8_t *st, uint64_t *bar, const CUtensorMap *qmap,
-                                             const CUtensorMap *kmap, int hq, int t0) {
+                                             const CUtensorMap *kmap, int hq, int t0, int hk, int total,
+                                             unsigned int *err) {
+    // (bounds-checking build: the tile's columns inside the q/k rows, its first token inside the tokens)
+    if (!GDN_INB(hq * D + 127, hk * D, err) || !GDN_INB(t0, total, err)) return;
+    (void)hk; (void)total; (void)err;
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
         tma_load_2d(st + ST_QK + kb * 16384, qmap, bar, hq * D + kb * 64, t0);
@@ -709,10 +721,13 @@ __device__ __forceinline__ void pass_load_qk(uint8_t *st, uint64_t *bar, const C
 __device__ __forceinline__ void pass_issue_loads(uint8_t *st, uint64_t *bar, const CUtensorMap *qmap,
                                                  const CUtensorMap *kmap, const CUtensorMap *phmap,
                                                  const CUtensorMap *plmap, const CUtensorMap *rhmap,
-                                                 const CUtensorMap *rlmap, int hq, int t0, int gc, int hv, int h) {
+                                                 const CUtensorMap *rlmap, int hq, int t0, int gc, int hv, int h,
+                                                 int hk, int total, int nch, unsigned int *err) {
     mbar_arrive_expect_tx(bar, kStageTx);
-    pass_load_qk(st, bar, qmap, kmap, hq, t0);
+    pass_load_qk(st, bar, qmap, kmap, hq, t0, hk, total, err);
     const int prow = (gc * hv + h) * D;
+    if (!GDN_INB((long)prow + D - 1, (long)nch * hv * D, err)) return;
+    (void)nch;
     tma_load_2d(st + ST_PH, phmap, bar, 0, prow);
     tma_load_2d(st + ST_PL, plmap, bar, 0, prow);
     tma_load_2d(st + ST_RH, rhmap, bar, 0, (gc * hv + h) * C);
@@ -741,18 +756,23 @@ struct ChunkInputs {
 __device__ __forceinline__ void load_chunk_inputs(ChunkInputs &in, const float *__restrict__ log_alpha,
                                                   const float *__restrict__ beta, const __nv_bfloat16 *__restrict__ v,
                                                   const float *__restrict__ norms, float q_scale, int gcx, int t0,
-                                                  int L, int hv, int h, int rowg, int lane, bool krow, int i) {
+                                                  int L, int hv, int h, int rowg, int lane, bool krow, int i,
+                                                  int total, int nch, unsigned int *err) {
     const int i0 = 2 * lane, i1 = 2 * lane + 1;
+    const long g_n = (long)total * hv;
+    (void)g_n; (void)nch; (void)err;
     // norms is null without qk_norm: the factors are then 1 (k) and q_scale (q)
-    in.f = norms ? norms[((size_t)gcx * hv + h) * 128 + (krow ? i : 64 + i)] : (krow ? 1.f : q_scale);
-    in.la0 = i0 < L ? log_alpha[(size_t)(t0 + i0) * hv + h] : 0.f;
-    in.la1 = i1 < L ? log_alpha[(size_t)(t0 + i1) * hv + h] : 0.f;
+    const size_t fi = ((size_t)gcx * hv + h) * 128 + (krow ? i : 64 + i);
+    in.f = norms ? (GDN_INB(fi, (long)nch * hv * 128, err) ? norms[fi] : 0.f) : (krow ? 1.f : q_scale);
+    in.la0 = i0 < L && GDN_INB((size_t)(t0 + i0) * hv + h, g_n, err) ? log_alpha[(size_t)(t0 + i0) * hv + h] : 0.f;
+    in.la1 = i1 < L && GDN_INB((size_t)(t0 + i1) * hv + h, g_n, err) ? log_alpha[(size_t)(t0 + i1) * hv + h] : 0.f;
     in.b = 0.f;
 #pragma unroll
     for (int q4 = 0; q4 < DG / 8; ++q4) in.v[q4] = make_uint4(0, 0, 0, 0);
-    if (krow && i < L) {
+    const size_t vi = ((size_t)(t0 + i) * hv + h) * D + rowg;
+    if (krow && i < L && GDN_INB(vi + DG - 1, g_n * D, err)) {
         in.b = beta[(size_t)(t0 + i) * hv + h];
-        const uint4 *vp = reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + i) * hv + h) * D + rowg);
+        const uint4 *vp = reinterpret_cast<const uint4 *>(v + vi);
 #pragma unroll
         for (int q4 = 0; q4 < DG / 8; ++q4) in.v[q4] = vp[q4];
     }
@@ -802,7 +822,9 @@ __device__ __forceinline__ void outputs_begin(float (&qs)[DG], uint32_t tmem_rx,
 template <bool NORM>
 __device__ __forceinline__ void outputs_end(float (&qs)[DG], int grp, int i, int L, int t0, int hv, int h, int rowg,
                                             void *__restrict__ out, int out_f32, bool valid, float (*ps)[64],
-                                            const float *__restrict__ norm_w, float norm_eps) {
+                                            const float *__restrict__ norm_w, float norm_eps, long out_n,
+                                            unsigned int *err) {
+    (void)out_n;
     if (NORM) {
         cluster_wait();
         float tot = 0.f;
@@ -814,7 +836,7 @@ __device__ __forceinline__ void outputs_end(float (&qs)[DG], int grp, int i, int
 #pragma unroll
         for (int e = 0; e < DG; ++e) qs[e] *= sc * norm_w[rowg + e];
     }
-    if (valid && i < L) {
+    if (valid && i < L && GDN_INB(((size_t)(t0 + i) * hv + h) * D + rowg + DG - 1, out_n, err)) {
         const size_t o = ((size_t)(t0 + i) * hv + h) * D + rowg;
         if (out_f32) {
             float4 *op = reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + o);
@@ -905,17 +927,18 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         tma_prefetch_desc(&plmap);
         tma_prefetch_desc(&rhmap);
         tma_prefetch_desc(&rlmap);
-        pass_issue_loads(sm, &bar_tma[0], &qmap, &kmap, &phmap, &plmap, &rhmap, &rlmap, hq, ta, gc0, hv, h);
+        pass_issue_loads(sm, &bar_tma[0], &qmap, &kmap, &phmap, &plmap, &rhmap, &rlmap, hq, ta, gc0, hv, h, hk, total, nch, err);
     }
     ChunkInputs nxt;
     if (started)
-        load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0, ta, min(C, tb - ta), hv, h, rowg, lane, krow, i);
+        load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0, ta, min(C, tb - ta), hv, h, rowg, lane, krow, i, total, nch, err);
 
     // state columns: thread (d, grp) holds S[rowg + r][d] for r < DG
     float S[DG];
     const size_t sbase = (((size_t)n * hv + h) * D + rowg) * D + d;
+    const bool state_ok = GDN_INB(sbase + (size_t)(DG - 1) * D, (long)n_seqs * hv * D * D, err);
 #pragma unroll
-    for (int r = 0; r < DG; ++r) S[r] = init_state ? init_state[sbase + (size_t)r * D] : 0.f;
+    for (int r = 0; r < DG; ++r) S[r] = init_state && state_ok ? init_state[sbase + (size_t)r * D] : 0.f;
 
     // The state operand [S_hi ; S_lo] is stored MN-major: row d (the dk index, K of the MMA) holds the 64
     // values n = 0..31 (S_hi rows) and 32..63 (S_lo rows); this thread writes its DG rows as two 16-byte
@@ -989,13 +1012,13 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             // next chunk's tiles go to the other stage once its last reader (the R X of chunk c - 1) is done
             if (c == 0 || mbar_wait(&bar_rx[par ^ 1], rx_parity(c - 1)))
                 pass_issue_loads(sm + (s ^ 1) * PASS_STAGE, &bar_tma[s ^ 1], &qmap, &kmap, &phmap, &plmap, &rhmap,
-                                 &rlmap, hq, t0 + C, gc + 1, hv, h);
+                                 &rlmap, hq, t0 + C, gc + 1, hv, h, hk, total, nch, err);
             else
                 ok = false;
         }
         if (c + 1 < nchunks)
             load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc + 1, t0 + C, min(C, tb - t0 - C), hv, h,
-                              rowg, lane, krow, i);
+                              rowg, lane, krow, i, total, nch, err);
 
         const float2 g2 = cumsum_pairs(cur.la0, cur.la1, L, lane);
         const float gL = g_of(g2, L - 1);
@@ -1090,7 +1113,7 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         } else {
             if (c > 0)
                 outputs_end<true>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, true,
-                                  ps_norm[(c - 1) & 1], norm_w, norm_eps);
+                                  ps_norm[(c - 1) & 1], norm_w, norm_eps, (long)total * hv * D, err);
 #pragma unroll
             for (int r = 0; r < DG; ++r) qs[r] = qcur_n[r];
         }
@@ -1122,13 +1145,13 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
                 if (!done) raise_error(err, kErrTimeout);
                 outputs_begin<true>(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, done, ps_norm[lp]);
                 outputs_end<true>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, done, ps_norm[lp], norm_w,
-                                  norm_eps);
+                                  norm_eps, (long)total * hv * D, err);
             } else {
                 cluster_arrive();
                 cluster_wait();
             }
         }
-        if (final_state) {
+        if (final_state && state_ok) {
 #pragma unroll
             for (int r = 0; r < DG; ++r) final_state[sbase + (size_t)r * D] = S[r];
         }
@@ -1307,12 +1330,14 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             // Q|K, P and R of chunk cc into stage cc & 1
             auto load_qk = [&](int cc) {
                 mbar_arrive_expect_tx(&bar_qk[cc & 1], kQkTx);
-                pass_load_qk(sm + (cc & 1) * PASS_STAGE, &bar_qk[cc & 1], &qmap, &kmap, hq, ta + cc * C);
+                pass_load_qk(sm + (cc & 1) * PASS_STAGE, &bar_qk[cc & 1], &qmap, &kmap, hq, ta + cc * C, hk, total,
+                             err);
             };
             auto load_p = [&](int cc) {
                 uint8_t *st = sm + (cc & 1) * PASS_STAGE;
                 const int prow = ((gc0 + cc) * hv + h) * D;
                 mbar_arrive_expect_tx(&bar_p[cc & 1], kPTx);
+                if (!GDN_INB((long)prow + D - 1, (long)nch * hv * D, err)) return;
                 tma_load_2d(st + ST_PH, &phmap, &bar_p[cc & 1], 0, prow);
                 tma_load_2d(st + ST_PL, &plmap, &bar_p[cc & 1], 0, prow);
             };
@@ -1320,6 +1345,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 uint8_t *st = sm + (cc & 1) * PASS_STAGE;
                 const int rrow = ((gc0 + cc) * hv + h) * C;
                 mbar_arrive_expect_tx(&bar_r[cc & 1], kRTx);
+                if (!GDN_INB((long)rrow + C - 1, (long)nch * hv * C, err)) return;
                 tma_load_2d(st + ST_RH, &rhmap, &bar_r[cc & 1], 0, rrow);
                 tma_load_2d(st + ST_RL, &rlmap, &bar_r[cc & 1], 0, rrow);
             };
@@ -1371,11 +1397,12 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         ChunkInputs nxt;
         if (started)
             load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0, ta, min(C, tb - ta), hv, h, rowg, lane,
-                              krow, i);
+                              krow, i, total, nch, err);
         float S[DG];
         const size_t sbase = (((size_t)n * hv + h) * D + rowg) * D + d;
+        const bool state_ok = GDN_INB(sbase + (size_t)(DG - 1) * D, (long)n_seqs * hv * D * D, err);
 #pragma unroll
-        for (int r = 0; r < DG; ++r) S[r] = init_state ? init_state[sbase + (size_t)r * D] : 0.f;
+        for (int r = 0; r < DG; ++r) S[r] = init_state && state_ok ? init_state[sbase + (size_t)r * D] : 0.f;
         auto write_sop = [&]() {
 #pragma unroll
             for (int j = 0; j < DG / 8; ++j) {
@@ -1410,7 +1437,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             finish_gates<GATE>(cur, L, lane, krow, i, gate_c, gate_b, h);
             if (c + 1 < nchunks)
                 load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0 + c + 1, t0 + C, min(C, tb - t0 - C),
-                                  hv, h, rowg, lane, krow, i);
+                                  hv, h, rowg, lane, krow, i, total, nch, err);
             const float2 g2 = cumsum_pairs(cur.la0, cur.la1, L, lane);
             const float gL = g_of(g2, L - 1);
             const float eg = __expf(g_of(g2, i));
@@ -1455,7 +1482,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                     tc_fence_after();
                     outputs_begin<false>(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, ok, nullptr);
                     outputs_end<false>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, ok, nullptr, nullptr,
-                                       0.f);
+                                       0.f, (long)total * hv * D, err);
                 }
 #pragma unroll
                 for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
@@ -1484,9 +1511,9 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 tc_fence_after();
                 if (!done) fail();
                 outputs_begin<false>(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, done, nullptr);
-                outputs_end<false>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, done, nullptr, nullptr, 0.f);
+                outputs_end<false>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, done, nullptr, nullptr, 0.f, (long)total * hv * D, err);
             }
-            if (final_state) {
+            if (final_state && state_ok) {
 #pragma unroll
                 for (int r = 0; r < DG; ++r) final_state[sbase + (size_t)r * D] = S[r];
             }

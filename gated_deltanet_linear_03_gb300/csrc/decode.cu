@@ -67,7 +67,7 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
                    const __nv_bfloat16 *__restrict__ v, const float *__restrict__ log_alpha,
                    const float *__restrict__ beta, void *__restrict__ out, int out_f32, int qk_norm,
                    float q_scale, const float *__restrict__ norm_w, float norm_eps,
-                   const float *__restrict__ gate_c, const float *__restrict__ gate_b) {
+                   const float *__restrict__ gate_c, const float *__restrict__ gate_b, unsigned int *err) {
     constexpr int LPR = D / 4;                  // lanes per row
     constexpr int GROUPS = 32 / LPR;            // lane groups per warp
     constexpr int WARP_ROWS = GROUPS * kRowsPerGroup;
@@ -86,17 +86,25 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
     const int hq = h / (hv / hk);
     const int row_in_head = (int)(row0 % D);
 
+    // extents (elements) of the buffers, for the bounds-checking build
+    const long n_states = (long)total_rows / ((long)hv * D);
+    const long state_n = (long)total_rows * D, qk_n = n_states * hk * D, v_n = n_states * hv * D;
+    (void)state_n; (void)qk_n; (void)v_n;
+
     // q, k slice of this lane: 4 bf16 = 8 bytes
     const size_t qk_off = ((size_t)nb * hk + hq) * D + gl * 4;
-    const uint2 kraw = *reinterpret_cast<const uint2 *>(k + qk_off);
-    const uint2 qraw = *reinterpret_cast<const uint2 *>(q + qk_off);
+    const bool qk_ok = GDN_INB(qk_off + 3, qk_n, err);
+    const uint2 kraw = qk_ok ? *reinterpret_cast<const uint2 *>(k + qk_off) : make_uint2(0, 0);
+    const uint2 qraw = qk_ok ? *reinterpret_cast<const uint2 *>(q + qk_off) : make_uint2(0, 0);
     const float kv[4] = {bf16_lo(kraw.x), bf16_hi(kraw.x), bf16_lo(kraw.y), bf16_hi(kraw.y)};
     const float qv[4] = {bf16_lo(qraw.x), bf16_hi(qraw.x), bf16_lo(qraw.y), bf16_hi(qraw.y)};
 
     float4 s[kRowsPerGroup];
     float4 *srow = reinterpret_cast<float4 *>(state + (size_t)row0 * D) + gl;
+    const bool state_ok = GDN_INB((row0 + kRowsPerGroup - 1) * D + gl * 4 + 3, state_n, err);
 #pragma unroll
-    for (int i = 0; i < kRowsPerGroup; ++i) s[i] = __ldcs(srow + (size_t)i * (D / 4));
+    for (int i = 0; i < kRowsPerGroup; ++i)
+        s[i] = state_ok ? __ldcs(srow + (size_t)i * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
 
     // k.q over the head (same for every row of the group), and the preparation factors of k and q
     float kq = kv[0] * qv[0] + kv[1] * qv[1] + kv[2] * qv[2] + kv[3] * qv[3];
@@ -118,9 +126,10 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
     }
     if (PREP) kq *= fk * fq;
 
-    const float la = clamp_log_alpha(gate_log_alpha(log_alpha[head], gate_c, gate_b, h));
+    const bool gate_ok = GDN_INB(head, n_states * hv, err);
+    const float la = clamp_log_alpha(gate_ok ? gate_log_alpha(log_alpha[head], gate_c, gate_b, h) : 0.f);
     const float alpha = __expf(la);
-    const float b = gate_beta(beta[head], gate_c);
+    const float b = gate_ok ? gate_beta(beta[head], gate_c) : 0.f;
 
     float part[16];
 #pragma unroll
@@ -144,7 +153,8 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
         for (int j = 0; j < PER; ++j)
             if (my_base + j == i) mine = part[j];
         const float sk = (PREP ? fk : 1.f) * __shfl_sync(0xffffffffu, mine, src_k);
-        u[i] = b * (__bfloat162float(vrow[i]) - alpha * sk);
+        const float vi = GDN_INB(head * D + row_in_head + i, v_n, err) ? __bfloat162float(vrow[i]) : 0.f;
+        u[i] = b * (vi - alpha * sk);
     }
 
     // write the updated rows
@@ -156,7 +166,7 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
         o.y = alpha * s[i].y + uk * kv[1];
         o.z = alpha * s[i].z + uk * kv[2];
         o.w = alpha * s[i].w + uk * kv[3];
-        __stcs(srow + (size_t)i * (D / 4), o);
+        if (state_ok) __stcs(srow + (size_t)i * (D / 4), o);
     }
 
     // outputs: the holder lane of sq_i writes o_i (with 32 lanes per row two
@@ -202,6 +212,7 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
             const int i = idx - 8;
             const float o = NORM ? ov[j] * scale * norm_w[row_in_head + i] : ov[j];
             const size_t oi = (size_t)head * D + row_in_head + i;
+            if (!GDN_INB(oi, v_n, err)) continue;
             if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
             else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(o);
         }
@@ -242,7 +253,8 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
                      const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
                      void *__restrict__ out, int out_f32, float *__restrict__ final_state, int qk_norm,
                      float q_scale, const float *__restrict__ norm_w, float norm_eps,
-                     const float *__restrict__ gate_c, const float *__restrict__ gate_b) {
+                     const float *__restrict__ gate_c, const float *__restrict__ gate_b, int n_seqs,
+                     unsigned int *err) {
     constexpr int LPR = D / 4, GROUPS = 32 / LPR, ROWS = short_rows<D>(), SLICES = D / ROWS;
     constexpr int NT = short_warps<D>() * 32;
     constexpr int PER = (16 / LPR) > 0 ? (16 / LPR) : 1;
@@ -259,29 +271,40 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
     const long tend = min(max((long)cu_seqlens[n + 1], tbeg), (long)total_tokens);
     const int L = (int)min(tend - tbeg, (long)kShortMaxTokens);   // the host sends only L <= kShortMaxTokens
 
+    // extents (elements) of the buffers, for the bounds-checking build
+    const long qk_n = (long)total_tokens * hk * D, v_n = (long)total_tokens * hv * D, g_n = (long)total_tokens * hv;
+    const long state_n = (long)n_seqs * hv * D * D;
+    (void)qk_n; (void)v_n; (void)g_n; (void)state_n; (void)n_seqs;
+
     // stage the tokens: q, k rows of head hq (16-byte pieces), v of this CTA's rows, gates
     for (int i = tid; i < L * (D / 8); i += NT) {
         const int t = i / (D / 8), c = i % (D / 8);
         const size_t g = ((size_t)(tbeg + t) * hk + hq) * D + c * 8;
-        *reinterpret_cast<uint4 *>(&sm.k[t][c * 8]) = *reinterpret_cast<const uint4 *>(k + g);
-        *reinterpret_cast<uint4 *>(&sm.q[t][c * 8]) = *reinterpret_cast<const uint4 *>(q + g);
+        const bool ok = GDN_INB(g + 7, qk_n, err);
+        *reinterpret_cast<uint4 *>(&sm.k[t][c * 8]) = ok ? *reinterpret_cast<const uint4 *>(k + g) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(&sm.q[t][c * 8]) = ok ? *reinterpret_cast<const uint4 *>(q + g) : make_uint4(0, 0, 0, 0);
     }
     for (int i = tid; i < L * (ROWS / 8); i += NT) {
         const int t = i / (ROWS / 8), c = i % (ROWS / 8);
+        const size_t g = ((size_t)(tbeg + t) * hv + h) * D + slice * ROWS + c * 8;
         *reinterpret_cast<uint4 *>(&sm.v[t][c * 8]) =
-            *reinterpret_cast<const uint4 *>(v + ((size_t)(tbeg + t) * hv + h) * D + slice * ROWS + c * 8);
+            GDN_INB(g + 7, v_n, err) ? *reinterpret_cast<const uint4 *>(v + g) : make_uint4(0, 0, 0, 0);
     }
     for (int t = tid; t < L; t += NT) {
-        sm.alpha[t] = __expf(clamp_log_alpha(gate_log_alpha(log_alpha[(size_t)(tbeg + t) * hv + h], gate_c, gate_b, h)));
-        sm.beta[t] = gate_beta(beta[(size_t)(tbeg + t) * hv + h], gate_c);
+        const size_t g = (size_t)(tbeg + t) * hv + h;
+        const bool ok = GDN_INB(g, g_n, err);
+        sm.alpha[t] = __expf(clamp_log_alpha(ok ? gate_log_alpha(log_alpha[g], gate_c, gate_b, h) : 0.f));
+        sm.beta[t] = ok ? gate_beta(beta[g], gate_c) : 0.f;
     }
 
     // this lane group's 8 state rows, 4 columns per lane
     const size_t head = (size_t)n * hv + h;
     float4 s[kRowsPerGroup];
-    float4 *srow = final_state ? reinterpret_cast<float4 *>(final_state + (head * D + row_in_head) * D) + gl
-                               : nullptr;
-    if (init_state) {
+    const bool state_ok = GDN_INB((head * D + row_in_head + kRowsPerGroup - 1) * D + gl * 4 + 3, state_n, err);
+    float4 *srow = final_state && state_ok
+                       ? reinterpret_cast<float4 *>(final_state + (head * D + row_in_head) * D) + gl
+                       : nullptr;
+    if (init_state && state_ok) {
         const float4 *irow = reinterpret_cast<const float4 *>(init_state + (head * D + row_in_head) * D) + gl;
 #pragma unroll
         for (int i = 0; i < kRowsPerGroup; ++i) s[i] = irow[(size_t)i * (D / 4)];
@@ -366,6 +389,7 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
                     const float o = alpha * fq * part[j] + u[i] * kq;
                     const size_t oi = ((size_t)(tbeg + t) * hv + h) * D + row_in_head + i;
                     if (NORM) sm.o[t][vrow0 + i] = o;
+                    else if (!GDN_INB(oi, v_n, err)) continue;
                     else if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
                     else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(o);
                 }
@@ -416,6 +440,7 @@ short_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__re
             const int t = i / ROWS, j = i % ROWS;
             const float o = sm.o[t][j] * sm.ps[t] * norm_w[slice * ROWS + j];
             const size_t oi = ((size_t)(tbeg + t) * hv + h) * D + slice * ROWS + j;
+            if (!GDN_INB(oi, v_n, err)) continue;
             if (out_f32) reinterpret_cast<float *>(out)[oi] = o;
             else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(o);
         }
@@ -440,7 +465,7 @@ cudaError_t launch_short_dn(const PrefillProblem &p) {
     const cudaError_t e = cudaLaunchKernelEx(&cfg, short_prefill_kernel<D, NORM>, p.total_tokens, p.hk, p.hv, p.q, p.k, p.v,
                                              p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.out, p.out_f32,
                                              p.final_state, p.qk_norm, p.q_scale, p.norm_w, p.norm_eps, p.gate_c,
-                                             p.gate_b);
+                                             p.gate_b, p.n_seqs, p.err);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -478,7 +503,7 @@ cudaError_t launch_decode_d(const DecodeProblem &p, unsigned grid) {
     cfg.numAttrs = (NORM && D == 128) ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_step_kernel<D, PREP, NORM>, (int)((long)p.n * p.hv * p.d), p.hk,
                                              p.hv, p.state, p.q, p.k, p.v, p.log_alpha, p.beta, p.out, p.out_f32,
-                                             p.qk_norm, p.q_scale, p.norm_w, p.norm_eps, p.gate_c, p.gate_b);
+                                             p.qk_norm, p.q_scale, p.norm_w, p.norm_eps, p.gate_c, p.gate_b, p.err);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

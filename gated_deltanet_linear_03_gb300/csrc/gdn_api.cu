@@ -446,7 +446,8 @@ gdn_status gdn_decode_step(int n, int hk, int hv, int dk, int dv, float *state,
     p.qk_norm = qk_norm; p.q_scale = q_scale;
     p.norm_w = norm_weight; p.norm_eps = norm_eps;
     p.gate_c = gate_scale; p.gate_b = gate_bias;
-    p.err = nullptr;
+    p.err = device_error_ptr();
+    if (!p.err) return GDN_ERR_CUDA;
     p.stream = static_cast<cudaStream_t>(stream);
     return gdn::launch_decode(p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -469,8 +470,8 @@ gdn_status gdn_device_error(void *stream) {
         const unsigned int zero = 0;
         if (cudaMemcpy(ptr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return GDN_ERR_CUDA;
     }
+    if (word & (gdn::kErrInternal | gdn::kErrBounds)) return GDN_ERR_INTERNAL;   // the cause, before its timeouts
     if (word & gdn::kErrTimeout) return GDN_ERR_TIMEOUT;
-    if (word & gdn::kErrInternal) return GDN_ERR_INTERNAL;
     return GDN_OK;
 }
 

@@ -49,12 +49,29 @@ __device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_flo
 // their entries are atomics, so host threads that fill the same entry at once only repeat the work.
 constexpr int kMaxDevices = 256;
 
-// Error word bits set by kernels (read back by gdn_device_error).
-enum : unsigned int { kErrTimeout = 1u, kErrInternal = 2u };
+// Error word bits set by kernels (read back by gdn_device_error; kErrBounds is reported as GDN_ERR_INTERNAL).
+enum : unsigned int { kErrTimeout = 1u, kErrInternal = 2u, kErrBounds = 4u };
 
 __device__ __forceinline__ void raise_error(unsigned int *err, unsigned int bit) {
     if (err) atomicOr(err, bit);
 }
+
+// Bounds-checking build (compiled with -DGDN_DEBUG_BOUNDS, as libgdn_debug.so): before every global access
+// whose address a kernel computes, and before every tensor-copy request, GDN_INB(last, extent, err) checks
+// the highest element index the access touches against the extent of its buffer (in elements, or rows for a
+// tensor copy).  An access out of range is skipped and kErrBounds is recorded in the device error word; a
+// skipped tensor load leaves its barrier incomplete, so the kernel's bounded wait then ends it with
+// GDN_ERR_TIMEOUT as well.  Nothing traps.  In the normal build GDN_INB is the constant true and costs nothing.
+#ifdef GDN_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds_check(long long last, long long extent, unsigned int *err) {
+    if (last >= 0 && last < extent) return true;
+    raise_error(err, kErrBounds);
+    return false;
+}
+#define GDN_INB(last, extent, err) (::gdn::in_bounds_check((long long)(last), (long long)(extent), (err)))
+#else
+#define GDN_INB(last, extent, err) true
+#endif
 
 // Per-call plan passed to the launchers (validated on the host already).
 struct PrefillProblem {

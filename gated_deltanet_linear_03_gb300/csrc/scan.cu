@@ -66,22 +66,29 @@ __device__ __forceinline__ void stage_block(ScanSmem<D, PREP> &sm, int buf, long
                                             const __nv_bfloat16 *__restrict__ k,
                                             const __nv_bfloat16 *__restrict__ v,
                                             const float *__restrict__ log_alpha,
-                                            const float *__restrict__ beta) {
+                                            const float *__restrict__ beta, long total, unsigned int *err) {
     constexpr int QK_CHUNKS = D / 8;      // 16-byte pieces per q/k row
     constexpr int V_CHUNKS = kRows / 8;   // 16-byte pieces of the v slice
+    (void)total;
+    (void)err;
     for (int i = threadIdx.x; i < nt * QK_CHUNKS; i += kThreads) {
         const int t = i / QK_CHUNKS, c = i % QK_CHUNKS;
         const size_t g = ((size_t)(t0 + t) * hk + hq) * D + c * 8;
+        if (!GDN_INB(g + 7, total * hk * D, err)) continue;
         cp_async16(&sm.k[buf][t][c * 8], k + g);
         cp_async16(&sm.q[buf][t][c * 8], q + g);
     }
     for (int i = threadIdx.x; i < nt * V_CHUNKS; i += kThreads) {
         const int t = i / V_CHUNKS, c = i % V_CHUNKS;
-        cp_async16(&sm.v[buf][t][c * 8], v + ((size_t)(t0 + t) * hv + h) * D + row0 + c * 8);
+        const size_t g = ((size_t)(t0 + t) * hv + h) * D + row0 + c * 8;
+        if (!GDN_INB(g + 7, total * hv * D, err)) continue;
+        cp_async16(&sm.v[buf][t][c * 8], v + g);
     }
     for (int t = threadIdx.x; t < nt; t += kThreads) {
-        cp_async4(&sm.la[buf][t], log_alpha + (size_t)(t0 + t) * hv + h);
-        cp_async4(&sm.b[buf][t], beta + (size_t)(t0 + t) * hv + h);
+        const size_t g = (size_t)(t0 + t) * hv + h;
+        if (!GDN_INB(g, total * hv, err)) continue;
+        cp_async4(&sm.la[buf][t], log_alpha + g);
+        cp_async4(&sm.b[buf][t], beta + g);
     }
 }
 
@@ -96,7 +103,8 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
                     const float *__restrict__ init_state, const int32_t *__restrict__ cu_seqlens,
                     void *__restrict__ out, int out_f32, float *__restrict__ final_state, int qk_norm,
                     float q_scale, const float *__restrict__ norm_w, float norm_eps,
-                    const float *__restrict__ gate_c, const float *__restrict__ gate_b) {
+                    const float *__restrict__ gate_c, const float *__restrict__ gate_b, int n_seqs,
+                    unsigned int *err) {
     constexpr int COLS = D / kTPR;        // state columns per thread
     constexpr int SLICES = D / kRows;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -115,7 +123,9 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
     // S[4m + e] is column 4(c + kTPR m) + e of row r
     float S[COLS];
     const size_t srow = (((size_t)n * hv + h) * D + row0 + r) * D + 4 * c;
-    if (init_state) {
+    const bool state_ok = GDN_INB(srow + kTPR * (COLS - 4) + 3, (long)n_seqs * hv * D * D, err);
+    (void)n_seqs;
+    if (init_state && state_ok) {
 #pragma unroll
         for (int j = 0; j < COLS; j += 4) {
             const float4 x = *reinterpret_cast<const float4 *>(init_state + srow + kTPR * j);
@@ -129,7 +139,8 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
     const long ntok = tend - tbeg;
     const int nblk = (int)((ntok + kTB - 1) / kTB);
     if (nblk > 0) {
-        stage_block<D, PREP>(sm, 0, tbeg, (int)min((long)kTB, ntok), hk, hv, hq, h, row0, q, k, v, log_alpha, beta);
+        stage_block<D, PREP>(sm, 0, tbeg, (int)min((long)kTB, ntok), hk, hv, hq, h, row0, q, k, v, log_alpha, beta,
+                             total_tokens, err);
         cp_async_commit();
     }
     for (int blk = 0; blk < nblk; ++blk) {
@@ -139,7 +150,7 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
         if (blk + 1 < nblk) {
             const long t1 = t0 + kTB;
             stage_block<D, PREP>(sm, buf ^ 1, t1, (int)min((long)kTB, tend - t1), hk, hv, hq, h, row0, q, k, v,
-                           log_alpha, beta);
+                           log_alpha, beta, total_tokens, err);
         }
         cp_async_commit();
         cp_async_wait_prev();
@@ -250,6 +261,7 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
         for (int i = threadIdx.x; i < nt * kRows; i += kThreads) {
             const int t = i / kRows, j = i % kRows;
             const size_t oi = ((size_t)(t0 + t) * hv + h) * D + row0 + j;
+            if (!GDN_INB(oi, (long)total_tokens * hv * D, err)) continue;
             if (out_f32) reinterpret_cast<float *>(out)[oi] = sm.o[t][j];
             else reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(sm.o[t][j]);
         }
@@ -257,7 +269,7 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
     }
     cp_async_wait_all();
 
-    if (final_state) {
+    if (final_state && state_ok) {
 #pragma unroll
         for (int j = 0; j < COLS; j += 4)
             *reinterpret_cast<float4 *>(final_state + srow + kTPR * j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
@@ -294,7 +306,7 @@ cudaError_t launch_scan_dp(const PrefillProblem &p) {
     cfg.numAttrs = NORM ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, scan_prefill_kernel<D, PREP, NORM>, p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha,
                            p.beta, p.init_state, p.cu_seqlens, p.out, p.out_f32, p.final_state, p.qk_norm, p.q_scale,
-                           p.norm_w, p.norm_eps, p.gate_c, p.gate_b);
+                           p.norm_w, p.norm_eps, p.gate_c, p.gate_b, p.n_seqs, p.err);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

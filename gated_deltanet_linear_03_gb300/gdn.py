@@ -39,12 +39,20 @@ _lib = None
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libgdn.so (built by ``__graft_entry__.build()``); raises if it is missing."""
+    """Load libgdn.so (built by ``__graft_entry__.build()``); raises if it is missing.  The handle is kept:
+    the wrappers below use it unless given another one (``lib=``)."""
     global _lib
     if _lib is not None:
         return _lib
+    _lib = bind(path)
+    return _lib
+
+
+def bind(path: str) -> ctypes.CDLL:
+    """A configured handle of a library with the gdn.h ABI at ``path`` (e.g. the bounds-checking build
+    ``libgdn_debug.so``), not kept as the default."""
     if not os.path.exists(path):
-        raise RuntimeError(f"libgdn.so not found at {path}; build it with "
+        raise RuntimeError(f"{os.path.basename(path)} not found at {path}; build it with "
                            "`python -c 'import __graft_entry__ as g; g.build()'`")
     lib = ctypes.CDLL(path)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -74,7 +82,6 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdn_status_string.argtypes = [I]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_version.restype = I
-    _lib = lib
     return lib
 
 
@@ -144,8 +151,8 @@ def resolve_algo(n_seqs: int, total_tokens: int, hk: int, hv: int, dk: int, dv: 
 
 
 def workspace_size(n_seqs: int, total_tokens: int, hk: int, hv: int, dk: int, dv: int,
-                   cu_seqlens_host: Sequence[int], algo: str = "chunked") -> int:
-    lib = load_library()
+                   cu_seqlens_host: Sequence[int], algo: str = "chunked", lib=None) -> int:
+    lib = lib or load_library()
     arr = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
     st = ctypes.c_int(0)
     n = lib.gdn_prefill_workspace_size(n_seqs, total_tokens, hk, hv, dk, dv, arr, ALGO[algo], ctypes.byref(st))
@@ -160,8 +167,9 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
             final_state=True, algo: str = "chunked", workspace: Optional[torch.Tensor] = None,
             cu_seqlens_host: Optional[Sequence[int]] = None, stream=None, qk_norm: bool = False,
             q_scale: float = 1.0, norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6,
-            gate_scale: Optional[torch.Tensor] = None, gate_bias: Optional[torch.Tensor] = None):
-    """Run ``gdn_prefill``.  Returns ``(out, final_state)``.
+            gate_scale: Optional[torch.Tensor] = None, gate_bias: Optional[torch.Tensor] = None, lib=None):
+    """Run ``gdn_prefill``.  Returns ``(out, final_state)``.  ``lib``: a handle from :func:`bind` instead of the
+    default library.
 
     ``gate_scale`` / ``gate_bias`` (fp32 [hv] each): ``log_alpha`` and ``beta`` hold raw per-token inputs a, y and
     the kernels compute log_alpha = -gate_scale softplus(a + gate_bias), beta = sigmoid(y).
@@ -173,7 +181,7 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
     ``final_state`` may be ``True`` (allocate), ``False``/``None`` (do not emit)
     or a tensor to write into (it may be ``init_state`` for an in-place update).
     """
-    lib = load_library()
+    lib = lib or load_library()
     _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 3)
     _need(v, "v", torch.bfloat16, 3)
@@ -196,7 +204,7 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, log_alpha: torch.
     elif final_state is not None:
         _need(final_state, "final_state", torch.float32, 4)
     cu_arr, cu_vals = _host_cu(cu_seqlens, cu_seqlens_host)
-    need = workspace_size(n_seqs, T, hk, hv, dk, dv, cu_vals, algo) if n_seqs > 0 else 0
+    need = workspace_size(n_seqs, T, hk, hv, dk, dv, cu_vals, algo, lib=lib) if n_seqs > 0 else 0
     if need and workspace is None:
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -425,11 +433,13 @@ def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.
                 log_alpha: torch.Tensor, beta: torch.Tensor, *, out: Optional[torch.Tensor] = None,
                 out_dtype=torch.bfloat16, stream=None, qk_norm: bool = False, q_scale: float = 1.0,
                 norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-6,
-                gate_scale: Optional[torch.Tensor] = None, gate_bias: Optional[torch.Tensor] = None) -> torch.Tensor:
+                gate_scale: Optional[torch.Tensor] = None, gate_bias: Optional[torch.Tensor] = None,
+                lib=None) -> torch.Tensor:
     """Run ``gdn_decode_step`` (state updated in place).  Returns ``out``.
 
-    ``norm_weight`` (fp32 [dv]): fuse the output normalisation o / sqrt(mean(o^2) + norm_eps) * weight."""
-    lib = load_library()
+    ``norm_weight`` (fp32 [dv]): fuse the output normalisation o / sqrt(mean(o^2) + norm_eps) * weight.
+    ``lib``: a handle from :func:`bind` instead of the default library."""
+    lib = lib or load_library()
     _need(state, "state", torch.float32, 4)
     _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 3)
@@ -453,12 +463,12 @@ def decode_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.
     return out
 
 
-def device_error(stream=None, device=None) -> int:
+def device_error(stream=None, device=None, lib=None) -> int:
     """Synchronise and return the device-side error status (0 = none) of ``device`` (default: the current
-    device; the error word is per device, shared by all of its streams)."""
+    device; the error word is per device, shared by all of its streams) kept by ``lib`` (default library)."""
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(device):
-        return int(load_library().gdn_device_error(_stream_ptr(stream, device)))
+        return int((lib or load_library()).gdn_device_error(_stream_ptr(stream, device)))
 
 
 def selftest_bounded_wait(limit_us: int, stream=None) -> None:
