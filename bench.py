@@ -391,6 +391,28 @@ def run_each_kernel_once(args):
     return 0 if err == 0 else 1
 
 
+def run_decode_replicas(args):
+    """Profiler target for the decode step's DRAM traffic: the batched 30-layer step on five 60 MiB state
+    replicas (300 MiB, more than L2), three untimed warm-up rounds, then five consecutive launches, one per
+    replica, as in the timed decode measurement.  Nothing is timed."""
+    import torch
+    from gated_deltanet_linear_03_gb300 import gdn, synth
+    dev = torch.device("cuda", 0)
+    gdn.load_library()
+    di = synth.decode_30(steps=4)
+    states = [di.state.to(dev) for _ in range(5)]
+    q, k, v = di.q.to(dev), di.k.to(dev), di.v.to(dev)
+    la, b = di.log_alpha.to(dev), di.beta.to(dev)
+    out = torch.empty(DECODE_LAYERS, HV, D, dtype=torch.bfloat16, device=dev)
+    for r in range(4):
+        for i in range(5):
+            gdn.decode_step(states[i], q[r], k[r], v[r], la[r], b[r], out=out)
+    err = gdn.device_error()
+    print(json.dumps({"profile_target": "decode step, 3 warm-up rounds then 5 launches on 5 rotating state replicas",
+                      "bytes_per_launch_algorithmic": DECODE_STATE_BYTES, "device_error": err}))
+    return 0 if err == 0 else 1
+
+
 def run_crossover(args):
     """Short-to-long prefill sweep: device time per call of the direct scan and of the chunked path (and, for
     a few tokens, of that many batched decode steps) for N sequences of T tokens each, continuing from a
@@ -488,15 +510,21 @@ def time_long_context(dev, stream, decode_steps=64):
     inp = synth.prefill_inputs([T], seed=1003, device=dev)
     args = (inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.cu_seqlens.to(dev))
     res = {"workload": "1 sequence x 131072 tokens, 16 q/k heads, 32 v heads, d=128, bf16 q/k/v, "
-                       "final state emitted"}
-    state = None
-    for algo, iters in (("chunked", 5), ("scan", 2)):
-        plan = gdn.PrefillPlan(*args, algo=algo, cu_seqlens_host=[0, T])
-        ms = time_plan(plan, stream, iters)
-        res[algo] = {"ms": ms, "tok_per_s": T / (ms * 1e-3)}
-        if algo == "chunked":
-            state = plan.final_state.clone()
-        del plan
+                       "final state emitted",
+           "protocol": "chunked and scan runs interleaved (chunked, scan, chunked, scan, ...), 3 of each after one "
+                       "untimed run of each; medians"}
+    plans = {algo: gdn.PrefillPlan(*args, algo=algo, cu_seqlens_host=[0, T]) for algo in ("chunked", "scan")}
+    times = {"chunked": [], "scan": []}
+    for algo in ("chunked", "scan"):
+        time_plan(plans[algo], stream, 1)
+    for _ in range(3):   # alternate the two paths so that clock or thermal drift affects both alike
+        for algo in ("chunked", "scan"):
+            times[algo].append(time_plan(plans[algo], stream, 1))
+    for algo in ("chunked", "scan"):
+        ms = statistics.median(times[algo])
+        res[algo] = {"ms": ms, "tok_per_s": T / (ms * 1e-3), "runs_ms": times[algo]}
+    state = plans["chunked"].final_state.clone()
+    del plans
     res["chunked_over_scan_speedup"] = res["scan"]["ms"] / res["chunked"]["ms"]
     di = synth.decode_inputs(1, decode_steps, seed=1006, device=dev)
     out = torch.empty(1, HV, D, dtype=torch.bfloat16, device=dev)
@@ -720,8 +748,9 @@ def run_gb300(args):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "algo": "chunked (tcgen05)", "parallelism": f"replicas x{world}",
-                   "l2": f"{n_rep} rotating input replicas (~{n_rep * 97} MiB) > L2"},
+        "config": {"workload": WORKLOAD},
+        "setup": {"algo": "chunked (tcgen05)", "parallelism": f"replicas x{world}",
+                  "l2": f"{n_rep} rotating input replicas (~{n_rep * 97} MiB) > L2"},
         "roofline": roofline,
         "kernels": kernels,
         "decode": {"workload": "batch-1 decode step, 30 layers x 32 v heads x 128x128 fp32 state, bf16 q/k/v",
@@ -736,8 +765,7 @@ def run_gb300(args):
                                           "hbm_gbs": DECODE_STATE_BYTES / (decode_layer_us * 1e-6) / 1e9,
                                           "launch": "30 single-layer launches per step, 64 steps in one "
                                                     "CUDA graph"}},
-        "scan": {"tok_per_s": T_TOKENS / (scan_ms * 1e-3), "ms": scan_ms,
-                 "fp32_tflops": FLOPS_SCAN * T_TOKENS * HV / (scan_ms * 1e-3) / 1e12},
+        "scan": scan_line(scan_ms, clocks, dev),
         "qk_prep": qk_prep,
         "long_context": long_ctx,
         "ragged": ragged,
@@ -755,6 +783,20 @@ def run_gb300(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def scan_line(scan_ms, clocks, dev):
+    """The direct scan on the 4K layer against the FP32 pipe: 6 d^2 FLOP per token per head on the CUDA cores;
+    peak = SMs x 128 FP32 lanes x 2 FLOP (one FMA) x the median SM clock sampled during the run."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0
+    peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+    tflops = FLOPS_SCAN * T_TOKENS * HV / (scan_ms * 1e-3) / 1e12
+    return {"tok_per_s": T_TOKENS / (scan_ms * 1e-3), "ms": scan_ms, "fp32_tflops": tflops,
+            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                         "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 FLOP x {mhz:.0f} MHz (median SM clock "
+                                        "sampled during the run)"}}
 
 
 def load_traffic(kernel: str):
@@ -782,6 +824,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--each-kernel-once", action="store_true",
                     help="run every kernel of the path twice on the bench workload, untimed (profiler target)")
+    ap.add_argument("--decode-replicas", action="store_true",
+                    help="decode step on 5 rotating state replicas after warm-up, untimed (profiler target)")
     ap.add_argument("--crossover", action="store_true",
                     help="sweep short to long sequences: scan vs chunked (vs decode steps) device time per call")
     args = ap.parse_args(argv)
@@ -789,6 +833,8 @@ def main(argv=None):
         return run_each_kernel_once(args)
     if args.crossover:
         return run_crossover(args)
+    if args.decode_replicas:
+        return run_decode_replicas(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -29,6 +29,12 @@ using sm100::ld_dsmem_f32;
 constexpr int kRowsPerGroup = 8;   // rows each lane group carries at once
 constexpr int kThreads = 128;
 
+// Threads of a decode CTA: 128 (32 rows at d = 128), except that with the output normalisation a d = 128 head
+// is one CTA of 512 threads, so that its sum of squares is a CTA reduction (at d = 32 and 64 a 128-thread CTA
+// already holds whole heads).  Both keep 32 warps per SM.
+template <int D, bool NORM>
+__host__ __device__ constexpr int decode_threads() { return (NORM && D == 128) ? 512 : kThreads; }
+
 // Reduce 16 per-lane partial sums over groups of LPR lanes by recursive
 // halving: each round a lane keeps half of its values and receives the
 // partner's partials for that half.  Afterwards lane `g` of a group holds the
@@ -57,11 +63,14 @@ __device__ __forceinline__ void reduce16(float (&v)[16], int lane) {
 }
 
 // NORM: fuse the output normalisation o <- o / sqrt(mean_head(o^2) + eps) * w.  Each warp's rows belong to
-// one head; a head is one warp (d = 32), one CTA (d = 64) or a cluster of four CTAs (d = 128), whose partial
-// sums of squares are exchanged through distributed shared memory.
+// one head; a head is one warp (d = 32) or one CTA (d = 64: 128 threads; d = 128: 512 threads), so the
+// head's sum of squares is a warp or CTA reduction.  (A d = 128 head used to span a cluster of four
+// 128-thread CTAs, whose two cluster barrier rounds per step cost 0.2 of the HBM rate.)
 // PREP: query/key preparation (qk_norm, or q_scale != 1); the plain instantiation has none of its arithmetic.
-template <int D, bool PREP, bool NORM>
-__global__ void __launch_bounds__(kThreads)
+// GATE: the gates are formed from raw inputs (gdn.h: gate_scale, gate_bias); the plain instantiation has no
+// gate code.
+template <int D, bool PREP, bool NORM, bool GATE>
+__global__ void __launch_bounds__(decode_threads<D, NORM>())
 decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
                    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                    const __nv_bfloat16 *__restrict__ v, const float *__restrict__ log_alpha,
@@ -71,11 +80,12 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
     constexpr int LPR = D / 4;                  // lanes per row
     constexpr int GROUPS = 32 / LPR;            // lane groups per warp
     constexpr int WARP_ROWS = GROUPS * kRowsPerGroup;
+    constexpr int NT = decode_threads<D, NORM>();
     constexpr int PER = (16 / LPR) > 0 ? (16 / LPR) : 1;  // sums held per lane after reduce16
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int group = lane / LPR, gl = lane % LPR;
-    const long row0 = ((long)blockIdx.x * (kThreads / 32) + warp) * WARP_ROWS + group * kRowsPerGroup;
+    const long row0 = ((long)blockIdx.x * (NT / 32) + warp) * WARP_ROWS + group * kRowsPerGroup;
     // whole group out of range (8 | D keeps groups in one head).  With NORM and d >= 64 the grid covers the
     // rows exactly (the host checks), so no thread of a CTA that meets a barrier below leaves early.
     if (row0 >= total_rows) return;
@@ -127,9 +137,12 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
     if (PREP) kq *= fk * fq;
 
     const bool gate_ok = GDN_INB(head, n_states * hv, err);
-    const float la = clamp_log_alpha(gate_ok ? gate_log_alpha(log_alpha[head], gate_c, gate_b, h) : 0.f);
-    const float alpha = __expf(la);
-    const float b = gate_ok ? gate_beta(beta[head], gate_c) : 0.f;
+    float la_raw = gate_ok ? log_alpha[head] : 0.f, b = gate_ok ? beta[head] : 0.f;
+    if (GATE) {
+        la_raw = gate_log_alpha(la_raw, gate_c, gate_b, h);
+        b = gate_beta(b, gate_c);
+    }
+    const float alpha = __expf(clamp_log_alpha(la_raw));
 
     float part[16];
 #pragma unroll
@@ -185,22 +198,16 @@ decode_step_kernel(int total_rows, int hk, int hv, float *__restrict__ state,
     }
     float scale = 1.f;
     if (NORM) {
-        __shared__ float warp_ss[kThreads / 32];
-        __shared__ float cta_ss;
+        __shared__ float warp_ss[NT / 32];
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         float head_ss = ss;   // d = 32: the warp is the head
-        if (D >= 64) {
+        if (D >= 64) {        // d = 64, 128: the CTA is the head
             if (lane == 0) warp_ss[warp] = ss;
             __syncthreads();
-            head_ss = (warp_ss[0] + warp_ss[1]) + (warp_ss[2] + warp_ss[3]);
-            if (D == 128) {   // the head spans the four CTAs of this cluster
-                if (threadIdx.x == 0) cta_ss = head_ss;
-                cluster_sync();
-                head_ss = (ld_dsmem_f32(&cta_ss, 0) + ld_dsmem_f32(&cta_ss, 1)) +
-                          (ld_dsmem_f32(&cta_ss, 2) + ld_dsmem_f32(&cta_ss, 3));
-                cluster_sync();   // no CTA leaves while its partial may still be read
-            }
+            head_ss = 0.f;
+#pragma unroll
+            for (int w = 0; w < NT / 32; ++w) head_ss += warp_ss[w];
         }
         scale = rsqrtf(head_ss * (1.f / D) + norm_eps);
     }
@@ -488,54 +495,48 @@ cudaError_t launch_short_prefill(const PrefillProblem &p) {
 
 namespace {
 
-template <int D, bool PREP, bool NORM>
-cudaError_t launch_decode_d(const DecodeProblem &p, unsigned grid) {
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (NORM && D == 128) ? 4 : 1;   // four 32-row CTAs make a 128-row head
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+template <int D, bool PREP, bool NORM, bool GATE>
+cudaError_t launch_decode_dg(const DecodeProblem &p) {
+    constexpr int NT = decode_threads<D, NORM>();
+    constexpr long rows_per_block = (long)(NT / 32) * (32 / (D / 4)) * kRowsPerGroup;
+    const long total_rows = (long)p.n * p.hv * p.d;
+    // with the output normalisation a CTA holds whole heads (d >= 64) or whole warps do (d = 32): no CTA may
+    // end early, so the rows must fill the grid exactly (always true: rows_per_block divides hv * d)
+    if (NORM && D >= 64 && total_rows % rows_per_block) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.gridDim = dim3((unsigned)((total_rows + rows_per_block - 1) / rows_per_block));
+    cfg.blockDim = dim3(NT);
     cfg.stream = p.stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = (NORM && D == 128) ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_step_kernel<D, PREP, NORM>, (int)((long)p.n * p.hv * p.d), p.hk,
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_step_kernel<D, PREP, NORM, GATE>, (int)((long)p.n * p.hv * p.d), p.hk,
                                              p.hv, p.state, p.q, p.k, p.v, p.log_alpha, p.beta, p.out, p.out_f32,
                                              p.qk_norm, p.q_scale, p.norm_w, p.norm_eps, p.gate_c, p.gate_b, p.err);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+template <int D, bool PREP, bool NORM>
+cudaError_t launch_decode_d(const DecodeProblem &p) {
+    return p.gate_c ? launch_decode_dg<D, PREP, NORM, true>(p) : launch_decode_dg<D, PREP, NORM, false>(p);
+}
+
 template <int D, bool PREP>
-cudaError_t launch_decode_prep(const DecodeProblem &p, unsigned grid) {
-    return p.norm_w ? launch_decode_d<D, PREP, true>(p, grid) : launch_decode_d<D, PREP, false>(p, grid);
+cudaError_t launch_decode_prep(const DecodeProblem &p) {
+    return p.norm_w ? launch_decode_d<D, PREP, true>(p) : launch_decode_d<D, PREP, false>(p);
 }
 
 template <int D>
-cudaError_t launch_decode_norm(const DecodeProblem &p, unsigned grid) {
-    return (p.qk_norm || p.q_scale != 1.f) ? launch_decode_prep<D, true>(p, grid) : launch_decode_prep<D, false>(p, grid);
+cudaError_t launch_decode_norm(const DecodeProblem &p) {
+    return (p.qk_norm || p.q_scale != 1.f) ? launch_decode_prep<D, true>(p) : launch_decode_prep<D, false>(p);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeProblem &p) {
-    const long total_rows = (long)p.n * p.hv * p.d;
-    if (total_rows == 0) return cudaSuccess;
-    int warp_rows = 0;
+    if ((long)p.n * p.hv * p.d == 0) return cudaSuccess;
     switch (p.d) {
-        case 32: warp_rows = 4 * kRowsPerGroup; break;
-        case 64: warp_rows = 2 * kRowsPerGroup; break;
-        case 128: warp_rows = kRowsPerGroup; break;
+        case 32: return launch_decode_norm<32>(p);
+        case 64: return launch_decode_norm<64>(p);
+        case 128: return launch_decode_norm<128>(p);
         default: return cudaErrorInvalidValue;
-    }
-    const long rows_per_block = (long)warp_rows * (kThreads / 32);
-    if (p.norm_w && p.d >= 64 && total_rows % rows_per_block) return cudaErrorInvalidValue;   // see the kernel
-    const unsigned grid = (unsigned)((total_rows + rows_per_block - 1) / rows_per_block);
-    switch (p.d) {
-        case 32: return launch_decode_norm<32>(p, grid);
-        case 64: return launch_decode_norm<64>(p, grid);
-        default: return launch_decode_norm<128>(p, grid);
     }
 }
 

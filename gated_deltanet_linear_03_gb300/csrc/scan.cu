@@ -95,7 +95,9 @@ __device__ __forceinline__ void stage_block(ScanSmem<D, PREP> &sm, int buf, long
 // PREP: query/key preparation enabled (qk_norm, or q_scale != 1); without it the token loop is the plain one.
 // NORM: fused output normalisation (launched as a cluster of the head's slices); the plain instantiation
 // carries no cluster code (its presence alone slowed the plain scan by 17%).
-template <int D, bool PREP, bool NORM>
+// GATE: the gates are formed from raw inputs (gdn.h: gate_scale, gate_bias); a separate instantiation for the
+// same reason (the gate code alone changed the plain scan's register allocation and cost it 11%).
+template <int D, bool PREP, bool NORM, bool GATE>
 __global__ void __launch_bounds__(kThreads)
 scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__restrict__ q,
                     const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
@@ -155,6 +157,13 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
         cp_async_commit();
         cp_async_wait_prev();
         __syncthreads();
+        if (GATE) {   // gates from raw inputs: mapped once per token of the block, in place (read after the
+                      // barrier that ends the k.q pass below)
+            for (int t = threadIdx.x; t < nt; t += kThreads) {
+                sm.la[buf][t] = gate_log_alpha(sm.la[buf][t], gate_c, gate_b, h);
+                sm.b[buf][t] = gate_beta(sm.b[buf][t], gate_c);
+            }
+        }
         // k.q (and |k|^2, |q|^2) of every token of the block, once: 16 lanes per token, 8 tokens per round.
         // Every warp runs the same number of rounds (the shuffles need all 32 lanes); tokens past nt compute
         // nothing.
@@ -178,10 +187,6 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
                 qq += __shfl_xor_sync(0xffffffffu, qq, off);
             }
             if (l == 0 && t < nt) {
-                if (gate_c) {   // gates from raw inputs: mapped once per token, in place
-                    sm.la[buf][t] = gate_log_alpha(sm.la[buf][t], gate_c, gate_b, h);
-                    sm.b[buf][t] = gate_beta(sm.b[buf][t], gate_c);
-                }
                 if (PREP) {
                     const float fk = qk_inv_norm(kk, qk_norm), fq = q_scale * qk_inv_norm(qq, qk_norm);
                     sm.fk[t] = fk;
@@ -276,8 +281,8 @@ scan_prefill_kernel(int total_tokens, int hk, int hv, const __nv_bfloat16 *__res
     }
 }
 
-template <int D, bool PREP, bool NORM>
-cudaError_t launch_scan_dp(const PrefillProblem &p) {
+template <int D, bool PREP, bool NORM, bool GATE>
+cudaError_t launch_scan_dpg(const PrefillProblem &p) {
     const size_t smem = sizeof(ScanSmem<D, PREP>);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -285,7 +290,7 @@ cudaError_t launch_scan_dp(const PrefillProblem &p) {
     static std::atomic<bool> attr_set[kMaxDevices];
     const bool cached = dev >= 0 && dev < kMaxDevices;
     if (!cached || !attr_set[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(scan_prefill_kernel<D, PREP, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(scan_prefill_kernel<D, PREP, NORM, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         if (cached) attr_set[dev].store(true, std::memory_order_release);
@@ -304,11 +309,16 @@ cudaError_t launch_scan_dp(const PrefillProblem &p) {
     cfg.stream = p.stream;
     cfg.attrs = attr;
     cfg.numAttrs = NORM ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, scan_prefill_kernel<D, PREP, NORM>, p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha,
+    e = cudaLaunchKernelEx(&cfg, scan_prefill_kernel<D, PREP, NORM, GATE>, p.total_tokens, p.hk, p.hv, p.q, p.k, p.v, p.log_alpha,
                            p.beta, p.init_state, p.cu_seqlens, p.out, p.out_f32, p.final_state, p.qk_norm, p.q_scale,
                            p.norm_w, p.norm_eps, p.gate_c, p.gate_b, p.n_seqs, p.err);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int D, bool PREP, bool NORM>
+cudaError_t launch_scan_dp(const PrefillProblem &p) {
+    return p.gate_c ? launch_scan_dpg<D, PREP, NORM, true>(p) : launch_scan_dpg<D, PREP, NORM, false>(p);
 }
 
 template <int D, bool NORM>
