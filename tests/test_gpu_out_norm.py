@@ -29,7 +29,7 @@ def bf16_ok(out, ref):
     return np.all(np.abs(np32(out).astype(np.float64) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-3)
 
 
-# d = 128: four CTAs of 32 rows per head (a cluster); d = 64: one CTA per head; d = 32: one warp per head,
+# d = 128: one 512-thread CTA per head; d = 64: one 128-thread CTA per head; d = 32: one warp per head,
 # including a batch whose rows leave the last CTA partly empty (n * hv * 32 not a multiple of 128)
 @pytest.mark.parametrize("d,hk,hv,n", [(128, 16, 32, 30), (128, 2, 4, 1), (64, 2, 4, 3), (32, 2, 2, 5), (32, 1, 1, 3)])
 @pytest.mark.parametrize("qk_norm", [False, True])
