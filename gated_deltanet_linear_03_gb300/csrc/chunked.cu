@@ -929,9 +929,13 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         tma_prefetch_desc(&rlmap);
         pass_issue_loads(sm, &bar_tma[0], &qmap, &kmap, &phmap, &plmap, &rhmap, &rlmap, hq, ta, gc0, hv, h, hk, total, nch, err);
     }
-    ChunkInputs nxt;
-    if (started)
+    ChunkInputs nxt, nxt2;   // loaded two chunks ahead, as in state_pass_kernel
+    if (started) {
         load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0, ta, min(C, tb - ta), hv, h, rowg, lane, krow, i, total, nch, err);
+        if (nchunks > 1)
+            load_chunk_inputs(nxt2, log_alpha, beta, v, norms, q_scale, gc0 + 1, ta + C, min(C, tb - ta - C), hv, h,
+                              rowg, lane, krow, i, total, nch, err);
+    }
 
     // state columns: thread (d, grp) holds S[rowg + r][d] for r < DG
     float S[DG];
@@ -993,6 +997,7 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         const int t0 = ta + c * C, L = min(C, tb - t0);
         const int gc = gc0 + c;
         ChunkInputs cur = nxt;
+        nxt = nxt2;
         finish_gates<GATE>(cur, L, lane, krow, i, gate_c, gate_b, h);
         const uint64_t so = s * kStageStep;
 
@@ -1016,9 +1021,9 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             else
                 ok = false;
         }
-        if (c + 1 < nchunks)
-            load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc + 1, t0 + C, min(C, tb - t0 - C), hv, h,
-                              rowg, lane, krow, i, total, nch, err);
+        if (c + 2 < nchunks)
+            load_chunk_inputs(nxt2, log_alpha, beta, v, norms, q_scale, gc + 2, t0 + 2 * C, min(C, tb - t0 - 2 * C),
+                              hv, h, rowg, lane, krow, i, total, nch, err);
 
         const float2 g2 = cumsum_pairs(cur.la0, cur.la1, L, lane);
         const float gL = g_of(g2, L - 1);
@@ -1394,10 +1399,16 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         const int rowg = row0 + grp * DG;
         const uint32_t tlane = (uint32_t)(32 * quad) << 16;
 
-        ChunkInputs nxt;
-        if (started)
+        // per-chunk inputs are loaded two chunks ahead: under the pass's tile traffic a global load can take
+        // longer than one chunk (one chunk ahead left the K-row threads waiting on them at the top of the loop)
+        ChunkInputs nxt, nxt2;
+        if (started) {
             load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0, ta, min(C, tb - ta), hv, h, rowg, lane,
                               krow, i, total, nch, err);
+            if (nchunks > 1)
+                load_chunk_inputs(nxt2, log_alpha, beta, v, norms, q_scale, gc0 + 1, ta + C, min(C, tb - ta - C), hv,
+                                  h, rowg, lane, krow, i, total, nch, err);
+        }
         float S[DG];
         const size_t sbase = (((size_t)n * hv + h) * D + rowg) * D + d;
         const bool state_ok = GDN_INB(sbase + (size_t)(DG - 1) * D, (long)n_seqs * hv * D * D, err);
@@ -1434,10 +1445,11 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             const uint32_t par = c & 1;
             const int t0 = ta + c * C, L = min(C, tb - t0);
             ChunkInputs cur = nxt;
+            nxt = nxt2;
             finish_gates<GATE>(cur, L, lane, krow, i, gate_c, gate_b, h);
-            if (c + 1 < nchunks)
-                load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0 + c + 1, t0 + C, min(C, tb - t0 - C),
-                                  hv, h, rowg, lane, krow, i, total, nch, err);
+            if (c + 2 < nchunks)
+                load_chunk_inputs(nxt2, log_alpha, beta, v, norms, q_scale, gc0 + c + 2, t0 + 2 * C,
+                                  min(C, tb - t0 - 2 * C), hv, h, rowg, lane, krow, i, total, nch, err);
             const float2 g2 = cumsum_pairs(cur.la0, cur.la1, L, lane);
             const float gL = g_of(g2, L - 1);
             const float eg = __expf(g_of(g2, i));
