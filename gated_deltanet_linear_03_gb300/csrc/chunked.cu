@@ -33,6 +33,9 @@
 // one bf16 pass.  The triangular solve runs in fp32 on the CUDA cores.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "gdn_internal.cuh"
 #include "sm100.cuh"
 
@@ -88,6 +91,61 @@ __device__ int first_chunk_of(const int32_t *cu, int n, int total) {
     }
     return acc;
 }
+
+// A position in the chunks of a run of consecutive sequences: sequence n (tokens [ta, tb), nk chunks), its
+// chunk k.  Past the run, n = end and the chunk is empty.
+struct ChunkCursor {
+    int n, ta, tb, k, nk;
+    __device__ __forceinline__ int t0() const { return ta + k * C; }
+    __device__ __forceinline__ int len() const { return min(C, tb - ta - k * C); }
+    __device__ __forceinline__ bool last_of_seq() const { return k == nk - 1; }
+};
+
+__device__ __forceinline__ void cursor_at_seq(ChunkCursor &cc, const int32_t *cu, int n_seqs, int total, int n) {
+    cc.n = n;
+    cc.k = 0;
+    if (n_seqs == 1) {   // the host checked cu_seqlens = {0, total}
+        cc.ta = 0;
+        cc.tb = total;
+    } else {
+        seq_range(cu, n, total, cc.ta, cc.tb);
+    }
+    cc.nk = (cc.tb - cc.ta + C - 1) / C;
+}
+
+// The first chunk of the first sequence in [m, end) that has tokens; on_empty(m') is called for every sequence
+// without tokens passed over.
+template <typename F>
+__device__ __forceinline__ void cursor_seek(ChunkCursor &cc, const int32_t *cu, int n_seqs, int total, int m,
+                                            int end, F on_empty) {
+    for (; m < end; ++m) {
+        cursor_at_seq(cc, cu, n_seqs, total, m);
+        if (cc.nk > 0) return;
+        on_empty(m);
+    }
+    cc.n = end;
+    cc.k = cc.nk = 0;
+    cc.ta = cc.tb = total;
+}
+
+// The next chunk of the run: the next one of this sequence, else the first of the next sequence with tokens.
+template <typename F>
+__device__ __forceinline__ void cursor_next(ChunkCursor &cc, const int32_t *cu, int n_seqs, int total, int end,
+                                            F on_empty) {
+    if (++cc.k < cc.nk) return;
+    cursor_seek(cc, cu, n_seqs, total, cc.n + 1, end, on_empty);
+}
+
+// Sequence buckets of the plain state pass: CTA (bucket b, head, row slice) carries the state through the
+// sequences [seq[b], seq[b+1]) one after another, which are the global chunks [chunk[b], chunk[b+1])
+// (sequences are packed, and their chunks numbered, in order).  The host balances the buckets by chunks.
+// With per_seq, bucket b is sequence b and its first chunk is found from cu_seqlens (any number of sequences).
+constexpr int kMaxPassBuckets = 64;
+struct PassBuckets {
+    int per_seq;
+    int seq[kMaxPassBuckets + 1];
+    int chunk[kMaxPassBuckets + 1];
+};
 
 // The next 1 KiB boundary of a dynamic shared-memory pointer.  Pointer arithmetic (no integer round trip)
 // keeps the shared address space visible to the compiler, so accesses through the result compile to
@@ -1191,7 +1249,9 @@ constexpr int kWsThreads = kPassThreads + 64;
 constexpr int kMmaWarp = kPassThreads / 32, kTmaWarp = kMmaWarp + 1;
 constexpr uint32_t kPTx = 16384 + 16384, kRTx = 8192 + 8192;
 
-template <bool GATE>
+// MULTI: a CTA may carry several sequences (buckets of more than one); without it each bucket is one sequence
+// and the chunk loop has none of the sequence-boundary code.
+template <bool GATE, bool MULTI>
 __global__ void __launch_bounds__(kWsThreads, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
@@ -1200,32 +1260,49 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                   const float *__restrict__ log_alpha, const float *__restrict__ beta,
                   const float *__restrict__ init_state, const int32_t *__restrict__ cu, int n_seqs, int total,
                   int nch, int hk, int hv, void *__restrict__ out, int out_f32, float *__restrict__ final_state,
-                  const float *__restrict__ gate_c, const float *__restrict__ gate_b, unsigned int *err) {
+                  const float *__restrict__ gate_c, const float *__restrict__ gate_b, unsigned int *err,
+                  const __grid_constant__ PassBuckets bk) {
     extern __shared__ uint8_t pass_raw[];
     uint8_t *sm = align1024(pass_raw);
     __shared__ uint64_t bar_qk[2], bar_p[2], bar_r[2], bar_qkf[2], bar_pf[2], bar_rf[2];
     __shared__ uint64_t bar_s, bar_x[2], bar_d1, bar_px, bar_rx[2];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;   // set by any thread whose wait ran out; everyone stops at the next check
+    __shared__ int warp_chunks[kWsThreads / 32];
 
     constexpr int SLICES = D / DS;
     const int slice = blockIdx.x % SLICES;
     const int h = (blockIdx.x / SLICES) % hv;
-    const int n = blockIdx.x / (SLICES * hv);
+    const int bucket = blockIdx.x / (SLICES * hv);
     const int hq = h / (hv / hk);
     const int row0 = slice * DS;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = smem_u32(sm);
 
-    int ta = 0, tb = total, gc0 = 0;   // one sequence: the host checked cu_seqlens = {0, total}
-    if (n_seqs > 1) {
-        seq_range(cu, n, total, ta, tb);
-        gc0 = first_chunk_of(cu, n, total);
+    // this CTA's sequences [sa, sb) and their chunks [gc0, gc0 + nchunks), carried one after another
+    const int sa = bk.per_seq ? bucket : bk.seq[bucket], sb = bk.per_seq ? bucket + 1 : bk.seq[bucket + 1];
+    const int gc0 = bk.per_seq ? (n_seqs > 1 && bucket < n_seqs ? first_chunk_of(cu, bucket, total) : 0)
+                               : bk.chunk[bucket];
+    int nchunks = bk.per_seq ? 0 : bk.chunk[bucket + 1] - gc0;   // per_seq: counted below
+    const bool table_ok = sa >= 0 && sa <= sb && sb <= n_seqs && gc0 >= 0 && nchunks >= 0 && gc0 + nchunks <= nch;
+    {   // the chunks the device's cu_seqlens gives these sequences, counted by all threads (summed below)
+        int cnt = 0;
+        if (table_ok) {
+            if (n_seqs == 1) {
+                if (tid == 0) cnt = (total + C - 1) / C;
+            } else {
+                for (int m = sa + tid; m < sb; m += kWsThreads) {
+                    int a, b;
+                    seq_range(cu, m, total, a, b);
+                    cnt += (b - a + C - 1) / C;
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+        if (lane == 0) warp_chunks[warp] = cnt;
     }
-    const int nchunks = (tb - ta + C - 1) / C;
-    const bool range_ok = gc0 + nchunks <= nch;
-    if (!range_ok && tid == 0) raise_error(err, kErrInternal);
-    const bool started = range_ok && nchunks > 0;
+    auto no_op = [](int) {};
 
     if (warp == 0) {
         tmem_alloc(&tmem_slot, PASS_TMEM_COLS);
@@ -1258,6 +1335,15 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    // the planned chunks must be the ones the device's sequence table gives (a host copy that disagrees with it
+    // would send the loads past the planned range): otherwise record the error and run nothing
+    int dev_chunks = 0;
+#pragma unroll
+    for (int w = 0; w < kWsThreads / 32; ++w) dev_chunks += warp_chunks[w];
+    if (bk.per_seq) nchunks = dev_chunks;
+    const bool range_ok = table_ok && dev_chunks == nchunks && gc0 + nchunks <= nch;
+    if (!range_ok && tid == 0) raise_error(err, kErrInternal);
+    const bool started = range_ok && nchunks > 0;
 
     // Shared-memory descriptors, as in state_pass_norm_kernel.
     const uint64_t dQK0 = smem_desc(base + ST_QK, 16, 1024, kSW);
@@ -1332,11 +1418,14 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             tma_prefetch_desc(&plmap);
             tma_prefetch_desc(&rhmap);
             tma_prefetch_desc(&rlmap);
-            // Q|K, P and R of chunk cc into stage cc & 1
+            // Q|K, P and R of chunk cc into stage cc & 1; the Q|K requests go in chunk order, following the
+            // run's token rows with a cursor
+            ChunkCursor qc;
+            cursor_seek(qc, cu, n_seqs, total, sa, sb, no_op);
             auto load_qk = [&](int cc) {
                 mbar_arrive_expect_tx(&bar_qk[cc & 1], kQkTx);
-                pass_load_qk(sm + (cc & 1) * PASS_STAGE, &bar_qk[cc & 1], &qmap, &kmap, hq, ta + cc * C, hk, total,
-                             err);
+                pass_load_qk(sm + (cc & 1) * PASS_STAGE, &bar_qk[cc & 1], &qmap, &kmap, hq, qc.t0(), hk, total, err);
+                cursor_next(qc, cu, n_seqs, total, sb, no_op);
             };
             auto load_p = [&](int cc) {
                 uint8_t *st = sm + (cc & 1) * PASS_STAGE;
@@ -1399,19 +1488,43 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         const int rowg = row0 + grp * DG;
         const uint32_t tlane = (uint32_t)(32 * quad) << 16;
 
-        // per-chunk inputs are loaded two chunks ahead: under the pass's tile traffic a global load can take
-        // longer than one chunk (one chunk ahead left the K-row threads waiting on them at the top of the loop)
+        // this thread's state elements S[rowg + r][d] of sequence m start at sbase_of(m) + r D
+        auto sbase_of = [&](int m) { return (((size_t)m * hv + h) * D + rowg) * D + d; };
+        auto state_in_range = [&](size_t sbase) {
+            return GDN_INB(sbase + (size_t)(DG - 1) * D, (long)n_seqs * hv * D * D, err);
+        };
+        // a sequence without tokens returns its initial state
+        auto copy_empty = [&](int m) {
+            const size_t sbm = sbase_of(m);
+            if (!final_state || !state_in_range(sbm)) return;
+#pragma unroll
+            for (int r = 0; r < DG; ++r) final_state[sbm + (size_t)r * D] = init_state ? init_state[sbm + (size_t)r * D] : 0.f;
+        };
+        // cur_c: chunk c; pre_c: the chunk whose inputs are loaded next.  Per-chunk inputs are loaded two chunks
+        // ahead: under the pass's tile traffic a global load can take longer than one chunk (one chunk ahead left
+        // the K-row threads waiting on them at the top of the loop).
+        ChunkCursor cur_c;
+        if (!range_ok) cursor_seek(cur_c, cu, n_seqs, total, 0, 0, no_op);   // nothing (the bucket table is invalid)
+        else if (MULTI) cursor_seek(cur_c, cu, n_seqs, total, sa, sb, copy_empty);
+        else cursor_at_seq(cur_c, cu, n_seqs, total, sa);
+        ChunkCursor pre_c = cur_c;
         ChunkInputs nxt, nxt2;
         if (started) {
-            load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0, ta, min(C, tb - ta), hv, h, rowg, lane,
-                              krow, i, total, nch, err);
-            if (nchunks > 1)
-                load_chunk_inputs(nxt2, log_alpha, beta, v, norms, q_scale, gc0 + 1, ta + C, min(C, tb - ta - C), hv,
-                                  h, rowg, lane, krow, i, total, nch, err);
+            load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0, pre_c.t0(), pre_c.len(), hv, h, rowg,
+                              lane, krow, i, total, nch, err);
+            cursor_next(pre_c, cu, n_seqs, total, sb, no_op);
+            if (nchunks > 1) {
+                load_chunk_inputs(nxt2, log_alpha, beta, v, norms, q_scale, gc0 + 1, pre_c.t0(), pre_c.len(), hv, h,
+                                  rowg, lane, krow, i, total, nch, err);
+                cursor_next(pre_c, cu, n_seqs, total, sb, no_op);
+            }
         }
         float S[DG];
-        const size_t sbase = (((size_t)n * hv + h) * D + rowg) * D + d;
-        const bool state_ok = GDN_INB(sbase + (size_t)(DG - 1) * D, (long)n_seqs * hv * D * D, err);
+        size_t sbase = sbase_of(MULTI ? cur_c.n : sa);
+        ChunkCursor next_c = cur_c;   // (MULTI) the first chunk of the next sequence, found a chunk early
+        bool next_ok = false;         // (MULTI) its initial state is read (fetched into L2 a chunk early)
+        // (one sequence per CTA: an empty one returns its initial state through the store after the loop)
+        bool state_ok = (MULTI ? started : range_ok) && state_in_range(sbase);
 #pragma unroll
         for (int r = 0; r < DG; ++r) S[r] = init_state && state_ok ? init_state[sbase + (size_t)r * D] : 0.f;
         auto write_sop = [&]() {
@@ -1443,13 +1556,29 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 break;
             }
             const uint32_t par = c & 1;
-            const int t0 = ta + c * C, L = min(C, tb - t0);
+            const int t0 = cur_c.t0(), L = cur_c.len();
+            const bool seq_end = MULTI && cur_c.last_of_seq();
+            if (MULTI && seq_end) {
+                // the next sequence (sequences without tokens in between return their initial states now) and
+                // its initial state, so that neither lookup waits at the sequence boundary
+                next_c = cur_c;
+                cursor_next(next_c, cu, n_seqs, total, sb, copy_empty);
+                const size_t nsb = sbase_of(next_c.n);
+                next_ok = c + 1 < nchunks && init_state && state_in_range(nsb);
+                if (next_ok) {
+#pragma unroll
+                    for (int r = 0; r < DG; ++r) prefetch_l2(init_state + nsb + (size_t)r * D);
+                }
+            }
             ChunkInputs cur = nxt;
             nxt = nxt2;
             finish_gates<GATE>(cur, L, lane, krow, i, gate_c, gate_b, h);
-            if (c + 2 < nchunks)
-                load_chunk_inputs(nxt2, log_alpha, beta, v, norms, q_scale, gc0 + c + 2, t0 + 2 * C,
-                                  min(C, tb - t0 - 2 * C), hv, h, rowg, lane, krow, i, total, nch, err);
+            if (c + 2 < nchunks) {
+                load_chunk_inputs(nxt2, log_alpha, beta, v, norms, q_scale, gc0 + c + 2, pre_c.t0(), pre_c.len(), hv,
+                                  h, rowg, lane, krow, i, total, nch, err);
+                if (MULTI) cursor_next(pre_c, cu, n_seqs, total, sb, no_op);
+                else ++pre_c.k;
+            }
             const float2 g2 = cumsum_pairs(cur.la0, cur.la1, L, lane);
             const float gL = g_of(g2, L - 1);
             const float eg = __expf(g_of(g2, i));
@@ -1511,9 +1640,25 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 #pragma unroll
                 for (int e = 0; e < DG; ++e) S[e] = fmaf(eL, S[e], a[e] + b[e]);
             }
+            if (MULTI && seq_end) {   // the sequence's final state; the next one starts from its initial state
+                if (final_state && state_ok) {
+#pragma unroll
+                    for (int r = 0; r < DG; ++r) final_state[sbase + (size_t)r * D] = S[r];
+                }
+                const size_t nsb = sbase_of(next_c.n);
+#pragma unroll
+                for (int r = 0; r < DG; ++r) S[r] = next_ok ? init_state[nsb + (size_t)r * D] : 0.f;
+            }
             publish_sop();
             prev_t0 = t0;
             prev_L = L;
+            if (MULTI && seq_end) {
+                cur_c = next_c;
+                sbase = sbase_of(cur_c.n);
+                state_ok = cur_c.n < sb && state_in_range(sbase);
+            } else {
+                ++cur_c.k;
+            }
         }
         if (!ok && range_ok) fail();
         if (ok) {
@@ -1525,7 +1670,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 outputs_begin<false>(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, done, nullptr);
                 outputs_end<false>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, done, nullptr, nullptr, 0.f, (long)total * hv * D, err);
             }
-            if (final_state && state_ok) {
+            if (!MULTI && final_state && state_ok) {
 #pragma unroll
                 for (int r = 0; r < DG; ++r) final_state[sbase + (size_t)r * D] = S[r];
             }
@@ -1567,6 +1712,90 @@ bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uin
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Multiprocessors of device dev (cached per device; 1 if the query fails).
+int multiprocessors(int dev) {
+    static std::atomic<int> cached[kMaxDevices];
+    const bool in_table = dev >= 0 && dev < kMaxDevices;
+    if (in_table) {
+        const int n = cached[dev].load(std::memory_order_relaxed);
+        if (n > 0) return n;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    if (in_table) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+// Buckets of the plain state pass.  Its CTAs take one SM each, hv * 4 of them per bucket.  One bucket per
+// sequence runs short sequences in waves of CTAs that each pay the pass's fixed cost (about two chunk times)
+// for one or two chunks: 1024 CTAs for eight sequences at 32 value heads.  A CTA carrying several sequences'
+// chunks one after another keeps the tile pipeline full across their boundaries, at ~1.1x per chunk (the
+// kernel with sequence boundaries in its loop, measured at 4K).  The candidates are: as many buckets of
+// consecutive sequences (with about equal chunks) as run in one wave, or one bucket per sequence, whose CTAs
+// run in waves (estimated as max(the longest sequence, all work spread over the SMs, the waves times the
+// shortest)).  Measured with eight sequences at 32 value heads, one bucket is faster up to 128 tokens per
+// sequence, even at 256 and slower from 512.
+int pass_buckets(PassBuckets &bk, int n_seqs, const int32_t *cu_host, long nch, int hv, int sms) {
+    constexpr double kCtaCost = 2.0, kMultiCost = 1.1;
+    const long per_bucket = (long)hv * (D / DS);
+    std::vector<long> first(n_seqs + 1, 0);   // first chunk of each sequence
+    for (int n = 0; n < n_seqs; ++n) first[n + 1] = first[n] + (cu_host[n + 1] - cu_host[n] + C - 1) / C;
+    // sequence starts of nb buckets: bucket b opens at the first sequence whose first chunk reaches b / nb of
+    // the total (strictly after the previous bucket's first sequence); returns the buckets made
+    auto split = [&](int nb, int *seq) {
+        seq[0] = 0;
+        if (nb == n_seqs) {   // one sequence per bucket
+            for (int b = 1; b <= nb; ++b) seq[b] = b;
+            return nb;
+        }
+        int made = 1;
+        for (int b = 1; b < nb; ++b) {
+            const long target = (b * nch + nb - 1) / nb;
+            int n = (int)(std::lower_bound(first.begin(), first.end() - 1, target) - first.begin());
+            n = std::max(n, seq[made - 1] + 1);
+            if (n >= n_seqs) break;
+            seq[made++] = n;
+        }
+        seq[made] = n_seqs;
+        return made;
+    };
+    int seq[kMaxPassBuckets + 1];
+    // one wave of buckets carrying several sequences each
+    const int one_wave = (int)std::max(1L, std::min<long>(sms / per_bucket, kMaxPassBuckets));
+    int best_nb = 1;
+    double best_cost = -1.0;
+    for (int nb = 1; nb <= std::min(n_seqs, one_wave); ++nb) {
+        const int made = split(nb, seq);
+        double longest = 0.0;
+        for (int b = 0; b < made; ++b)
+            longest = std::max(longest, (double)(first[seq[b + 1]] - first[seq[b]]) * (made < n_seqs ? kMultiCost : 1.0));
+        if (best_cost < 0.0 || longest + kCtaCost < best_cost) {
+            best_cost = longest + kCtaCost;
+            best_nb = nb;
+        }
+    }
+    // one bucket per sequence
+    bk.per_seq = 0;
+    if (n_seqs > one_wave) {
+        double longest = 0.0, shortest = 0.0, work = 0.0;
+        for (int n = 0; n < n_seqs; ++n) {
+            const double t = (double)(first[n + 1] - first[n]) + kCtaCost;
+            longest = std::max(longest, t);
+            shortest = n == 0 ? t : std::min(shortest, t);
+            work += t;
+        }
+        const double waves = (double)((n_seqs * per_bucket + sms - 1) / sms);
+        const double cost = std::max({longest, work * (double)per_bucket / (double)sms, waves * shortest});
+        if (cost < best_cost) {
+            bk.per_seq = 1;
+            return n_seqs;
+        }
+    }
+    const int made = split(best_nb, bk.seq);
+    for (int b = 0; b <= made; ++b) bk.chunk[b] = (int)first[bk.seq[b]];
+    return made;
+}
+
 long total_chunks(int n_seqs, const int32_t *cu_host) {
     long nch = 0;
     for (int n = 0; n < n_seqs; ++n) nch += (cu_host[n + 1] - cu_host[n] + C - 1) / C;
@@ -1601,7 +1830,8 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
     if (!cached || !attrs_set[dev].load(std::memory_order_acquire)) {
         const void *prep[] = {(const void *)chunk_prep_kernel<false, false>, (const void *)chunk_prep_kernel<true, false>,
                               (const void *)chunk_prep_kernel<false, true>, (const void *)chunk_prep_kernel<true, true>};
-        const void *pass[] = {(const void *)state_pass_kernel<false>, (const void *)state_pass_kernel<true>,
+        const void *pass[] = {(const void *)state_pass_kernel<false, false>, (const void *)state_pass_kernel<true, false>,
+                              (const void *)state_pass_kernel<false, true>, (const void *)state_pass_kernel<true, true>,
                               (const void *)state_pass_norm_kernel<false>, (const void *)state_pass_norm_kernel<true>};
         for (const void *f : prep)
             if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
@@ -1653,11 +1883,15 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
                                    p.init_state, p.cu_seqlens, p.n_seqs, p.total_tokens, (int)nch, p.hk, p.hv, p.out,
                                    p.out_f32, p.final_state, p.norm_w, p.norm_eps, p.gate_c, p.gate_b, p.err);
         } else {
-            auto pass = gate ? state_pass_kernel<true> : state_pass_kernel<false>;
-            pass<<<grid2, kWsThreads, PASS_SMEM, p.stream>>>(
+            PassBuckets bk;
+            const int nb = pass_buckets(bk, p.n_seqs, p.cu_seqlens_host, nch, p.hv, multiprocessors(dev));
+            const bool multi = nb < p.n_seqs;   // some bucket carries more than one sequence
+            auto pass = multi ? (gate ? state_pass_kernel<true, true> : state_pass_kernel<false, true>)
+                              : (gate ? state_pass_kernel<true, false> : state_pass_kernel<false, false>);
+            pass<<<(unsigned)(nb * p.hv * (D / DS)), kWsThreads, PASS_SMEM, p.stream>>>(
                 qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm, p.q_scale, p.log_alpha, p.beta, p.init_state,
                 p.cu_seqlens, p.n_seqs, p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state,
-                p.gate_c, p.gate_b, p.err);
+                p.gate_c, p.gate_b, p.err, bk);
             e = cudaSuccess;
         }
         if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;

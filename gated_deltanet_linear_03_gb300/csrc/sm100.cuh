@@ -80,6 +80,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return mbar_wait_for(bar, parity, kWaitTimeoutNs);
 }
 
+// Bring a global line into L2 ahead of its use (no register is written).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------------------ clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

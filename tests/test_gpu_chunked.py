@@ -1,7 +1,8 @@
 """GPU parity of the chunked (tcgen05) prefill against the fp64 oracle, through the C ABI.
 
 Cases span several chunks and ragged tails (lengths that are not multiples of
-64, empty sequences, one-token sequences), both head groupings the kernels
+64, empty sequences, one-token sequences), sequence buckets (one state-pass CTA
+carrying several sequences one after another), both head groupings the kernels
 specialise on, slow-decay gates that make the carried state matter, and the
 full model-shaped workloads (4K exhaustively; 128K and the ragged 8-sequence
 batch on sampled heads, where the oracle checks every token of those heads).
@@ -43,6 +44,10 @@ CASES = {
     "group1": lambda: synth.prefill_inputs([150, 90], hk=4, hv=4, seed=35, init_std=0.05),
     "group4": lambda: synth.prefill_inputs([129, 64], hk=2, hv=8, seed=36, init_std=0.05),
     "group3_odd": lambda: synth.prefill_inputs([77], hk=1, hv=3, seed=37, init_std=0.05),
+    # 8 value heads: the state pass runs 4 buckets of consecutive sequences, each CTA carrying the state
+    # through several sequences (empty ones first, in the middle and last), with slow decay and initial states
+    "buckets_many_seqs": lambda: synth.prefill_inputs([0, 1, 63, 64, 65, 0, 130, 7, 200, 0, 2, 64, 0], hk=2, hv=8,
+                                                      seed=38, gates="slow", init_std=0.05),
 }
 
 

@@ -68,6 +68,7 @@ CASES = {
     "group4": lambda: synth.prefill_inputs([129, 64], hk=2, hv=8, seed=92, init_std=0.05),
     "group3_gates": lambda: synth.prefill_inputs([77, 1], hk=1, hv=3, seed=93, raw_gates="per_head"),
     "short_many": lambda: synth.prefill_inputs([32, 5, 17, 1, 32, 9, 30, 2], seed=94, init_std=0.02),
+    "buckets": lambda: synth.prefill_inputs([0, 65, 1, 0, 130, 64, 3, 0], seed=99, init_std=0.02),   # one state-pass CTA carries all eight
 }
 
 
