@@ -394,6 +394,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     const int t0 = loc.t0, L = loc.len;
     const uint32_t base = smem_u32(sm);
     const uint32_t tlane = (uint32_t)(32 * quad) << 16;
+    // the state pass may start its prologue (and its first chunk's products, which need no workspace) on SMs
+    // this grid has left; it waits for this grid before reading the workspace
+    if (tid == 0) grid_launch_dependents();
 
     if (warp == 0) {
         tmem_alloc(&tmem_slot, PREP_TMEM_COLS);
@@ -1443,10 +1446,12 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 tma_load_2d(st + ST_RH, &rhmap, &bar_r[cc & 1], 0, rrow);
                 tma_load_2d(st + ST_RL, &rlmap, &bar_r[cc & 1], 0, rrow);
             };
-            // both stages start empty
+            // both stages start empty; Q|K come from the inputs, P and R from the preparation, which may still
+            // be finishing (programmatic dependent launch)
             int nq = min(2, nchunks), np = nq, nr = nq;   // chunks < nq (np, nr) have had Q|K (P, R) requested
+            for (int cc = 0; cc < nq; ++cc) load_qk(cc);
+            grid_dependency_wait();
             for (int cc = 0; cc < nq; ++cc) {
-                load_qk(cc);
                 load_p(cc);
                 load_r(cc);
             }
@@ -1500,6 +1505,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 #pragma unroll
             for (int r = 0; r < DG; ++r) final_state[sbm + (size_t)r * D] = init_state ? init_state[sbm + (size_t)r * D] : 0.f;
         };
+        if (norms) grid_dependency_wait();   // the q/k preparation factors come from the preparation
         // cur_c: chunk c; pre_c: the chunk whose inputs are loaded next.  Per-chunk inputs are loaded two chunks
         // ahead: under the pass's tile traffic a global load can take longer than one chunk (one chunk ahead left
         // the K-row threads waiting on them at the top of the loop).
@@ -1888,11 +1894,24 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
             const bool multi = nb < p.n_seqs;   // some bucket carries more than one sequence
             auto pass = multi ? (gate ? state_pass_kernel<true, true> : state_pass_kernel<false, true>)
                               : (gate ? state_pass_kernel<true, false> : state_pass_kernel<false, false>);
-            pass<<<(unsigned)(nb * p.hv * (D / DS)), kWsThreads, PASS_SMEM, p.stream>>>(
-                qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm, p.q_scale, p.log_alpha, p.beta, p.init_state,
-                p.cu_seqlens, p.n_seqs, p.total_tokens, (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state,
-                p.gate_c, p.gate_b, p.err, bk);
-            e = cudaSuccess;
+            // Right after this call's preparation the pass is its programmatic dependent: its CTAs may start on
+            // SMs the preparation has left, run their prologue and first products (which read only the
+            // inputs, complete since before the preparation started), and wait for the preparation before
+            // reading the workspace.  Launched alone it follows the stream as usual.
+            cudaLaunchAttribute pdl[1];
+            pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            pdl[0].val.programmaticStreamSerializationAllowed = 1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(nb * p.hv * (D / DS)));
+            cfg.blockDim = dim3(kWsThreads);
+            cfg.dynamicSmemBytes = PASS_SMEM;
+            cfg.stream = p.stream;
+            cfg.attrs = pdl;
+            cfg.numAttrs = (phases & 1) && nch > 0 ? 1 : 0;
+            e = cudaLaunchKernelEx(&cfg, pass, qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm, p.q_scale,
+                                   p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.n_seqs, p.total_tokens,
+                                   (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state, p.gate_c, p.gate_b,
+                                   p.err, bk);
         }
         if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     }

@@ -80,6 +80,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return mbar_wait_for(bar, parity, kWaitTimeoutNs);
 }
 
+// Programmatic dependent launch: a kernel launched after this one with programmatic stream serialization may
+// start once every CTA of this one has signalled (or exited); it must wait before reading this one's results.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the preceding kernel (if it was launched as a programmatic dependency's primary) has completed and
+// its memory is visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Bring a global line into L2 ahead of its use (no register is written).
 __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

@@ -178,6 +178,20 @@ def test_full_size_sampled_heads(gdn, full_size, which, algo):
                   what=f"{which} {algo}")
 
 
+@pytest.mark.parametrize("lengths", [
+    [600] * 70,                           # 70 sequences of 10 chunks: one state-pass CTA per sequence (beyond the
+                                          # 64-entry bucket table: the first chunks come from cu_seqlens)
+    [40, 0, 1, 64, 65, 0, 129] * 10,      # 70 short ones: one CTA carries them all, empty ones included
+])
+def test_many_sequences_bucket_layouts(gdn, lengths):
+    heads = [0, 13, 31]
+    inp = synth.prefill_inputs(lengths, seed=1301 + len(set(lengths)), init_std=0.02)
+    ref_out, ref_fin = oracle.prefill(*sampled_heads(inp, heads))
+    out, fin = run(gdn, inp, "chunked", torch.float32)
+    check_prefill(out[:, heads].contiguous(), fin[:, heads].contiguous(), ref_out, ref_fin,
+                  what=f"{len(lengths)} sequences")
+
+
 def test_long_128k_then_decode(gdn, full_size):
     """The long-context case end to end: the 128K-token prefill emits its final state, and 64 batch-1
     decode steps continue from it in place.  Sampled heads follow the oracle's own continuation from the
