@@ -377,8 +377,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     __shared__ uint64_t bar_tma, bar_mma;
     __shared__ uint32_t tmem_slot;
 
-    const int gc = blockIdx.x;
-    const int h = blockIdx.y;
+    // chunk-major, last chunk first: the state pass reads the first chunks first, so they are the ones written
+    // last, the most likely to be still in L2 when it starts
+    const int nch = (int)(gridDim.x / hv);
+    const int h = (int)(blockIdx.x % hv);
+    const int gc = nch - 1 - (int)(blockIdx.x / hv);
     const int hq = h / (hv / hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;   // TMEM lane quadrant; which column half the warp takes
@@ -486,7 +489,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             f *= qk_inv_norm(ss, 1);
         }
         (isq ? qf_s : kf_s)[r] = f;
-        if (ok && qk_norm && GDN_INB(((size_t)gc * hv + h) * 128 + tid, (long)gridDim.x * hv * 128, err))
+        if (ok && qk_norm && GDN_INB(((size_t)gc * hv + h) * 128 + tid, (long)nch * hv * 128, err))
             norms[((size_t)gc * hv + h) * 128 + tid] = f;   // read by the pass only with qk_norm
     }
     if (warp == 1) {
@@ -701,7 +704,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     __syncthreads();
     if (ok && tid == 0) {
         const int prow = (gc * hv + h) * D;
-        if (GDN_INB((long)prow + D - 1, (long)gridDim.x * hv * D, err)) {
+        if (GDN_INB((long)prow + D - 1, (long)nch * hv * D, err)) {
             tma_store_2d(&phmap, sm + PREP_KQ, 0, prow);
             tma_store_2d(&plmap, sm + PREP_KQ + 16384, 0, prow);
         }
@@ -727,7 +730,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     __syncthreads();
     if (ok && tid == 0) {
         const int rrow = (gc * hv + h) * C;
-        if (GDN_INB((long)rrow + C - 1, (long)gridDim.x * hv * C, err)) {
+        if (GDN_INB((long)rrow + C - 1, (long)nch * hv * C, err)) {
             tma_store_2d(&rhmap, sm + PREP_A, 0, rrow);
             tma_store_2d(&rlmap, sm + PREP_A + 8192, 0, rrow);
         }
@@ -1859,7 +1862,7 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
 
     const bool prep_qk = p.qk_norm || p.q_scale != 1.f, gate = p.gate_c != nullptr;
     if ((phases & 1) && nch > 0) {
-        dim3 grid((unsigned)nch, (unsigned)p.hv);
+        dim3 grid((unsigned)(nch * p.hv));
         auto prep = prep_qk ? (gate ? chunk_prep_kernel<true, true> : chunk_prep_kernel<true, false>)
                             : (gate ? chunk_prep_kernel<false, true> : chunk_prep_kernel<false, false>);
         prep<<<grid, kPrepThreads, PREP_SMEM, p.stream>>>(qmap, kmap, phmap, plmap, rhmap, rlmap, p.log_alpha,
