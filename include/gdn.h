@@ -107,9 +107,13 @@ typedef enum {
  *   cu_seqlens       int32 [n_seqs + 1] on the device: sequence n is tokens
  *                    [cu_seqlens[n], cu_seqlens[n+1])
  *   cu_seqlens_host  the same n_seqs + 1 values in host memory; used to plan the
- *                    launch without a device synchronisation.  It must start at
- *                    0, be non-decreasing and end at total_tokens.  The kernels
- *                    also clamp the device copy to [0, total_tokens].
+ *                    launch without a device synchronisation (the workspace, the
+ *                    grids, and which sequences one state-pass CTA carries one
+ *                    after another).  It must start at 0, be non-decreasing and
+ *                    end at total_tokens.  The kernels also clamp the device
+ *                    copy to [0, total_tokens]; where the device copy gives a
+ *                    state-pass CTA other chunks than the host copy planned, that
+ *                    CTA records GDN_ERR_INTERNAL and runs nothing.
  *   out              [T, hv, dv], dtype out_dtype (GDN_DTYPE_BF16 or _F32)
  *   final_state      fp32 [n_seqs, hv, dv, dk] or NULL.  It may be the same
  *                    buffer as init_state (updated in place); any other overlap
