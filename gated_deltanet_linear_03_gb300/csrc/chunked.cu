@@ -213,8 +213,8 @@ constexpr uint32_t PREP_KQ = 0;        // kb0: K rows | Q rows, kb1: K rows | Q 
 constexpr uint32_t PREP_A = 32768;     // fp32 A [64][68]; later (Gamma T)^T hi / lo, then R hi / lo
 constexpr int A_LD = 68;
 constexpr uint32_t PREP_AQK = PREP_A + 64 * A_LD * 4;   // 50176: Aqk hi, Aqk lo tiles [64 x 64] bf16
-constexpr uint32_t PREP_Y = PREP_AQK + 16384;           // fp32 scratch [3][16][16]
-constexpr uint32_t PREP_G = PREP_Y + 3 * 256 * 4;       // g [64], beta [64], Gamma = e^{g_L - g} [64],
+constexpr uint32_t PREP_Y = PREP_AQK + 16384;           // fp32 scratch [4][16][16]
+constexpr uint32_t PREP_G = PREP_Y + 4 * 256 * 4;       // g [64], beta [64], Gamma = e^{g_L - g} [64],
                                                         // the q/k preparation factors f_k [64], f_q [64],
                                                         // then alpha = e^{log_alpha} [64]
 constexpr uint32_t PREP_SMEM = PREP_G + 1536 + 1024;    // + alignment slack: 3 CTAs per SM
@@ -232,9 +232,10 @@ constexpr int kPrepThreads = 256;   // 8 warps: warps w and w + 4 share TMEM lan
 //                                              first takes rows 0-7 of its block, the second rows 8-15
 //                                              once those are in shared memory (rows of A read as 16-byte
 //                                              words)
-//   below them       T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ   level by level in I; threads 0-127 take the
-//                                              blocks of even J, threads 128-255 those of odd J (the sums of
-//                                              the last level are balanced differently)
+//   below them       by recursive doubling on block pairs: T_10 and T_32 together, then the lower-left
+//                                              32 x 32 block from the two 32 x 32 diagonal halves (four
+//                                              barriers; level by level in the block row it took six, and
+//                                              the preparation 60.6 against 57.8 us at the 4K layer)
 // In the block products each thread owns a strip of two adjacent columns of one row: four consecutive
 // elements of the left factor come in one 16-byte load (the same address for the lanes of a row) and each
 // row of the right factor in one 8-byte load, so a pair of FMAs costs about one shared-memory load.
@@ -298,65 +299,88 @@ __device__ __forceinline__ void solve_unit_lower_blocked(const float *__restrict
         }
     }
     __syncthreads();
+    // Below the diagonal blocks, by recursive doubling on block pairs (16 block products, four barriers):
+    //   level 1  T_10 = -T_11 (A_10 T_00)  and  T_32 = -T_33 (A_32 T_22)
+    //   level 2  the lower-left 32 x 32 block  T_lh = -T_h (A_hl T_l),  T_l = [T_00 0; T_10 T_11], T_h = [T_22 0; T_32 T_33]
+    // Threads 0-127 and 128-255 (par) take balanced halves of each step; in a block product each thread owns a
+    // strip of two adjacent columns of one row (the same loads as the level-by-level form).
     const int par = tid >> 7, r = (tid >> 3) & 15, c = (tid & 7) * 2;
+    // y += (row r of the 16-block of `left` at rows 16 I, columns 16 K) x (16-block of T at rows 16 K, columns 16 J)
+    auto acc_AT = [&](int I, int K, int J, float &y0, float &y1) {
+        const float *arow = A + (16 * I + r) * A_LD + 16 * K;
+        const float *tb = t_row(sm, 16 * K) + 16 * J + c;
+        float z0 = 0.f, z1 = 0.f;
 #pragma unroll
-    for (int I = 1; I < 4; ++I) {
-        // Y_J = sum_{K=J}^{I-1} A_IK T_KJ for J < I (I - J block products); at I = 3 the second half takes
-        // J = 1 and 2 (three products against three for J = 0)
-#pragma unroll
-        for (int J = 0; J < I; ++J) {
-            const int owner = I == 3 ? (J > 0) : (J & 1);
-            if (owner != par) continue;   // warp-uniform
-            const float *arow = A + (16 * I + r) * A_LD;
-            float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
-#pragma unroll
-            for (int K = J; K < I; ++K) {
-                const float *tb = t_row(sm, 16 * K) + 16 * J + c;   // the 16 rows of block K are contiguous
-#pragma unroll
-                for (int k4 = 0; k4 < 16; k4 += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(arow + 16 * K + k4);
-                    const float2 t0 = *reinterpret_cast<const float2 *>(tb + (k4 + 0) * 64);
-                    const float2 t1 = *reinterpret_cast<const float2 *>(tb + (k4 + 1) * 64);
-                    const float2 t2 = *reinterpret_cast<const float2 *>(tb + (k4 + 2) * 64);
-                    const float2 t3 = *reinterpret_cast<const float2 *>(tb + (k4 + 3) * 64);
-                    y0 = fmaf(a4.x, t0.x, y0);
-                    y1 = fmaf(a4.x, t0.y, y1);
-                    z0 = fmaf(a4.y, t1.x, z0);
-                    z1 = fmaf(a4.y, t1.y, z1);
-                    y0 = fmaf(a4.z, t2.x, y0);
-                    y1 = fmaf(a4.z, t2.y, y1);
-                    z0 = fmaf(a4.w, t3.x, z0);
-                    z1 = fmaf(a4.w, t3.y, z1);
-                }
-            }
-            *reinterpret_cast<float2 *>(Y + J * 256 + r * 16 + c) = make_float2(y0 + z0, y1 + z1);
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(arow + k4);
+            const float2 t0 = *reinterpret_cast<const float2 *>(tb + (k4 + 0) * 64);
+            const float2 t1 = *reinterpret_cast<const float2 *>(tb + (k4 + 1) * 64);
+            const float2 t2 = *reinterpret_cast<const float2 *>(tb + (k4 + 2) * 64);
+            const float2 t3 = *reinterpret_cast<const float2 *>(tb + (k4 + 3) * 64);
+            y0 = fmaf(a4.x, t0.x, y0);
+            y1 = fmaf(a4.x, t0.y, y1);
+            z0 = fmaf(a4.y, t1.x, z0);
+            z1 = fmaf(a4.y, t1.y, z1);
+            y0 = fmaf(a4.z, t2.x, y0);
+            y1 = fmaf(a4.z, t2.y, y1);
+            z0 = fmaf(a4.w, t3.x, z0);
+            z1 = fmaf(a4.w, t3.y, z1);
         }
+        y0 += z0;
+        y1 += z1;
+    };
+    // y += (row r of the 16-block of T at rows 16 I, columns 16 K) x (Y block yb)
+    auto acc_TY = [&](int I, int K, const float *yb, float &y0, float &y1) {
+        const float *trow = t_row(sm, 16 * I + r) + 16 * K;
+        float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(trow + k4);
+            const float2 t0 = *reinterpret_cast<const float2 *>(yb + (k4 + 0) * 16 + c);
+            const float2 t1 = *reinterpret_cast<const float2 *>(yb + (k4 + 1) * 16 + c);
+            const float2 t2 = *reinterpret_cast<const float2 *>(yb + (k4 + 2) * 16 + c);
+            const float2 t3 = *reinterpret_cast<const float2 *>(yb + (k4 + 3) * 16 + c);
+            y0 = fmaf(a4.x, t0.x, y0);
+            y1 = fmaf(a4.x, t0.y, y1);
+            z0 = fmaf(a4.y, t1.x, z0);
+            z1 = fmaf(a4.y, t1.y, z1);
+            y0 = fmaf(a4.z, t2.x, y0);
+            y1 = fmaf(a4.z, t2.y, y1);
+            z0 = fmaf(a4.w, t3.x, z0);
+            z1 = fmaf(a4.w, t3.y, z1);
+        }
+        y0 += z0;
+        y1 += z1;
+    };
+    auto put = [&](float *dst, float y0, float y1) { *reinterpret_cast<float2 *>(dst) = make_float2(y0, y1); };
+    {   // level 1: par 0 the pair (0, 1), par 1 the pair (2, 3)
+        const int lo = 2 * par;
+        float y0 = 0.f, y1 = 0.f;
+        acc_AT(lo + 1, lo, lo, y0, y1);                      // Y = A_{lo+1,lo} T_{lo,lo}
+        put(Y + par * 256 + r * 16 + c, y0, y1);
         __syncthreads();
-        // T_IJ = -T_II Y_J
-#pragma unroll
-        for (int J = 0; J < I; ++J) {
-            if ((J & 1) != par) continue;
-            float *trow = t_row(sm, 16 * I + r);
-            const float *yb = Y + J * 256 + c;
-            float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
-#pragma unroll
-            for (int k4 = 0; k4 < 16; k4 += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(trow + 16 * I + k4);
-                const float2 t0 = *reinterpret_cast<const float2 *>(yb + (k4 + 0) * 16);
-                const float2 t1 = *reinterpret_cast<const float2 *>(yb + (k4 + 1) * 16);
-                const float2 t2 = *reinterpret_cast<const float2 *>(yb + (k4 + 2) * 16);
-                const float2 t3 = *reinterpret_cast<const float2 *>(yb + (k4 + 3) * 16);
-                y0 = fmaf(a4.x, t0.x, y0);
-                y1 = fmaf(a4.x, t0.y, y1);
-                z0 = fmaf(a4.y, t1.x, z0);
-                z1 = fmaf(a4.y, t1.y, z1);
-                y0 = fmaf(a4.z, t2.x, y0);
-                y1 = fmaf(a4.z, t2.y, y1);
-                z0 = fmaf(a4.w, t3.x, z0);
-                z1 = fmaf(a4.w, t3.y, z1);
-            }
-            *reinterpret_cast<float2 *>(trow + 16 * J + c) = make_float2(-(y0 + z0), -(y1 + z1));
-        }
+        float t0 = 0.f, t1 = 0.f;
+        acc_TY(lo + 1, lo + 1, Y + par * 256, t0, t1);       // T_{lo+1,lo} = -T_{lo+1,lo+1} Y
+        put(t_row(sm, 16 * (lo + 1) + r) + 16 * lo + c, -t0, -t1);
+        __syncthreads();
+    }
+    {   // level 2: Y_ab = sum_k A_ak (T_l)_kb for a in {2, 3}, b in {0, 1}; par 0 rows a = 2, par 1 a = 3
+        const int a = 2 + par;
+        float y0 = 0.f, y1 = 0.f, w0 = 0.f, w1 = 0.f;
+        acc_AT(a, 0, 0, y0, y1);                             // Y_a0 = A_a0 T_00 + A_a1 T_10
+        acc_AT(a, 1, 0, y0, y1);
+        acc_AT(a, 1, 1, w0, w1);                             // Y_a1 = A_a1 T_11
+        put(Y + (2 * par) * 256 + r * 16 + c, y0, y1);
+        put(Y + (2 * par + 1) * 256 + r * 16 + c, w0, w1);
+        __syncthreads();
+        // T_2b = -T_22 Y_2b, T_3b = -(T_32 Y_2b + T_33 Y_3b); par 0 columns b = 0, par 1 b = 1
+        const int b = par;
+        float u0 = 0.f, u1 = 0.f, v0 = 0.f, v1 = 0.f;
+        acc_TY(2, 2, Y + (0 + b) * 256, u0, u1);
+        acc_TY(3, 2, Y + (0 + b) * 256, v0, v1);
+        acc_TY(3, 3, Y + (2 + b) * 256, v0, v1);
+        put(t_row(sm, 32 + r) + 16 * b + c, -u0, -u1);
+        put(t_row(sm, 48 + r) + 16 * b + c, -v0, -v1);
         __syncthreads();
     }
 }
