@@ -773,10 +773,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 // Kernel 2a: state passing + outputs with the fused output normalisation
 // (sequential over chunks; the four row slices of a head form a cluster)
 // ============================================================================
-// One pipeline stage: Q|K 32 KiB, P_hi 16, P_lo 16, R_hi 16, R_lo 16 KiB (each R tile holds 64 rows
-// loaded per chunk and 64 zero rows, so that R feeds an M = 128 MMA whose upper rows are unused).
-constexpr uint32_t PASS_STAGE = 98304;
-constexpr uint32_t ST_QK = 0, ST_PH = 32768, ST_PL = 49152, ST_RH = 65536, ST_RL = 81920;
+// One pipeline stage: Q|K 32 KiB, P_hi 16, P_lo 16, R_hi 8, R_lo 8 KiB.  R feeds M = 128 MMAs whose upper 64
+// accumulator rows are unused: the group on R_hi reads R_lo as its upper rows, the accumulating group on R_lo
+// reads whatever follows it (the next stage's Q|K, or the state operand), so the valid rows hold
+// (R_hi + R_lo) X and the upper ones anything (never read).
+constexpr uint32_t PASS_STAGE = 81920;
+constexpr uint32_t ST_QK = 0, ST_PH = 32768, ST_PL = 49152, ST_RH = 65536, ST_RL = 73728;
 constexpr uint32_t PASS_SOP = 2 * PASS_STAGE;      // [S_hi ; S_lo] tile, 2 k-blocks x 8 KiB
 constexpr uint32_t PASS_XOP = PASS_SOP + 16384;    // [X_hi ; X_lo] tile(s) [64 x 64] bf16 (state_pass_kernel: by chunk parity)
 constexpr uint32_t PASS_SMEM = PASS_XOP + 2 * 8192 + 1024;
@@ -1002,11 +1004,6 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         mbar_init(&bar_rx[1], 1);
         fence_mbar_init();
     }
-    // zero the padding rows of the R tiles once (rows 64..127 feed only unused accumulator rows)
-    for (int x = tid; x < 4 * 512; x += kPassThreads) {
-        const int st = x / 1024, t = (x / 512) & 1, o = x % 512;
-        reinterpret_cast<uint4 *>(sm + st * PASS_STAGE + (t ? ST_RL : ST_RH) + 8192)[o] = make_uint4(0, 0, 0, 0);
-    }
     __syncthreads();
     if (tid == 32 && started) {
         tma_prefetch_desc(&qmap);
@@ -1157,7 +1154,7 @@ state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         } else if (tid == kRxIssuer) {
             const uint32_t rx = tmem + TM_RX + 64 * par;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)   // R X (64 (+64 pad) x 64) = R_hi [X_hi ; X_lo]^T
+            for (int kk = 0; kk < 4; ++kk)   // R X (64 valid rows x 64) = R_hi [X_hi ; X_lo]^T
                 mma_bf16(rx, dRH0 + so + 2 * kk, dXOP + 128 * kk, idb, kk > 0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)   //   + R_lo [X_hi ; X_lo]^T
@@ -1355,12 +1352,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         abort_flag = 0;
         fence_mbar_init();
     }
-    // zero the padding rows of the R tiles once (rows 64..127 feed only unused accumulator rows)
-    for (int x = tid; x < 4 * 512; x += kWsThreads) {
-        const int st = x / 1024, t = (x / 512) & 1, o = x % 512;
-        reinterpret_cast<uint4 *>(sm + st * PASS_STAGE + (t ? ST_RL : ST_RH) + 8192)[o] = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();   // the zeros are read by the tensor cores
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1391,7 +1382,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 
     if (warp == kMmaWarp) {
         if (lane == 0 && started) {
-            // R X of chunk cc (64 (+64 pad) x 64) = (R_hi + R_lo) [X_hi ; X_lo]^T into TMEM buffer cc & 1
+            // R X of chunk cc (64 valid rows x 64) = (R_hi + R_lo) [X_hi ; X_lo]^T into TMEM buffer cc & 1
             auto issue_rx = [&](int cc) -> bool {
                 const int sc = cc & 1;
                 if (!mbar_wait(&bar_r[sc], ph(cc))) return false;
