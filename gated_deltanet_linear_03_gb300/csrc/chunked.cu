@@ -18,8 +18,9 @@
 //        = e^{g_L} S0 + (P X)^T,                    P = K^T diag(e^{g_L-g}) T
 // A, T, R and P depend only on k, q and the gates, so they are computed for
 // every chunk in parallel by `chunk_prep_kernel`; only the X -> state step is
-// sequential over chunks, in `state_pass_kernel` (or `state_pass_norm_kernel`
-// when the output normalisation is fused).
+// sequential over chunks, in `state_pass_kernel` (which, when the output
+// normalisation is fused, runs as clusters of the four slice CTAs of a head
+// that exchange the per-token sums of squares).
 //
 // Tensor-core use (tcgen05.mma, bf16 operands, fp32 accumulation in TMEM,
 // operands staged by TMA in 128B-swizzled shared memory):
@@ -770,8 +771,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 }
 
 // ============================================================================
-// Kernel 2a: state passing + outputs with the fused output normalisation
-// (sequential over chunks; the four row slices of a head form a cluster)
+// Kernel 2: state passing + outputs (sequential over chunks)
 // ============================================================================
 // One pipeline stage: Q|K 32 KiB, P_hi 16, P_lo 16, R_hi 8, R_lo 8 KiB.  R feeds M = 128 MMAs whose upper 64
 // accumulator rows are unused: the group on R_hi reads R_lo as its upper rows, the accumulating group on R_lo
@@ -783,7 +783,6 @@ constexpr uint32_t PASS_SOP = 2 * PASS_STAGE;      // [S_hi ; S_lo] tile, 2 k-bl
 constexpr uint32_t PASS_XOP = PASS_SOP + 16384;    // [X_hi ; X_lo] tile(s) [64 x 64] bf16 (state_pass_kernel: by chunk parity)
 constexpr uint32_t PASS_SMEM = PASS_XOP + 2 * 8192 + 1024;
 constexpr uint32_t kQkTx = 32768;                                   // Q|K of a stage
-constexpr uint32_t kStageTx = kQkTx + 16384 + 16384 + 8192 + 8192;   // all tiles of a stage
 constexpr uint32_t PASS_TMEM_COLS = 256;
 // TMEM columns (each accumulator 64 columns: 32 for the S_hi / X_hi part, 32 for the S_lo / X_lo part):
 //   [Q;K] [S_hi;S_lo]^T  (M = 128 token rows: Q rows in lanes 0-63, K rows in 64-127);
@@ -807,31 +806,11 @@ __device__ __forceinline__ void pass_load_qk(uint8_t *st, uint64_t *bar, const C
     }
 }
 
-// All tiles of one chunk into a stage on one barrier: Q|K, then P_hi, P_lo, R_hi, R_lo of (chunk gc, head h).
-__device__ __forceinline__ void pass_issue_loads(uint8_t *st, uint64_t *bar, const CUtensorMap *qmap,
-                                                 const CUtensorMap *kmap, const CUtensorMap *phmap,
-                                                 const CUtensorMap *plmap, const CUtensorMap *rhmap,
-                                                 const CUtensorMap *rlmap, int hq, int t0, int gc, int hv, int h,
-                                                 int hk, int total, int nch, unsigned int *err) {
-    mbar_arrive_expect_tx(bar, kStageTx);
-    pass_load_qk(st, bar, qmap, kmap, hq, t0, hk, total, err);
-    const int prow = (gc * hv + h) * D;
-    if (!GDN_INB((long)prow + D - 1, (long)nch * hv * D, err)) return;
-    (void)nch;
-    tma_load_2d(st + ST_PH, phmap, bar, 0, prow);
-    tma_load_2d(st + ST_PL, plmap, bar, 0, prow);
-    tma_load_2d(st + ST_RH, rhmap, bar, 0, (gc * hv + h) * C);
-    tma_load_2d(st + ST_RL, rlmap, bar, 0, (gc * hv + h) * C);
-}
-
 // 8 warps: warps w and w + 4 share TMEM lane quadrant w % 4 and split the CTA's 32 value rows (NG row groups).
 // 128 and 512 threads (32 and 8 rows per thread) measured 119 and 146 us against 115 us at the 4K layer.
 constexpr int kPassThreads = 256;
 constexpr int NG = kPassThreads / 128;
 
-// MMA issuers in state_pass_norm_kernel: thread 0 (a Q-row warp, idle until the X barrier) issues [Q;K] S^T;
-// lanes 0 of warps 2 and 3 (K-row warps, idle between the X barrier and the state update) issue P X and R X.
-constexpr int kPxIssuer = 64, kRxIssuer = 96;
 constexpr int DG = DS / NG;         // state rows per thread
 
 // Per-chunk inputs that are read with plain loads (gates, beta, this thread's v
@@ -884,48 +863,20 @@ __device__ __forceinline__ void finish_gates(ChunkInputs &in, int L, int lane, b
 
 // Outputs of one chunk for this thread's token and 16 value rows (Q-row threads):
 // O_i = e^{g_i} (Q S^T)_i (in qs) + (R X)_i ((R_hi + R_lo) X_hi, and (R_hi + R_lo) X_lo).
-// outputs_begin adds R X into qs; outputs_end writes them.  NORM: the output normalisation over the head's
-// 128 rows, which this cluster's four CTAs hold 32 of each: begin publishes the token's sum of squares over
-// this thread's rows and arrives on the cluster barrier, end waits for it, adds the head's sums through
-// distributed shared memory and scales.  Every thread of the cluster takes part in each round (K-row threads
-// arrive early and wait later); `valid` false keeps the round but skips TMEM and global memory.
-template <bool NORM>
-__device__ __forceinline__ void outputs_begin(float (&qs)[DG], uint32_t tmem_rx, int grp, int i, int L, bool valid,
-                                              float (*ps)[64]) {
+// outputs_begin adds R X into qs (`valid` false skips TMEM); outputs_end writes them.
+__device__ __forceinline__ void outputs_begin(float (&qs)[DG], uint32_t tmem_rx, int grp, bool valid) {
     if (valid) {
         float a[DG], b[DG];
         tmem_ldx2<DG>(tmem_rx + grp * DG, tmem_rx + 32 + grp * DG, a, b);
 #pragma unroll
         for (int e = 0; e < DG; ++e) qs[e] += a[e] + b[e];
     }
-    if (NORM) {
-        float ss = 0.f;
-        if (valid && i < L) {
-#pragma unroll
-            for (int e = 0; e < DG; ++e) ss = fmaf(qs[e], qs[e], ss);
-        }
-        ps[grp][i] = ss;
-        cluster_arrive();
-    }
 }
 
-template <bool NORM>
-__device__ __forceinline__ void outputs_end(float (&qs)[DG], int grp, int i, int L, int t0, int hv, int h, int rowg,
-                                            void *__restrict__ out, int out_f32, bool valid, float (*ps)[64],
-                                            const float *__restrict__ norm_w, float norm_eps, long out_n,
+__device__ __forceinline__ void outputs_end(const float (&qs)[DG], int i, int L, int t0, int hv, int h, int rowg,
+                                            void *__restrict__ out, int out_f32, bool valid, long out_n,
                                             unsigned int *err) {
     (void)out_n;
-    if (NORM) {
-        cluster_wait();
-        float tot = 0.f;
-#pragma unroll
-        for (int rk = 0; rk < D / DS; ++rk)
-#pragma unroll
-            for (int g = 0; g < NG; ++g) tot += ld_dsmem_f32(&ps[g][i], rk);
-        const float sc = rsqrtf(tot * (1.f / D) + norm_eps);
-#pragma unroll
-        for (int e = 0; e < DG; ++e) qs[e] *= sc * norm_w[rowg + e];
-    }
     if (valid && i < L && GDN_INB(((size_t)(t0 + i) * hv + h) * D + rowg + DG - 1, out_n, err)) {
         const size_t o = ((size_t)(t0 + i) * hv + h) * D + rowg;
         if (out_f32) {
@@ -942,321 +893,10 @@ __device__ __forceinline__ void outputs_end(float (&qs)[DG], int grp, int i, int
     }
 }
 
-// Thread roles (256 threads).  TMEM lane quadrant quad = warp % 4, row group grp = warp / 4 (which DG = 16 of
-// the CTA's 32 value rows).  Lane l of quadrant quad is accumulator row 32 quad + l: for [Q;K] S^T and
-// R X that row is a token (Q rows for quad 0-1, K rows for quad 2-3); for P X it is state column d.
-// Thread 0 issues the [Q;K] S^T MMAs and thread 32 the TMA loads (both Q-row threads, which have nothing
-// to do before the X barrier); threads kPxIssuer and kRxIssuer (K-row threads, which have nothing to do
-// between the X barrier and the state update) issue P X and R X.
-// GATE: the gates are formed from raw inputs (gdn.h: gate_scale, gate_bias).
-template <bool GATE>
-__global__ void __launch_bounds__(kPassThreads, 1)
-state_pass_norm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                  const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
-                  const __grid_constant__ CUtensorMap rhmap, const __grid_constant__ CUtensorMap rlmap,
-                  const __nv_bfloat16 *__restrict__ v, const float *__restrict__ norms, float q_scale,
-                  const float *__restrict__ log_alpha, const float *__restrict__ beta,
-                  const float *__restrict__ init_state, const int32_t *__restrict__ cu, int n_seqs, int total,
-                  int nch, int hk, int hv, void *__restrict__ out, int out_f32, float *__restrict__ final_state,
-                  const float *__restrict__ norm_w, float norm_eps, const float *__restrict__ gate_c,
-                  const float *__restrict__ gate_b, unsigned int *err) {
-    extern __shared__ uint8_t pass_raw[];
-    uint8_t *sm = align1024(pass_raw);
-    __shared__ uint64_t bar_tma[2], bar_d1, bar_px, bar_rx[2];
-    __shared__ float ps_norm[2][NG][64];   // per-token sums of squares of each group's rows, by chunk parity
-    __shared__ uint32_t tmem_slot;
-
-    constexpr int SLICES = D / DS;
-    const int slice = blockIdx.x % SLICES;
-    const int h = (blockIdx.x / SLICES) % hv;
-    const int n = blockIdx.x / (SLICES * hv);
-    const int hq = h / (hv / hk);
-    const int row0 = slice * DS;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, grp = warp >> 2;
-    const int lrow = 32 * quad + lane;     // TMEM lane of this thread
-    const int d = lrow;                    // state column (dk index) in P X
-    const int i = lrow & 63;               // token row in [Q;K] S^T and R X
-    const bool krow = quad >= 2;           // lanes 64..127 hold the K rows
-    const int rowg = row0 + grp * DG;      // first value row of this thread's group
-    const uint32_t base = smem_u32(sm);
-
-    int ta = 0, tb = total, gc0 = 0;   // one sequence: the host checked cu_seqlens = {0, total}
-    if (n_seqs > 1) {
-        seq_range(cu, n, total, ta, tb);
-        gc0 = first_chunk_of(cu, n, total);
-    }
-    const int nchunks = (tb - ta + C - 1) / C;
-    bool ok = gc0 + nchunks <= nch;
-    if (!ok && tid == 0) raise_error(err, kErrInternal);
-    const bool started = ok && nchunks > 0;   // chunk 0's tiles are requested below
-
-    if (warp == 0) {
-        tmem_alloc(&tmem_slot, PASS_TMEM_COLS);
-        tmem_relinquish();
-    }
-    if (tid == 0) {
-        mbar_init(&bar_tma[0], 1);
-        mbar_init(&bar_tma[1], 1);
-        mbar_init(&bar_d1, 1);
-        mbar_init(&bar_px, 1);
-        mbar_init(&bar_rx[0], 1);
-        mbar_init(&bar_rx[1], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 32 && started) {
-        tma_prefetch_desc(&qmap);
-        tma_prefetch_desc(&kmap);
-        tma_prefetch_desc(&phmap);
-        tma_prefetch_desc(&plmap);
-        tma_prefetch_desc(&rhmap);
-        tma_prefetch_desc(&rlmap);
-        pass_issue_loads(sm, &bar_tma[0], &qmap, &kmap, &phmap, &plmap, &rhmap, &rlmap, hq, ta, gc0, hv, h, hk, total, nch, err);
-    }
-    ChunkInputs nxt, nxt2;   // loaded two chunks ahead, as in state_pass_kernel
-    if (started) {
-        load_chunk_inputs(nxt, log_alpha, beta, v, norms, q_scale, gc0, ta, min(C, tb - ta), hv, h, rowg, lane, krow, i, total, nch, err);
-        if (nchunks > 1)
-            load_chunk_inputs(nxt2, log_alpha, beta, v, norms, q_scale, gc0 + 1, ta + C, min(C, tb - ta - C), hv, h,
-                              rowg, lane, krow, i, total, nch, err);
-    }
-
-    // state columns: thread (d, grp) holds S[rowg + r][d] for r < DG
-    float S[DG];
-    const size_t sbase = (((size_t)n * hv + h) * D + rowg) * D + d;
-    const bool state_ok = GDN_INB(sbase + (size_t)(DG - 1) * D, (long)n_seqs * hv * D * D, err);
-#pragma unroll
-    for (int r = 0; r < DG; ++r) S[r] = init_state && state_ok ? init_state[sbase + (size_t)r * D] : 0.f;
-
-    // The state operand [S_hi ; S_lo] is stored MN-major: row d (the dk index, K of the MMA) holds the 64
-    // values n = 0..31 (S_hi rows) and 32..63 (S_lo rows); this thread writes its DG rows as two 16-byte
-    // pieces of each half.
-    auto write_sop = [&]() {
-#pragma unroll
-        for (int j = 0; j < DG / 8; ++j) {
-            uint4 hi, lo;
-            split8_bf16(&S[8 * j], hi, lo);
-            *reinterpret_cast<uint4 *>(sm + PASS_SOP + sw128_offset(d, grp * DG + 8 * j)) = hi;
-            *reinterpret_cast<uint4 *>(sm + PASS_SOP + sw128_offset(d, DS + grp * DG + 8 * j)) = lo;
-        }
-    };
-    write_sop();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_slot;
-    const uint32_t tlane = (uint32_t)(32 * quad) << 16;
-
-    // Shared-memory descriptors (the same for every thread, built outside divergent code); a K step adds a
-    // byte offset >> 4 to the start field (all tiles sit far below 256 KiB, so the 14-bit field never carries).
-    const uint64_t dQK0 = smem_desc(base + ST_QK, 16, 1024, kSW);
-    const uint64_t dPH0 = smem_desc(base + ST_PH, 16, 1024, kSW);
-    const uint64_t dPL0 = smem_desc(base + ST_PL, 16, 1024, kSW);
-    const uint64_t dRH0 = smem_desc(base + ST_RH, 16, 1024, kSW);
-    const uint64_t dRL0 = smem_desc(base + ST_RL, 16, 1024, kSW);
-    const uint64_t dSOP = smem_desc(base + PASS_SOP, 8192, 1024, kSW);   // MN-major B: 16 K-rows = 2048 B
-    const uint64_t dXOP = smem_desc(base + PASS_XOP, 8192, 1024, kSW);
-    constexpr uint64_t kStageStep = PASS_STAGE >> 4;
-    constexpr uint32_t idb = idesc_bf16_f32(128, 64, false, true);   // A K-major, B MN-major, N = 64
-
-    // Chunk c's R X is committed to bar_rx[c & 1]; this is the parity of its completion there.
-    auto rx_parity = [](int cc) { return (uint32_t)((cc >> 1) & 1); };
-
-    float qs[DG];
-    float qcur_n[DG];   // this chunk's e^g Q S^T, kept until the previous chunk's outputs have left
-    int c = 0, prev_t0 = 0, prev_L = 0, c_stop = nchunks;
-    // Every chunk keeps its cluster barrier round even after an error (the cluster barrier has no time limit,
-    // so no CTA may leave the sequence of rounds its peers still run): work stops, rounds do not.
-    for (; c < nchunks; ++c) {
-        if (!ok) {
-            if (c > 0) {
-                cluster_arrive();
-                cluster_wait();
-            }
-            continue;
-        }
-        const int s = c & 1;
-        const uint32_t par = c & 1;
-        const int t0 = ta + c * C, L = min(C, tb - t0);
-        const int gc = gc0 + c;
-        ChunkInputs cur = nxt;
-        nxt = nxt2;
-        finish_gates<GATE>(cur, L, lane, krow, i, gate_c, gate_b, h);
-        const uint64_t so = s * kStageStep;
-
-        if (tid == 0) {
-            // D1[128 x 64] = [Q ; K] [S_hi ; S_lo]^T, once this chunk's tiles have landed
-            if (mbar_wait(&bar_tma[s], (c >> 1) & 1)) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    mma_bf16(tmem + TM_D1, dQK0 + so + off, dSOP + 128 * kk, idb, kk > 0);
-                }
-                mma_commit(&bar_d1);
-            } else {
-                ok = false;
-            }
-        } else if (tid == 32 && c + 1 < nchunks) {
-            // next chunk's tiles go to the other stage once its last reader (the R X of chunk c - 1) is done
-            if (c == 0 || mbar_wait(&bar_rx[par ^ 1], rx_parity(c - 1)))
-                pass_issue_loads(sm + (s ^ 1) * PASS_STAGE, &bar_tma[s ^ 1], &qmap, &kmap, &phmap, &plmap, &rhmap,
-                                 &rlmap, hq, t0 + C, gc + 1, hv, h, hk, total, nch, err);
-            else
-                ok = false;
-        }
-        if (c + 2 < nchunks)
-            load_chunk_inputs(nxt2, log_alpha, beta, v, norms, q_scale, gc + 2, t0 + 2 * C, min(C, tb - t0 - 2 * C),
-                              hv, h, rowg, lane, krow, i, total, nch, err);
-
-        const float2 g2 = cumsum_pairs(cur.la0, cur.la1, L, lane);
-        const float gL = g_of(g2, L - 1);
-        const float eg = __expf(g_of(g2, i));
-
-        if (krow) {
-            // X_i = beta_i (v_i - e^{g_i} (K S^T)_i), split into bf16 hi/lo.  The X tile is stored MN-major:
-            // row i (the token, K of the MMA) holds n = 0..31 (X_hi) and 32..63 (X_lo).  It is rewritten only
-            // after the previous chunk's R X, its last reader, is complete.
-            if (!mbar_wait(&bar_d1, par)) ok = false;
-            if (c > 0 && !mbar_wait(&bar_rx[par ^ 1], rx_parity(c - 1))) ok = false;
-            tc_fence_after();
-            float a[DG], b[DG];   // x S_hi^T and x S_lo^T, this group's rows
-            tmem_ldx2<DG>(tmem + tlane + TM_D1 + grp * DG, tmem + tlane + TM_D1 + 32 + grp * DG, a, b);
-            const float bi = cur.b, be = cur.b * eg * cur.f;
-#pragma unroll
-            for (int q4 = 0; q4 < DG / 8; ++q4) {
-                const uint4 x = cur.v[q4];
-                const float vv[8] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y),
-                                     bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w)};
-                float xv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xv[e] = bi * vv[e] - be * (a[q4 * 8 + e] + b[q4 * 8 + e]);
-                uint4 hi, lo;
-                split8_bf16(xv, hi, lo);
-                *reinterpret_cast<uint4 *>(sm + PASS_XOP + sw128_offset(i, grp * DG + 8 * q4)) = hi;
-                *reinterpret_cast<uint4 *>(sm + PASS_XOP + sw128_offset(i, DS + grp * DG + 8 * q4)) = lo;
-            }
-        }
-        // X tile complete
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-
-        if (tid == kPxIssuer) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {   // P X (dk x 64) = P_hi [X_hi ; X_lo]^T + P_lo [X_hi ; X_lo]^T
-                mma_bf16(tmem + TM_PX, dPH0 + so + 2 * kk, dXOP + 128 * kk, idb, kk > 0);
-                mma_bf16(tmem + TM_PX, dPL0 + so + 2 * kk, dXOP + 128 * kk, idb, 1);
-            }
-            mma_commit(&bar_px);             // the state update waits only for this
-        } else if (tid == kRxIssuer) {
-            const uint32_t rx = tmem + TM_RX + 64 * par;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)   // R X (64 valid rows x 64) = R_hi [X_hi ; X_lo]^T
-                mma_bf16(rx, dRH0 + so + 2 * kk, dXOP + 128 * kk, idb, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)   //   + R_lo [X_hi ; X_lo]^T
-                mma_bf16(rx, dRL0 + so + 2 * kk, dXOP + 128 * kk, idb, 1);
-            mma_commit(&bar_rx[par]);
-        }
-        if (krow && c > 0) cluster_arrive();   // K-row threads' share of this chunk's output round
-        if (!krow) {
-            // Q-row threads, off the state chain while P X runs: e^{g_i} (Q S^T)_i of this chunk (D1 is
-            // rewritten only after the end-of-chunk barrier), then the previous chunk's outputs, whose R X
-            // sits in the other buffer.
-            if (!mbar_wait(&bar_d1, par)) ok = false;
-            tc_fence_after();
-            float qcur[DG];
-            {
-                float a[DG], b[DG];
-                tmem_ldx2<DG>(tmem + tlane + TM_D1 + grp * DG, tmem + tlane + TM_D1 + 32 + grp * DG, a, b);
-#pragma unroll
-                for (int r = 0; r < DG; ++r) qcur[r] = (eg * cur.f) * (a[r] + b[r]);
-            }
-#pragma unroll
-            for (int r = 0; r < DG; ++r) qcur_n[r] = qcur[r];
-            if (c > 0) {
-                if (!mbar_wait(&bar_rx[par ^ 1], rx_parity(c - 1))) ok = false;
-                tc_fence_after();
-                // the outputs leave after the state update: the cluster round then overlaps the update instead
-                // of delaying it
-                outputs_begin<true>(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, true,
-                                    ps_norm[(c - 1) & 1]);
-            }
-        }
-
-        // state: S[r][d] <- e^{g_L} S[r][d] + (P X)[d][r] + (P X)[d][32 + r]   (this group's DG rows)
-        if (!mbar_wait(&bar_px, par)) ok = false;
-        tc_fence_after();
-        {
-            const float eL = __expf(gL);
-            float a[DG], b[DG];
-            tmem_ldx2<DG>(tmem + tlane + TM_PX + grp * DG, tmem + tlane + TM_PX + 32 + grp * DG, a, b);
-#pragma unroll
-            for (int e = 0; e < DG; ++e) S[e] = fmaf(eL, S[e], a[e] + b[e]);
-        }
-        write_sop();
-        if (krow) {
-            if (c > 0) cluster_wait();
-        } else {
-            if (c > 0)
-                outputs_end<true>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, true,
-                                  ps_norm[(c - 1) & 1], norm_w, norm_eps, (long)total * hv * D, err);
-#pragma unroll
-            for (int r = 0; r < DG; ++r) qs[r] = qcur_n[r];
-        }
-        prev_t0 = t0;
-        prev_L = L;
-        fence_proxy_async_smem();
-        tc_fence_before();
-        ok = __syncthreads_and(ok);
-        tc_fence_after();
-        if (!ok && c_stop == nchunks) c_stop = c + 1;
-    }
-
-    if (!ok) {
-        // the loop's work stopped after chunk c_stop - 1; its prefetch of chunk c_stop may still be in flight
-        if (tid == 0 && started) {
-            raise_error(err, kErrTimeout);
-            if (c_stop < nchunks) mbar_wait(&bar_tma[c_stop & 1], (c_stop >> 1) & 1);
-        }
-        if (nchunks > 0) {   // the last chunk's output round, kept
-            cluster_arrive();
-            cluster_wait();
-        }
-    } else {
-        if (nchunks > 0) {
-            const uint32_t lp = (nchunks - 1) & 1;
-            if (!krow) {
-                const bool done = mbar_wait(&bar_rx[lp], rx_parity(nchunks - 1));
-                tc_fence_after();
-                if (!done) raise_error(err, kErrTimeout);
-                outputs_begin<true>(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, done, ps_norm[lp]);
-                outputs_end<true>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, done, ps_norm[lp], norm_w,
-                                  norm_eps, (long)total * hv * D, err);
-            } else {
-                cluster_arrive();
-                cluster_wait();
-            }
-        }
-        if (final_state && state_ok) {
-#pragma unroll
-            for (int r = 0; r < DG; ++r) final_state[sbase + (size_t)r * D] = S[r];
-        }
-    }
-    tc_fence_before();
-    cluster_sync();   // no CTA leaves while a peer may still read its sums
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, PASS_TMEM_COLS);
-}
-
-// ============================================================================
-// Kernel 2b: state passing + outputs, warp-specialised (no output normalisation)
-// ============================================================================
-// Warps 0-7 compute exactly as in state_pass_norm_kernel (same TMEM quadrants, rows and arithmetic); lane 0
-// of warp 8 issues every MMA and lane 0 of warp 9 every tensor load.  The compute warps never wait behind an
+// Thread roles (320 threads).  Warps 0-7 compute: TMEM lane quadrant quad = warp % 4, row group grp = warp / 4
+// (which DG = 16 of the CTA's 32 value rows).  Lane l of quadrant quad is accumulator row 32 quad + l: for
+// [Q;K] S^T and R X that row is a token (Q rows for quad 0-1, K rows for quad 2-3); for P X it is state
+// column d.  Lane 0 of warp 8 issues every MMA and lane 0 of warp 9 every tensor load.  The compute warps never wait behind an
 // issuing thread (a tensor load's issue can stall its thread for thousands of cycles when memory is busy):
 // they meet the issuers through mbarriers only, two per chunk.
 //   bar_x[b]  X buffer b written (128 arrivals, the K-row threads)              -> P X, later R X
@@ -1278,7 +918,16 @@ constexpr uint32_t kPTx = 16384 + 16384, kRTx = 8192 + 8192;
 
 // MULTI: a CTA may carry several sequences (buckets of more than one); without it each bucket is one sequence
 // and the chunk loop has none of the sequence-boundary code.
-template <bool GATE, bool MULTI>
+// NORM: the output normalisation o <- o / sqrt(mean_head(o^2) + eps) * w over the head's 128 rows, which the
+// four slice CTAs of a (bucket, head) hold 32 each; they form a cluster.  Per chunk every Q-row thread writes
+// its token's sum of squares over its 16 rows into its CTA's block of the slot array (two slot sets by chunk
+// parity); after a named barrier of the 128 Q-row threads one of them sends the block (512 bytes) to the same
+// place in each peer CTA with a bulk copy that completes on the peer's norm barrier, and arms its own barrier
+// for the three peers' blocks.  Every Q-row thread then waits on its own barrier and adds its token's eight
+// sums.  Only the Q-row threads take part, so the MMA and tile warps never wait on the cluster.  A slot set is
+// written again two chunks later: by then the peers have received this CTA's block of the chunk in between,
+// which it sends only after reading; the barrier's phases advance the same way, so they never alias.
+template <bool GATE, bool MULTI, bool NORM>
 __global__ void __launch_bounds__(kWsThreads, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap phmap, const __grid_constant__ CUtensorMap plmap,
@@ -1288,11 +937,14 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                   const float *__restrict__ init_state, const int32_t *__restrict__ cu, int n_seqs, int total,
                   int nch, int hk, int hv, void *__restrict__ out, int out_f32, float *__restrict__ final_state,
                   const float *__restrict__ gate_c, const float *__restrict__ gate_b, unsigned int *err,
-                  const __grid_constant__ PassBuckets bk) {
+                  const __grid_constant__ PassBuckets bk, const float *__restrict__ norm_w, float norm_eps) {
     extern __shared__ uint8_t pass_raw[];
     uint8_t *sm = align1024(pass_raw);
     __shared__ uint64_t bar_qk[2], bar_p[2], bar_r[2], bar_qkf[2], bar_pf[2], bar_rf[2];
     __shared__ uint64_t bar_s, bar_x[2], bar_d1, bar_px, bar_rx[2];
+    __shared__ uint64_t bar_norm[2];
+    // [chunk parity][cluster rank][row group][token]; the bulk copies need 16-byte aligned blocks
+    __shared__ __align__(128) float norm_part[NORM ? 2 * 4 * NG * 64 : 4];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;   // set by any thread whose wait ran out; everyone stops at the next check
     __shared__ int warp_chunks[kWsThreads / 32];
@@ -1349,12 +1001,17 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         mbar_init(&bar_s, kPassThreads);
         mbar_init(&bar_d1, 1);
         mbar_init(&bar_px, 1);
+        if (NORM) {
+            mbar_init(&bar_norm[0], 1);
+            mbar_init(&bar_norm[1], 1);
+        }
         abort_flag = 0;
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (NORM) cluster_sync();   // every CTA's norm barrier is initialised before any peer arrives on it
     const uint32_t tmem = tmem_slot;
     // the planned chunks must be the ones the device's sequence table gives (a host copy that disagrees with it
     // would send the loads past the planned range): otherwise record the error and run nothing
@@ -1366,7 +1023,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     if (!range_ok && tid == 0) raise_error(err, kErrInternal);
     const bool started = range_ok && nchunks > 0;
 
-    // Shared-memory descriptors, as in state_pass_norm_kernel.
+    // Shared-memory descriptors (the same for every thread, built outside divergent code); a K step adds a
+    // byte offset >> 4 to the start field (all tiles sit far below 256 KiB, so the 14-bit field never carries).
     const uint64_t dQK0 = smem_desc(base + ST_QK, 16, 1024, kSW);
     const uint64_t dPH0 = smem_desc(base + ST_PH, 16, 1024, kSW);
     const uint64_t dPL0 = smem_desc(base + ST_PL, 16, 1024, kSW);
@@ -1502,7 +1160,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         }
         __syncwarp();
     } else {
-        // compute warps: roles as in state_pass_norm_kernel
+        // compute warps
         const int quad = warp & 3, grp = warp >> 2;
         const int lrow = 32 * quad + lane;
         const int d = lrow;
@@ -1570,8 +1228,52 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         };
         if (started) publish_sop();
 
-        float qs[DG];
+        float qs[DG], qcur[DG];   // Q-row threads: outputs being finished, and this chunk's e^g f_q Q S^T
         int prev_t0 = 0, prev_L = 0;
+        const uint32_t crank = NORM ? cluster_ctarank() : 0u;
+        // Outputs of chunk j (Q-row threads; qs holds e^g f_q Q S^T, R X is in TMEM at trx), in two steps so that
+        // with NORM the exchange of the head's sums of squares waits off the state chain: send_outputs adds R X
+        // and sends this CTA's sums (NORM), finish_outputs (after the state update) waits for the peers' sums,
+        // normalises and writes.  finish_outputs is false when the exchange timed out.
+        auto send_outputs = [&](int j, uint32_t trx, bool valid) {
+            outputs_begin(qs, trx, grp, valid);
+            if (NORM) {
+                float ss = 0.f;
+                if (valid && i < prev_L) {
+#pragma unroll
+                    for (int e = 0; e < DG; ++e) ss = fmaf(qs[e], qs[e], ss);
+                }
+                const int np = j & 1;
+                constexpr uint32_t kBlock = NG * 64 * 4;   // one CTA's sums of a chunk, bytes
+                float *mine = norm_part + (np * 4 + (int)crank) * NG * 64;
+                mine[grp * 64 + i] = ss;
+                fence_proxy_async_smem();                          // read by the bulk copies
+                asm volatile("bar.sync 1, 128;" ::: "memory");    // the Q-row threads (warps 0, 1, 4, 5)
+                if (tid == 0) {
+#pragma unroll
+                    for (uint32_t rk = 0; rk < 4; ++rk)
+                        if (rk != crank) bulk_copy_to_peer(mine, mine, kBlock, &bar_norm[np], rk);
+                    mbar_arrive_expect_tx(&bar_norm[np], 3 * kBlock);
+                }
+            }
+        };
+        auto finish_outputs = [&](int j, bool valid) -> bool {
+            bool got = true;
+            if (NORM) {
+                const int np = j & 1;
+                got = mbar_spin_cluster(&bar_norm[np], (uint32_t)((j >> 1) & 1));
+                float tot = 0.f;
+#pragma unroll
+                for (int rk = 0; rk < 4; ++rk)
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) tot += norm_part[((np * 4 + rk) * NG + g) * 64 + i];
+                const float sc = rsqrtf(tot * (1.f / D) + norm_eps);
+#pragma unroll
+                for (int e = 0; e < DG; ++e) qs[e] *= sc * norm_w[rowg + e];
+            }
+            outputs_end(qs, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, valid && got, (long)total * hv * D, err);
+            return got;
+        };
         bool ok = range_ok;   // an empty sequence runs no chunk and returns its initial state
         int c = 0;
         for (; ok && c < nchunks; ++c) {
@@ -1634,8 +1336,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 fence_proxy_async_smem();
                 mbar_arrive(&bar_x[par]);
             } else {
-                // Q-row threads: e^{g_i} (Q S^T)_i of this chunk, then the previous chunk's outputs
-                float qcur[DG];
+                // Q-row threads: e^{g_i} (Q S^T)_i of this chunk (into qcur), and the previous chunk's outputs
                 {
                     float a[DG], b[DG];
                     tmem_ldx2<DG>(tmem + tlane + TM_D1 + grp * DG, tmem + tlane + TM_D1 + 32 + grp * DG, a, b);
@@ -1645,12 +1346,16 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 if (c > 0) {
                     if (!mbar_wait(&bar_rx[par ^ 1], ph(c - 1))) ok = false;
                     tc_fence_after();
-                    outputs_begin<false>(qs, tmem + tlane + TM_RX + 64 * (par ^ 1), grp, i, prev_L, ok, nullptr);
-                    outputs_end<false>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, ok, nullptr, nullptr,
-                                       0.f, (long)total * hv * D, err);
-                }
+                    send_outputs(c - 1, tmem + tlane + TM_RX + 64 * (par ^ 1), ok);
+                    if (!NORM) {
+                        finish_outputs(c - 1, ok);
 #pragma unroll
-                for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
+                        for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
+                    }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
+                }
             }
 
             // state: S[r][d] <- e^{g_L} S[r][d] + (P X)[d][r] + (P X)[d][32 + r]
@@ -1674,6 +1379,11 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 for (int r = 0; r < DG; ++r) S[r] = next_ok ? init_state[nsb + (size_t)r * D] : 0.f;
             }
             publish_sop();
+            if (NORM && !krow && c > 0) {   // the previous chunk's normalised outputs, now off the state chain
+                if (!finish_outputs(c - 1, ok)) ok = false;
+#pragma unroll
+                for (int r = 0; r < DG; ++r) qs[r] = qcur[r];
+            }
             prev_t0 = t0;
             prev_L = L;
             if (MULTI && seq_end) {
@@ -1691,8 +1401,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 const bool done = mbar_wait(&bar_rx[lp], ph(nchunks - 1));
                 tc_fence_after();
                 if (!done) fail();
-                outputs_begin<false>(qs, tmem + tlane + TM_RX + 64 * lp, grp, i, prev_L, done, nullptr);
-                outputs_end<false>(qs, grp, i, prev_L, prev_t0, hv, h, rowg, out, out_f32, done, nullptr, nullptr, 0.f, (long)total * hv * D, err);
+                send_outputs(nchunks - 1, tmem + tlane + TM_RX + 64 * lp, done);
+                if (!finish_outputs(nchunks - 1, done)) fail();
             }
             if (!MULTI && final_state && state_ok) {
 #pragma unroll
@@ -1703,6 +1413,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (NORM) cluster_sync();   // no CTA leaves while a peer may still write its slots or barriers
     if (tid == 0 && started && abort_flag) raise_error(err, kErrTimeout);
     if (warp == 0) tmem_dealloc(tmem, PASS_TMEM_COLS);
 }
@@ -1854,9 +1565,14 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
     if (!cached || !attrs_set[dev].load(std::memory_order_acquire)) {
         const void *prep[] = {(const void *)chunk_prep_kernel<false, false>, (const void *)chunk_prep_kernel<true, false>,
                               (const void *)chunk_prep_kernel<false, true>, (const void *)chunk_prep_kernel<true, true>};
-        const void *pass[] = {(const void *)state_pass_kernel<false, false>, (const void *)state_pass_kernel<true, false>,
-                              (const void *)state_pass_kernel<false, true>, (const void *)state_pass_kernel<true, true>,
-                              (const void *)state_pass_norm_kernel<false>, (const void *)state_pass_norm_kernel<true>};
+        const void *pass[] = {(const void *)state_pass_kernel<false, false, false>,
+                              (const void *)state_pass_kernel<true, false, false>,
+                              (const void *)state_pass_kernel<false, true, false>,
+                              (const void *)state_pass_kernel<true, true, false>,
+                              (const void *)state_pass_kernel<false, false, true>,
+                              (const void *)state_pass_kernel<true, false, true>,
+                              (const void *)state_pass_kernel<false, true, true>,
+                              (const void *)state_pass_kernel<true, true, true>};
         for (const void *f : prep)
             if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
         for (const void *f : pass)
@@ -1886,51 +1602,47 @@ cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
-        // with the output normalisation the D / DS slices of a (sequence, head) form one cluster
-        const unsigned grid2 = (unsigned)(p.n_seqs * p.hv * (D / DS));
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = D / DS;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
         const float *nrm = p.qk_norm ? norms : nullptr;
-        if (p.norm_w) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(grid2);
-            cfg.blockDim = dim3(kPassThreads);
-            cfg.dynamicSmemBytes = PASS_SMEM;
-            cfg.stream = p.stream;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            e = cudaLaunchKernelEx(&cfg, gate ? state_pass_norm_kernel<true> : state_pass_norm_kernel<false>, qmap,
-                                   kmap, phmap, plmap, rhmap, rlmap, p.v, nrm, p.q_scale, p.log_alpha, p.beta,
-                                   p.init_state, p.cu_seqlens, p.n_seqs, p.total_tokens, (int)nch, p.hk, p.hv, p.out,
-                                   p.out_f32, p.final_state, p.norm_w, p.norm_eps, p.gate_c, p.gate_b, p.err);
-        } else {
-            PassBuckets bk;
-            const int nb = pass_buckets(bk, p.n_seqs, p.cu_seqlens_host, nch, p.hv, multiprocessors(dev));
-            const bool multi = nb < p.n_seqs;   // some bucket carries more than one sequence
-            auto pass = multi ? (gate ? state_pass_kernel<true, true> : state_pass_kernel<false, true>)
-                              : (gate ? state_pass_kernel<true, false> : state_pass_kernel<false, false>);
-            // Right after this call's preparation the pass is its programmatic dependent: its CTAs may start on
-            // SMs the preparation has left, run their prologue and first products (which read only the
-            // inputs, complete since before the preparation started), and wait for the preparation before
-            // reading the workspace.  Launched alone it follows the stream as usual.
-            cudaLaunchAttribute pdl[1];
-            pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            pdl[0].val.programmaticStreamSerializationAllowed = 1;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)(nb * p.hv * (D / DS)));
-            cfg.blockDim = dim3(kWsThreads);
-            cfg.dynamicSmemBytes = PASS_SMEM;
-            cfg.stream = p.stream;
-            cfg.attrs = pdl;
-            cfg.numAttrs = (phases & 1) && nch > 0 ? 1 : 0;
-            e = cudaLaunchKernelEx(&cfg, pass, qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm, p.q_scale,
-                                   p.log_alpha, p.beta, p.init_state, p.cu_seqlens, p.n_seqs, p.total_tokens,
-                                   (int)nch, p.hk, p.hv, p.out, p.out_f32, p.final_state, p.gate_c, p.gate_b,
-                                   p.err, bk);
+        PassBuckets bk;
+        const int nb = pass_buckets(bk, p.n_seqs, p.cu_seqlens_host, nch, p.hv, multiprocessors(dev));
+        const bool multi = nb < p.n_seqs;   // some bucket carries more than one sequence
+        const bool norm = p.norm_w != nullptr;
+        using PassFn = decltype(&state_pass_kernel<false, false, false>);
+        const PassFn table[8] = {state_pass_kernel<false, false, false>, state_pass_kernel<true, false, false>,
+                                 state_pass_kernel<false, true, false>,  state_pass_kernel<true, true, false>,
+                                 state_pass_kernel<false, false, true>,  state_pass_kernel<true, false, true>,
+                                 state_pass_kernel<false, true, true>,   state_pass_kernel<true, true, true>};
+        const PassFn pass = table[(gate ? 1 : 0) + (multi ? 2 : 0) + (norm ? 4 : 0)];
+        // With the output normalisation the four slice CTAs of a (bucket, head) form one cluster.  Right after
+        // this call's preparation the pass is its programmatic dependent: its CTAs may start on SMs the
+        // preparation has left, run their prologue and first products (which read only the inputs, complete
+        // since before the preparation started), and wait for the preparation before reading the workspace.
+        // Launched alone it follows the stream as usual.
+        cudaLaunchAttribute attr[2];
+        int nattr = 0;
+        if (norm) {
+            attr[nattr].id = cudaLaunchAttributeClusterDimension;
+            attr[nattr].val.clusterDim.x = D / DS;
+            attr[nattr].val.clusterDim.y = 1;
+            attr[nattr].val.clusterDim.z = 1;
+            ++nattr;
         }
+        if ((phases & 1) && nch > 0) {
+            attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+            ++nattr;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(nb * p.hv * (D / DS)));
+        cfg.blockDim = dim3(kWsThreads);
+        cfg.dynamicSmemBytes = PASS_SMEM;
+        cfg.stream = p.stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = nattr;
+        e = cudaLaunchKernelEx(&cfg, pass, qmap, kmap, phmap, plmap, rhmap, rlmap, p.v, nrm, p.q_scale, p.log_alpha,
+                               p.beta, p.init_state, p.cu_seqlens, p.n_seqs, p.total_tokens, (int)nch, p.hk, p.hv,
+                               p.out, p.out_f32, p.final_state, p.gate_c, p.gate_b, p.err, bk, p.norm_w,
+                               p.norm_eps);
         if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -114,6 +114,40 @@ __device__ __forceinline__ float ld_dsmem_f32(const float *p, uint32_t rank) {
     return v;
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's shared memory at src
+// to the same offset as dst in CTA `rank` of the cluster, completing its bytes on the mbarrier at bar's offset
+// in that CTA.
+__device__ __forceinline__ void bulk_copy_to_peer(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                                  uint32_t rank) {
+    uint32_t rdst, rbar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rdst) : "r"(smem_u32(dst)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(rdst), "r"(smem_u32(src)), "r"(bytes), "r"(rbar)
+                 : "memory");
+}
+// Wait for a phase of a local mbarrier with acquire at cluster scope (other CTAs' released writes become
+// visible); false after kWaitTimeoutNs.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_spin_cluster(uint64_t *bar, uint32_t parity) {
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_test_wait_cluster(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
