@@ -426,10 +426,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     // this grid has left; it waits for this grid before reading the workspace
     if (tid == 0) grid_launch_dependents();
 
-    if (warp == 0) {
-        tmem_alloc(&tmem_slot, PREP_TMEM_COLS);
-        tmem_relinquish();
-    }
+    // Thread 0 requests the tiles first (their latency is the longest); warp 2 allocates TMEM meanwhile.
     if (tid == 0) {
         mbar_init(&bar_tma, 1);
         mbar_init(&bar_mma, 1);
@@ -443,6 +440,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 tma_load_2d(sm + PREP_KQ + kb * 16384 + 8192, &qmap, &bar_tma, hq * D + kb * 64, t0);
             }
         }
+    }
+    if (warp == 2) {
+        tmem_alloc(&tmem_slot, PREP_TMEM_COLS);
+        tmem_relinquish();
     }
     float *g_s = reinterpret_cast<float *>(sm + PREP_G);  // [64]
     float *b_s = g_s + 64;                                // [64]
@@ -767,7 +768,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, PREP_TMEM_COLS);
+    if (warp == 2) tmem_dealloc(tmem, PREP_TMEM_COLS);
 }
 
 // ============================================================================
@@ -942,7 +943,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     uint8_t *sm = align1024(pass_raw);
     __shared__ uint64_t bar_qk[2], bar_p[2], bar_r[2], bar_qkf[2], bar_pf[2], bar_rf[2];
     __shared__ uint64_t bar_s, bar_x[2], bar_d1, bar_px, bar_rx[2];
-    __shared__ uint64_t bar_norm[2];
+    __shared__ uint64_t bar_norm[2];   // (NORM) the peers' sums of a chunk have landed, by chunk parity
+    __shared__ uint32_t nsum_count;    // (NORM) Q-row threads that have written their sums, over all chunks so far
     // [chunk parity][cluster rank][row group][token]; the bulk copies need 16-byte aligned blocks
     __shared__ __align__(128) float norm_part[NORM ? 2 * 4 * NG * 64 : 4];
     __shared__ uint32_t tmem_slot;
@@ -1006,6 +1008,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             mbar_init(&bar_norm[1], 1);
         }
         abort_flag = 0;
+        nsum_count = 0;
         fence_mbar_init();
     }
     tc_fence_before();
@@ -1247,9 +1250,12 @@ state_pass_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 constexpr uint32_t kBlock = NG * 64 * 4;   // one CTA's sums of a chunk, bytes
                 float *mine = norm_part + (np * 4 + (int)crank) * NG * 64;
                 mine[grp * 64 + i] = ss;
-                fence_proxy_async_smem();                          // read by the bulk copies
-                asm volatile("bar.sync 1, 128;" ::: "memory");    // the Q-row threads (warps 0, 1, 4, 5)
-                if (tid == 0) {
+                fence_proxy_async_smem();   // read by the bulk copies
+                // The last of the 128 Q-row threads to count itself in (acquire-release: every other thread's
+                // sums and proxy fence come before) sends.  Nobody waits here: a named barrier would block for
+                // good on a thread whose own bounded wait ran out and left the loop, while a missing count only
+                // means no send, and the peers' waits, then this CTA's own, run out in turn.
+                if (count_in_shared(&nsum_count) == 128u * (uint32_t)(j + 1) - 1u) {
 #pragma unroll
                     for (uint32_t rk = 0; rk < 4; ++rk)
                         if (rk != crank) bulk_copy_to_peer(mine, mine, kBlock, &bar_norm[np], rk);

@@ -114,6 +114,12 @@ __device__ __forceinline__ float ld_dsmem_f32(const float *p, uint32_t rank) {
     return v;
 }
 
+// Add one to a shared-memory counter with acquire-release ordering at CTA scope; returns the prior value.
+__device__ __forceinline__ uint32_t count_in_shared(uint32_t *ctr) {
+    uint32_t prior;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(prior) : "r"(smem_u32(ctr)) : "memory");
+    return prior;
+}
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's shared memory at src
 // to the same offset as dst in CTA `rank` of the cluster, completing its bytes on the mbarrier at bar's offset
 // in that CTA.
