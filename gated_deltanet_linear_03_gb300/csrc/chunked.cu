@@ -922,10 +922,11 @@ constexpr uint32_t kPTx = 16384 + 16384, kRTx = 8192 + 8192;
 // NORM: the output normalisation o <- o / sqrt(mean_head(o^2) + eps) * w over the head's 128 rows, which the
 // four slice CTAs of a (bucket, head) hold 32 each; they form a cluster.  Per chunk every Q-row thread writes
 // its token's sum of squares over its 16 rows into its CTA's block of the slot array (two slot sets by chunk
-// parity); after a named barrier of the 128 Q-row threads one of them sends the block (512 bytes) to the same
-// place in each peer CTA with a bulk copy that completes on the peer's norm barrier, and arms its own barrier
-// for the three peers' blocks.  Every Q-row thread then waits on its own barrier and adds its token's eight
-// sums.  Only the Q-row threads take part, so the MMA and tile warps never wait on the cluster.  A slot set is
+// parity); the last of the 128 Q-row threads to count itself in (a shared counter) sends the block (512 bytes)
+// to the same place in each peer CTA with a bulk copy that completes on the peer's norm barrier, and arms its
+// own barrier for the three peers' blocks.  After the state update every Q-row thread waits on its own barrier
+// and adds its token's eight sums.  Only the Q-row threads take part, so the MMA and tile warps never wait on
+// the cluster, and the wait is off the state chain.  A slot set is
 // written again two chunks later: by then the peers have received this CTA's block of the chunk in between,
 // which it sends only after reading; the barrier's phases advance the same way, so they never alias.
 template <bool GATE, bool MULTI, bool NORM>
