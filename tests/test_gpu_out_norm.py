@@ -115,3 +115,34 @@ def test_prefill_output_norm_noalloc_and_phases(gdn):
     plan.run_phase("pass")
     torch.cuda.synchronize()
     check_prefill(plan.out, plan.final_state, ref_out, ref_fin, what="phases norm")
+
+
+# The chunked pass carries the norm in every form the host can pick: many short sequences (several per CTA,
+# with raw gates: the multi-sequence, gated instantiation), eight long ones (one sequence per CTA: 1024
+# four-CTA clusters over several waves), both with raw q/k and bf16 outputs as a model would run them.
+NORM_PASS_FORMS = {
+    "many_short_raw_gates": ([37, 0, 129, 64, 1, 300, 65, 2, 90, 17, 250, 3], dict(raw_gates="per_head")),
+    "eight_long": ([600, 520, 700, 513, 640, 600, 530, 610], {}),
+}
+
+
+@pytest.mark.parametrize("form", list(NORM_PASS_FORMS))
+def test_chunked_norm_every_pass_form(gdn, form):
+    lengths, extra = NORM_PASS_FORMS[form]
+    inp = synth.prefill_inputs(lengths, seed=68, init_std=0.02, raw_qk=True, **extra)
+    w = weight(128, 69)
+    kw = dict(qk_norm=True, q_scale=1.0 / np.sqrt(128), norm_weight=w.numpy(), norm_eps=1e-6)
+    gk = {}
+    if inp.gate_scale is not None:
+        kw.update(gate_scale=inp.gate_scale.numpy(), gate_bias=inp.gate_bias.numpy())
+        gk = dict(gate_scale=inp.gate_scale.cuda(), gate_bias=inp.gate_bias.cuda())
+    from helpers import oracle_args, to_device
+    ref_out, ref_fin = oracle.prefill(*oracle_args(inp), **kw)
+    dv_ = to_device(inp)
+    kw.update(norm_weight=w.cuda(), **gk)
+    out, fin = gdn.prefill(dv_.q, dv_.k, dv_.v, dv_.log_alpha, dv_.beta, dv_.cu_seqlens, init_state=dv_.init_state,
+                           out_dtype=torch.bfloat16, algo="chunked", cu_seqlens_host=inp.cu_seqlens.tolist(), **kw)
+    torch.cuda.synchronize()
+    assert gdn.device_error() == 0
+    assert bf16_ok(out, ref_out), f"{form}: bf16 normalised outputs"
+    assert state_rel_err(fin, ref_fin) <= STATE_RTOL, f"{form}: final state"
