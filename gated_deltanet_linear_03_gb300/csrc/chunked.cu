@@ -1546,6 +1546,14 @@ long total_chunks(int n_seqs, const int32_t *cu_host) {
 
 }  // namespace
 
+int plan_state_pass(int n_seqs, const int32_t *cu_host, int hv, int sms, int *first_seq, int capacity) {
+    PassBuckets bk;
+    const int nb = pass_buckets(bk, n_seqs, cu_host, total_chunks(n_seqs, cu_host), hv, sms);
+    if (capacity < nb + 1) return -1;
+    for (int b = 0; b <= nb; ++b) first_seq[b] = bk.per_seq ? b : bk.seq[b];
+    return nb;
+}
+
 size_t chunked_workspace_bytes(int n_seqs, const int32_t *cu_host, int hv, int d) {
     if (d != D) return 0;
     const long nch = total_chunks(n_seqs, cu_host);

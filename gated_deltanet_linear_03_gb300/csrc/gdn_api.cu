@@ -153,6 +153,13 @@ int gdn_prefill_algo(int n_seqs, int total_tokens, int hk, int hv, int dk, int d
     return resolve_auto(n_seqs, hv, dk, cu_seqlens_host);
 }
 
+int gdn_prefill_pass_plan(int n_seqs, int total_tokens, int hv, const int32_t *cu_seqlens_host, int multiprocessors,
+                          int *bucket_first_seq, int capacity) {
+    if (hv < 1 || multiprocessors < 1 || !bucket_first_seq || check_cu(n_seqs, total_tokens, cu_seqlens_host) != GDN_OK)
+        return -1;
+    return gdn::plan_state_pass(n_seqs, cu_seqlens_host, hv, multiprocessors, bucket_first_seq, capacity);
+}
+
 size_t gdn_prefill_workspace_size(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
                                   const int32_t *cu_seqlens_host, int algo, gdn_status *status) {
     gdn_status st = check_heads(hk, hv, dk, dv);

@@ -119,5 +119,8 @@ cudaError_t launch_short_prefill(const PrefillProblem &p);
 // phases: bit 0 = per-chunk preparation, bit 1 = state passing + outputs
 cudaError_t launch_chunked_prefill(const PrefillProblem &p, int phases);
 size_t chunked_workspace_bytes(int n_seqs, const int32_t *cu_host, int hv, int d);
+// The state pass's buckets for `sms` multiprocessors: first_seq[0..nb] (bucket b carries sequences
+// [first_seq[b], first_seq[b + 1])); returns nb, or -1 when capacity < nb + 1.  Host only.
+int plan_state_pass(int n_seqs, const int32_t *cu_host, int hv, int sms, int *first_seq, int capacity);
 
 }  // namespace gdn

@@ -24,7 +24,8 @@ DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 # every symbol include/gdn.h declares
 EXPORTS = ("gdn_prefill", "gdn_prefill_chunked_phase", "gdn_prefill_workspace_size", "gdn_decode_step",
            "gdn_device_error", "gdn_status_string", "gdn_version", "gdn_prefill_noalloc", "gdn_prefill_algo",
-           "gdn_prefill_host", "gdn_prefill_host_staging_size", "gdn_selftest_bounded_wait")
+           "gdn_prefill_host", "gdn_prefill_host_staging_size", "gdn_selftest_bounded_wait",
+           "gdn_prefill_pass_plan")
 NOALLOC_SCRATCH_BYTES = 97 * 1024 * 1024
 PHASE = {"prep": 1, "pass": 2}
 
@@ -72,6 +73,8 @@ def bind(path: str) -> ctypes.CDLL:
     lib.gdn_prefill_host_staging_size.restype = Z
     lib.gdn_prefill_algo.argtypes = [I, I, I, I, I, I, P]
     lib.gdn_prefill_algo.restype = I
+    lib.gdn_prefill_pass_plan.argtypes = [I, I, I, P, I, P, I]
+    lib.gdn_prefill_pass_plan.restype = I
     lib.gdn_decode_step.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, I, ctypes.c_float, P, ctypes.c_float, P,
                                     P, P]
     lib.gdn_decode_step.restype = I
@@ -148,6 +151,18 @@ def resolve_algo(n_seqs: int, total_tokens: int, hk: int, hv: int, dk: int, dv: 
     if a < 0:
         raise GdnError(1, "gdn_prefill_algo")
     return {v: k for k, v in ALGO.items()}[a]
+
+
+def pass_plan(cu_seqlens_host: Sequence[int], hv: int, multiprocessors: int = 152) -> list:
+    """The state pass's buckets (``gdn_prefill_pass_plan``): the first sequence of each bucket, then n_seqs."""
+    lib = load_library()
+    n = len(cu_seqlens_host) - 1
+    arr = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+    out = (ctypes.c_int * (n + 1))()
+    nb = lib.gdn_prefill_pass_plan(n, int(cu_seqlens_host[-1]), hv, arr, multiprocessors, out, n + 1)
+    if nb < 1:
+        raise GdnError(1, "gdn_prefill_pass_plan")
+    return list(out[:nb + 1])
 
 
 def workspace_size(n_seqs: int, total_tokens: int, hk: int, hv: int, dk: int, dv: int,

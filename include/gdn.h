@@ -205,7 +205,7 @@ GDN_API size_t gdn_prefill_workspace_size(int n_seqs, int total_tokens, int hk, 
  * value heads):
  *   - the scan when the longest sequence has at most 16 tokens, or at most 32
  *     tokens with n_seqs * hv <= 64 (the chunked path pays a fixed cost of
- *     about 13 us for one short sequence and 45 us for eight);
+ *     about 12 us for one short sequence and 34 us for eight);
  *   - the scan whenever dk != 128 (the chunked path implements d = 128 only);
  *   - the chunked path otherwise.
  * It needs no CUDA call.  gdn_prefill and gdn_prefill_workspace_size apply the
@@ -213,6 +213,30 @@ GDN_API size_t gdn_prefill_workspace_size(int n_seqs, int total_tokens, int hk, 
  */
 GDN_API int gdn_prefill_algo(int n_seqs, int total_tokens, int hk, int hv, int dk, int dv,
                              const int32_t *cu_seqlens_host);
+
+/*
+ * gdn_prefill_pass_plan: how the chunked path's state pass groups the
+ * sequences into buckets, for inspection.  A bucket is a run of consecutive
+ * sequences that one state-pass CTA per (value head, 32-row slice) carries one
+ * after another; the chunks of one sequence are sequential ("Optimizing
+ * on-device inference for Apple Silicon", section "Qwen creates three workload
+ * shapes": the blocked form still passes the state from chunk to chunk).  The
+ * plan is the one gdn_prefill makes on a device with `multiprocessors` SMs
+ * (152 on GB300): either one wave of buckets of several sequences each, or one
+ * bucket per sequence, whichever a chunk-count cost estimate favours.
+ *
+ *   cu_seqlens_host    int32 [n_seqs + 1] host array, as for gdn_prefill
+ *   bucket_first_seq   host array of `capacity` ints; on success entries
+ *                      [0, nb] hold the buckets' first sequences followed by
+ *                      n_seqs (bucket b carries sequences [bucket_first_seq[b],
+ *                      bucket_first_seq[b + 1])).  n_seqs + 1 entries always
+ *                      suffice.
+ *
+ * Returns nb >= 1, or -1 when an argument is invalid or capacity < nb + 1.  It
+ * needs no CUDA call.
+ */
+GDN_API int gdn_prefill_pass_plan(int n_seqs, int total_tokens, int hv, const int32_t *cu_seqlens_host,
+                                  int multiprocessors, int *bucket_first_seq, int capacity);
 
 /*
  * gdn_decode_step: one token for each of n independent states (batch-1 decode
