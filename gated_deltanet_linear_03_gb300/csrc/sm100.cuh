@@ -102,9 +102,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;" ::: "memory");
 }
-// The two halves of cluster_sync, for threads that arrive early and wait later.
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 // A float at the same shared-memory offset in CTA `rank` of the cluster (distributed shared memory).
 __device__ __forceinline__ float ld_dsmem_f32(const float *p, uint32_t rank) {
     uint32_t remote;
